@@ -1,0 +1,456 @@
+"""Benchmark of the rotated INT2 paged KV-cache hot path on GB300.
+
+One step = one pass of the whole hot path over one batch: rotate the n_new new key /
+value rows per sequence and the decode queries (kv_rotate_qk), quantize-on-write flush
+(kv_quant_flush), GQA decode attention over the mixed cache (kv_attn_decode).  The cache
+is built once (untimed); before every timed step the cache's seq_len / s_quant are reset
+to the pre-step state and L2 is flushed by a 512 MB memset (both untimed), so every step
+does identical work from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+Prints one JSON line (rank 0).  Multi-GPU runs are independent replicas, one per rank
+(weak scaling): the decode units (sequence, kv head) need no exchange.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "INT2 paged decode attention: effective HBM GB/s (% of ~8 TB/s), tokens/s"
+UNIT = "GB/s"
+DEFAULT_CONFIG = 2
+NOMINAL_HBM_GBS = 7900.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---- algorithmic bytes ---------------------------------------------------------------------
+def step_bytes(w: synth.Workload, ctx: np.ndarray, sq_before: np.ndarray, sq_after: np.ndarray) -> dict:
+    """Minimum bytes one step must move (per the cache layout): decode reads + the
+    rotate / flush traffic of the new tokens."""
+    d, hkv, g, B = w.head_dim, w.n_kv_heads, w.gqa, w.batch
+    ng = d // w.group_size
+    int2_tok = 2 * (d // 4) + 2 * 4 * ng + (2 if w.key_l2norm else 0)
+    L = ctx + w.n_new
+    dec_int2 = dec_win = ptab = 0
+    for Lb, sqb in zip(L, sq_after):
+        Lb, sqb = int(Lb), int(sqb)
+        n_int2 = max(0, min(sqb, Lb) - w.s_sink)
+        n_win = min(w.s_sink, Lb) + max(0, Lb - max(sqb, w.s_sink))
+        dec_int2 += n_int2 * hkv * int2_tok
+        dec_win += n_win * hkv * 4 * d
+        ptab += -(-n_int2 // w.page_size) * 4
+    qb = B * w.n_q_heads * d * 2
+    decode = dec_int2 + dec_win + ptab + qb + B * w.n_q_heads * d * 4
+    n_new_rows = B * w.n_new * hkv
+    mats = 0
+    if w.transform != "hadamard":
+        mats += 2 * hkv * d * d * 4                  # T_K (keys) and T_K^{-T} (queries)
+    if w.value_transform != "identity":
+        mats += hkv * d * d * 4
+    rotate = mats + 2 * qb + 2 * n_new_rows * d * 2 * 2
+    n_fl = int(np.sum(sq_after - sq_before)) * hkv
+    flush = n_fl * (2 * d * 2 + int2_tok)
+    return {"decode": int(decode), "decode_int2": int(dec_int2), "decode_window": int(dec_win),
+            "rotate": int(rotate), "flush": int(flush), "total": int(decode + rotate + flush)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            j = json.load(open(p))
+            return float(j["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attn.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "bit_rotated_kv_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        j = json.load(open(p))
+        e = j.get(workload)
+        if e and e.get("kernel_hash") == kernel_hash():
+            return int(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+    return None
+
+
+# ---- clocks --------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._thr = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                      "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                                     timeout=5).stdout.strip()
+                if out:
+                    self.samples.append((time.time(), out))
+            except Exception:
+                pass
+            self._stop.wait(0.1)
+
+    def start(self):
+        self._thr = threading.Thread(target=self._run, daemon=True)
+        self._thr.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thr:
+            self._thr.join(timeout=10)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- the GPU arm ----------------------------------------------------------------------------
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    import bit_rotated_kv_gb300 as kvq
+    from tests import harness
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synth.CONFIGS[args.config]
+    run = harness.GpuRun(w, device=dev, do_step=False, ring_extra=max(1024, w.n_new))
+    r = run.runner
+    stream = torch.cuda.current_stream()
+    seq0, sq0 = r.cache.seq_len.clone(), r.cache.s_quant.clone()
+    k_new, v_new, sidx, pos = r.step_inputs(run.k_all, run.v_all, run.lengths, w.n_new)
+    q = run.q
+    ctx = run.lengths
+    sq_before = sq0.cpu().numpy().astype(np.int64)
+    sq_after = np.array([synth_sq(w, int(c)) for c in ctx], np.int64)
+    nbytes = step_bytes(w, ctx, sq_before, sq_after)
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def reset():
+        r.cache.seq_len.copy_(seq0)
+        r.cache.s_quant.copy_(sq0)
+        flush_buf.zero_()
+
+    def step(ev=None):
+        # ev: (after rotate, after flush) events, or None
+        r.append(k_new, v_new, sidx, pos, q, r.q_out)
+        if ev is not None:
+            ev[0].record(stream)
+        r.flush(w.n_new + w.s_flush)
+        if ev is not None:
+            ev[1].record(stream)
+        r.decode(r.q_out, r.out)
+
+    # warm-up (untimed)
+    for _ in range(args.warmup):
+        reset()
+        step()
+    torch.cuda.synchronize()
+    if int(r.status.item()) != 0:
+        raise RuntimeError(f"device status {int(r.status.item())}")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    # clock soak: keep the GPU on this step while the sampler warms up (untimed)
+    t_end = time.time() + args.soak
+    while time.time() < t_end:
+        for _ in range(50):
+            reset()
+            step()
+        torch.cuda.synchronize()
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_s, ev_r, ev_f, ev_e = mk(), mk(), mk(), mk()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        reset()
+        ev_s[i].record(stream)
+        step((ev_r[i], ev_f[i]))
+        ev_e[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.stop()
+    avg = lambda a, b: sum(a[i].elapsed_time(b[i]) for i in range(args.steps)) / args.steps
+    t_step = avg(ev_s, ev_e)
+    t_dec = avg(ev_f, ev_e)
+    kernel_ms = {"kv_rotate_qk": round(avg(ev_s, ev_r), 5), "kv_quant_flush": round(avg(ev_r, ev_f), 5),
+                 "kv_attn_decode": round(t_dec, 5)}
+    t_step_max = allreduce_max(t_step, world)
+    status = int(r.status.item())
+
+    # ---- end to end through the C ABI with host buffers: H2D of the step's inputs from
+    # pinned memory, the three calls, D2H of the attention output, every step
+    h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    h_s, h_p, h_q = sidx.cpu().pin_memory(), pos.cpu().pin_memory(), q.cpu().pin_memory()
+    h_out = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
+    d_k, d_v, d_s, d_p, d_q = (torch.empty_like(x, device=dev) for x in (h_k, h_v, h_s, h_p, h_q))
+    h2d = sum(x.numel() * x.element_size() for x in (h_k, h_v, h_s, h_p, h_q))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_k.copy_(h_k, non_blocking=True); d_v.copy_(h_v, non_blocking=True)
+        d_s.copy_(h_s, non_blocking=True); d_p.copy_(h_p, non_blocking=True); d_q.copy_(h_q, non_blocking=True)
+        r.append(d_k, d_v, d_s, d_p, d_q, r.q_out)
+        r.flush(w.n_new + w.s_flush)
+        r.decode(r.q_out, r.out)
+        h_out.copy_(r.out, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        reset()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        reset()
+        torch.cuda.synchronize()
+        s_ev = torch.cuda.Event(enable_timing=True); e_ev = torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)
+        e2e_step()
+        e_ev.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(s_ev.elapsed_time(e_ev))
+    t_e2e = allreduce_max(sum(e2e_ms) / len(e2e_ms), world)
+
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes["decode"] / (t_dec * 1e-3) / 1e9
+    value = world * nbytes["total"] / (t_step_max * 1e-3) / 1e9
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step_max, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int2 codes x f16 tensor-core MMA, f32 accumulate",
+        "data": "synthetic (seeded; shapes of the pages' Qwen3 workloads, random transforms)",
+        "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+                   "head_dim": w.head_dim, "context": int(ctx.max()) + w.n_new, "n_new_tokens": w.n_new,
+                   "group_size": w.group_size, "kappa": [w.kappa_k, w.kappa_v],
+                   "windows_sink_keep_flush": [w.s_sink, w.s_keep, w.s_flush], "transform": w.transform,
+                   "l2": "flushed between timed steps (512 MB memset, untimed)",
+                   "bytes_per_step": nbytes, "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * w.batch / (t_step_max * 1e-3), 1),
+        "hbm_frac_of_nominal_8tbs": round(value / NOMINAL_HBM_GBS, 4),
+        "roofline": {"kernel": "kv_attn_decode", "bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s", "traffic": profiled_traffic(w.name),
+                     "decode_ms": round(t_dec, 5), "bytes_per_launch": nbytes["decode"]},
+        "e2e": {"value": round(world * nbytes["total"] / (t_e2e * 1e-3) / 1e9, 2), "unit": UNIT,
+                "ms_per_step": round(t_e2e, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "kernel_ms": kernel_ms,
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(),
+        "device_status": status,
+    }
+    return res
+
+
+def synth_sq(w, ctx: int) -> int:
+    s = w.s_sink
+    L = ctx
+    while L - s >= w.s_keep + w.s_flush:
+        s += w.s_flush
+    L += w.n_new
+    while L - s >= w.s_keep + w.s_flush:
+        s += w.s_flush
+    return s
+
+
+# ---- CPU baseline: the oracle as it stands on a bounded sample -----------------------------
+def oracle_step_sample(config: int, budget_s: float) -> dict:
+    """Time the oracle's step work (rotate the new rows and queries, quantize the flushed
+    tokens, dequantize the cache, float64 attention) on whole (sequence, kv head) units of
+    the workload until about budget_s of CPU time has been spent; returns GB/s equivalent."""
+    from oracle import attention, cache, quant, transform
+    from oracle.fp import bf16_to_f32, f32_to_bf16_bits
+    w = synth.CONFIGS[config]
+    tk, tkit, tv = synth.transforms(w)
+    lengths = synth.context_lengths(w)
+    ctx = lengths
+    sq_b = np.array([synth_sq(w.replace(n_new=0), int(c)) for c in ctx])
+    sq_a = np.array([synth_sq(w, int(c)) for c in ctx])
+    full = step_bytes(w, ctx, sq_b, sq_a)["total"]
+    units = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)]
+    per_unit = full / len(units)
+    done = 0
+    spent = 0.0
+    i = 0
+    while spent < budget_s and i < 4 * len(units):
+        b, h = units[i % len(units)]
+        i += 1
+        ui = synth.unit_inputs(w, b, h, lengths)
+        L = ui.ctx + w.n_new
+        kind = "hadamard" if w.transform == "hadamard" else "dense"
+        # state before the step (untimed): rotated rows and quantized cache of the context
+        k_rot = f32_to_bf16_bits(transform.rotate_rows(None if tk is None else tk[h], ui.k[:ui.ctx], kind))
+        v_rot = f32_to_bf16_bits(transform.rotate_rows(None if tv is None else tv[h], ui.v[:ui.ctx]))
+        sqb = int(sq_b[b])
+        unit = cache.build_unit(k_rot, v_rot, ui.ctx, sqb, s_sink=w.s_sink, group=w.group_size,
+                                kappa_k=w.kappa_k, kappa_v=w.kappa_v, quantizer=w.quantizer,
+                                alpha=w.quest_alpha, key_l2norm=w.key_l2norm)
+        t0 = time.process_time()
+        # the step: rotate new rows + queries, flush, dequantize the cache, attend
+        kn = f32_to_bf16_bits(transform.rotate_rows(None if tk is None else tk[h], ui.k[ui.ctx:L], kind))
+        vn = f32_to_bf16_bits(transform.rotate_rows(None if tv is None else tv[h], ui.v[ui.ctx:L]))
+        qr = transform.rotate_rows(None if tkit is None else tkit[h], ui.q, kind)
+        k_all = np.concatenate([k_rot, kn])
+        v_all = np.concatenate([v_rot, vn])
+        sqa = cache.flush(L, sqb, w.s_keep, w.s_flush)
+        kh = bf16_to_f32(k_all).astype(np.float64)
+        vh = bf16_to_f32(v_all).astype(np.float64)
+        lo = min(w.s_sink, L)
+        if sqb > lo:
+            kh[lo:sqb] = quant.dequantize(unit["qk"])
+            vh[lo:sqb] = quant.dequantize(unit["qv"])
+        if sqa > sqb:
+            kh[sqb:sqa] = quant.dequantize(quant.quantize_rows(k_all[sqb:sqa], w.group_size, w.kappa_k, w.quantizer,
+                                                               w.quest_alpha, w.key_l2norm))
+            vh[sqb:sqa] = quant.dequantize(quant.quantize_rows(v_all[sqb:sqa], w.group_size, w.kappa_v, w.quantizer,
+                                                               w.quest_alpha, False))
+        attention.decode(qr.astype(np.float64), kh, vh, 1.0 / math.sqrt(w.head_dim))
+        spent += time.process_time() - t0
+        done += 1
+    gbs = done * per_unit / spent / 1e9
+    return {"value": gbs, "units": done, "seconds": spent, "workload": w.name}
+
+
+def cpu_baseline(config: int, budget_s: float) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"print(json.dumps(bench.oracle_step_sample({config}, {budget_s})))")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=1800)
+    if out.returncode:
+        raise RuntimeError(out.stderr[-2000:])
+    j = json.loads(out.stdout.strip().splitlines()[-1])
+    return {"value": round(j["value"], 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{j['units']} (sequence, kv head) units of {j['workload']}: rotate new rows + queries, "
+                      f"quantize flushed tokens, dequantize cache, float64 attention; {j['seconds']:.1f} s CPU, "
+                      f"1 thread"}
+
+
+# ---- distributed helpers --------------------------------------------------------------------
+_PG = None
+
+
+def init_dist():
+    global _PG
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if _cuda_ok() else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        _PG = dist
+    return rank, world, local
+
+
+def _cuda_ok():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def barrier(world):
+    if world > 1 and _PG is not None:
+        _PG.barrier()
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world > 1 and _PG is not None:
+        import torch
+        dev = torch.device("cuda", torch.cuda.current_device()) if _cuda_ok() else torch.device("cpu")
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        _PG.all_reduce(t, op=_PG.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds on the step while clocks are sampled")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = init_dist()
+    if args.impl == "reference":
+        if rank == 0:
+            cb = cpu_baseline(args.config, args.cpu_budget)
+            w = synth.CONFIGS[args.config]
+            res = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
+                   "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+                   "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+                   "config": {"workload": w.name}, "cpu_baseline": cb,
+                   "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            print(json.dumps(res), flush=True)
+        return
+    res = run_ours(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(args.config, args.cpu_budget)
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

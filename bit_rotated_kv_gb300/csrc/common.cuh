@@ -1,0 +1,96 @@
+// Shared device helpers of the rotated INT2 KV-cache library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 16;
+constexpr int kCodeBytes = 512;      // 16 tokens x 128 channels x 2 bits, per K or V
+constexpr int kMaxGqa = 8;
+
+// Bytes of one (page, kv head) chunk: K codes, V codes, K scales, V scales, [K norms],
+// padded to 32 bytes.
+__host__ __device__ inline int page_head_bytes(int group_size, int key_l2norm) {
+  int ng = kHeadDim / group_size;
+  int b = 2 * kCodeBytes + 2 * kPage * ng * 4 + (key_l2norm ? kPage * 2 : 0);
+  return (b + 31) / 32 * 32;
+}
+__host__ __device__ inline int k_scale_off() { return 2 * kCodeBytes; }
+__host__ __device__ inline int v_scale_off(int ng) { return 2 * kCodeBytes + kPage * ng * 4; }
+__host__ __device__ inline int norm_off(int ng) { return 2 * kCodeBytes + 2 * kPage * ng * 4; }
+
+// First device fault wins; never traps.
+__device__ __forceinline__ void set_status(int32_t* st, int code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// ---- error-free float arithmetic (no contraction: explicit _rn intrinsics) ----------
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  float bb = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  e = __fsub_rn(b, __fsub_rn(s, a));
+}
+// (hi, lo) += a * b, keeping the product's rounding error.
+__device__ __forceinline__ void ff_mac(float& hi, float& lo, float a, float b) {
+  float p = __fmul_rn(a, b);
+  float pe = __fmaf_rn(a, b, -p);
+  float s, e;
+  two_sum(hi, p, s, e);
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(e, pe));
+}
+__device__ __forceinline__ void ff_add(float ah, float al, float bh, float bl, float& sh, float& sl) {
+  float s, e;
+  two_sum(ah, bh, s, e);
+  e = __fadd_rn(e, __fadd_rn(al, bl));
+  fast_two_sum(s, e, sh, sl);
+}
+
+// Round the double-float value hi + lo (|lo| <= ulp(hi)/2 after fast_two_sum) to bf16,
+// nearest-even, deciding exact float32 ties by the sign of lo.
+__device__ __forceinline__ uint16_t ff_to_bf16(float hi, float lo) {
+  float h, l;
+  fast_two_sum(hi, lo, h, l);
+  uint32_t b = __float_as_uint(h);
+  if ((b & 0x7f800000u) == 0x7f800000u) {                      // inf / nan
+    return (uint16_t)((b >> 16) | ((b & 0x007fffffu) ? 0x40u : 0u));
+  }
+  uint32_t rem = b & 0xffffu;
+  uint32_t up = b >> 16;
+  if (rem > 0x8000u) {
+    up += 1;
+  } else if (rem == 0x8000u) {
+    if (l != 0.0f) {
+      if ((l > 0.0f) == (h > 0.0f)) up += 1;                     // beyond the midpoint
+    } else {
+      up += (up & 1u);                                           // exact tie: to even
+    }
+  }
+  return (uint16_t)up;
+}
+
+// float64 -> float16, nearest-even, in one rounding: round to odd into float32 first
+// (24 >= 11 + 2 bits keeps the final rounding correct), then float32 -> float16.
+__device__ __forceinline__ __half double_to_half_rn(double d) {
+  float f = __double2float_rz(d);
+  if ((double)f != d && isfinite(d) && fabs(d) < 3.0e38) {
+    uint32_t u = __float_as_uint(f) | 1u;
+    f = __uint_as_float(u);
+  }
+  return __float2half_rn(f);
+}
+
+}  // namespace kvq

@@ -1,0 +1,296 @@
+// kv_quant_flush: quantize-on-write of tokens leaving the BF16 recent window into
+// INT2 pages (per token, per group: range -> Delta16, z16 -> 2-bit codes).
+//
+// Source: WUSH-KV digest, inference algorithm (maintain S_quant; quantize S_flush-
+// aligned spans beyond S_sink / S_keep in place; per-group QuEST or kappa-quantile
+// affine quantizer); OSCAR summary, section 3 "Scale Determination and Clipping"
+// (per-token affine scale + zero point, percentile clipping) and section 4 "KV Cache
+// Update" (demotion reuses the clip-quantize step); OScaR reading note, "整数量化基础"
+// (Q(x), Delta = (max - min)/(2^b - 1)), KIVI background (z = -min/Delta) and step 2
+// "Omni-Token Scaling" (s = ||k||, k / s quantized, s stored).
+//
+// Design (GB300): one warp per (token, kv head) handles its key row and value row;
+// lane l owns channels 4l..4l+3, a group of G channels is G/4 lanes.  The quantile
+// needs only a few order statistics near the ends, found by repeated warp-level max
+// (min) extraction with exact tie handling -- no sort.  Codes are staged in shared
+// memory and re-packed into the MMA-fragment layout the decode kernel reads with one
+// 128-bit load per thread.  Every float operation is an explicit IEEE round-to-nearest
+// intrinsic, so the results are bit-identical to the float32 / float64 definition.
+#include "common.cuh"
+#include "launch.h"
+
+namespace kvq {
+
+struct FlushParams {
+  uint8_t* pages;
+  const int32_t* page_table;
+  const int32_t* seq_len;
+  int32_t* s_quant;
+  const uint16_t* ring_k;
+  const uint16_t* ring_v;
+  int32_t* counters;
+  int32_t* status;
+  int batch, hkv, s_sink, s_keep, s_flush, ring_cap, max_pages, num_pages, max_tokens;
+  int group, quantizer, l2, page_bytes, tokens_per_cta;
+  int i_lo[2], i_hi[2], n_lo[2], n_hi[2];   // [0] keys, [1] values
+  float f_lo[2], f_hi[2];
+  double alpha;
+};
+
+__device__ __forceinline__ void sort4(float& a, float& b, float& c, float& d) {
+  float t;
+  t = fminf(a, b); b = fmaxf(a, b); a = t;
+  t = fminf(c, d); d = fmaxf(c, d); c = t;
+  t = fminf(a, c); c = fmaxf(a, c); a = t;
+  t = fminf(b, d); d = fmaxf(b, d); b = t;
+  t = fminf(b, c); c = fmaxf(b, c); b = t;
+}
+
+// Extract n values from the top (largest first) of the group's 4*NL values; returns the
+// last two extracted: cur = n-th largest, prev = (n-1)-th largest.
+template <bool TOP>
+__device__ __forceinline__ void extract(const float s[4], int n, int nl, unsigned gmask, int lane,
+                                        float& cur, float& prev) {
+  int ptr = TOP ? 3 : 0;
+  float cand = TOP ? s[3] : s[0];
+  cur = prev = cand;
+  for (int it = 0; it < n; ++it) {
+    float m = cand;
+    for (int o = nl >> 1; o > 0; o >>= 1) {
+      float other = __shfl_xor_sync(0xffffffffu, m, o);
+      m = TOP ? fmaxf(m, other) : fminf(m, other);
+    }
+    unsigned bal = __ballot_sync(0xffffffffu, cand == m) & gmask;
+    int owner = __ffs(bal) - 1;
+    if (lane == owner) {
+      ptr += TOP ? -1 : 1;
+      float inf = TOP ? -INFINITY : INFINITY;
+      cand = (ptr == 0) ? s[0] : (ptr == 1) ? s[1] : (ptr == 2) ? s[2] : (ptr == 3) ? s[3] : inf;
+    }
+    prev = cur;
+    cur = m;
+  }
+}
+
+// Quantize one row held as 4 float32 values per lane; writes 4 codes per lane into cbuf
+// (one byte per channel) and returns the group's Delta16 / z16 in dz (valid on all lanes).
+__device__ __forceinline__ void quant_row(const FlushParams& P, int which, const float y[4], int lane,
+                                          uint8_t* cbuf, __half2& dz, bool& bad) {
+  const int nl = P.group >> 2;
+  const unsigned gmask = nl == 32 ? 0xffffffffu : (((1u << nl) - 1u) << (lane & ~(nl - 1)));
+  __half d16, z16;
+  if (P.quantizer == KVQ_QUANT_AFFINE_KAPPA) {
+    float s[4] = {y[0], y[1], y[2], y[3]};
+    sort4(s[0], s[1], s[2], s[3]);
+    float hc, hp, lc, lp;
+    extract<true>(s, P.n_hi[which], nl, gmask, lane, hc, hp);
+    extract<false>(s, P.n_lo[which], nl, gmask, lane, lc, lp);
+    const int g = P.group;
+    float hi = (P.i_hi[which] >= g - 1) ? hc
+                                        : __fadd_rn(hc, __fmul_rn(P.f_hi[which], __fsub_rn(hp, hc)));
+    float lo = (P.i_lo[which] >= g - 1) ? lc
+                                        : __fadd_rn(lp, __fmul_rn(P.f_lo[which], __fsub_rn(lc, lp)));
+    float delta = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+    d16 = __float2half_rn(delta);
+    if (__half2float(d16) == 0.0f) d16 = __float2half_rn(1.0f);
+    float z = -__fdiv_rn(lo, __half2float(d16));
+    z16 = __float2half_rn(z);
+  } else {
+    double ss = 0.0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[m], (double)y[m]));
+    for (int o = nl >> 1; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    double rms = __dsqrt_rn(__ddiv_rn(ss, (double)P.group));
+    double delta = __ddiv_rn(__dmul_rn(__dmul_rn(2.0, P.alpha), rms), 3.0);
+    d16 = double_to_half_rn(delta);
+    if (__half2float(d16) == 0.0f) d16 = __float2half_rn(1.0f);
+    z16 = __float2half_rn(1.5f);
+  }
+  float df = __half2float(d16), zf = __half2float(z16);
+  if (!isfinite(df) || !isfinite(zf)) bad = true;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    float u = __fadd_rn(__fdiv_rn(y[m], df), zf);
+    int c = __float2int_rn(u);
+    c = c < 0 ? 0 : (c > 3 ? 3 : c);
+    cbuf[4 * lane + m] = (uint8_t)c;
+  }
+  dz = __halves2half2(d16, z16);
+}
+
+__global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
+  // shared-memory copy of the parameters (see rotate_kernel)
+  __shared__ FlushParams Ps;
+  if (threadIdx.x == 0) Ps = Pk;
+  __syncthreads();
+  const FlushParams& P = Ps;
+  const int b = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __shared__ uint8_t cbuf[8][2][kHeadDim];
+  __shared__ int sh_sq, sh_n;
+  if (threadIdx.x == 0) {
+    int L = P.seq_len[b], sq = P.s_quant[b];
+    int avail = L - sq - P.s_keep;
+    int n = avail >= P.s_flush ? (avail / P.s_flush) * P.s_flush : 0;
+    int cap = (P.max_tokens / P.s_flush) * P.s_flush;
+    n = n < cap ? n : cap;
+    if (sq < P.s_sink || L < 0) {
+      set_status(P.status, KVQ_ERR_BOUNDS);
+      n = 0;
+    }
+    sh_sq = sq;
+    sh_n = n;
+  }
+  __syncthreads();
+  const int sq = sh_sq, n = sh_n;
+  const int t0 = blockIdx.x * P.tokens_per_cta;
+  const int t1 = min(n, t0 + P.tokens_per_cta);
+  const int ng = kHeadDim / P.group;
+  for (int row = t0 * P.hkv + warp; row < t1 * P.hkv; row += 8) {
+    const int tok = sq + row / P.hkv, h = row % P.hkv;
+    const int rel = tok - P.s_sink;
+    const int pidx = rel / kPage, tp = rel % kPage;
+    int pid = (pidx < P.max_pages) ? P.page_table[(size_t)b * P.max_pages + pidx] : -1;
+    if (pid < 0 || pid >= P.num_pages) {
+      if (lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
+      continue;
+    }
+    uint8_t* chunk = P.pages + ((size_t)pid * P.hkv + h) * P.page_bytes;
+    const size_t roff = (((size_t)b * P.hkv + h) * P.ring_cap + (tok % P.ring_cap)) * kHeadDim;
+    bool bad = false;
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+      const uint16_t* src = (which == 0 ? P.ring_k : P.ring_v) + roff;
+      uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+      float y[4];
+      y[0] = __uint_as_float(raw.x << 16);
+      y[1] = __uint_as_float(raw.x & 0xffff0000u);
+      y[2] = __uint_as_float(raw.y << 16);
+      y[3] = __uint_as_float(raw.y & 0xffff0000u);
+      if (which == 0 && P.l2) {
+        double ss = 0.0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[m], (double)y[m]));
+        for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+        __half s16 = double_to_half_rn(__dsqrt_rn(ss));
+        float sf = __half2float(s16);
+        if (!isfinite(sf)) bad = true;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) y[m] = (sf == 0.0f) ? 0.0f : __fdiv_rn(y[m], sf);
+        if (lane == 0) reinterpret_cast<__half*>(chunk + norm_off(ng))[tp] = s16;
+      }
+      __half2 dz;
+      quant_row(P, which, y, lane, cbuf[warp][which], dz, bad);
+      const int nl = P.group >> 2;
+      if ((lane & (nl - 1)) == 0) {
+        const int g = lane / nl;
+        const int off = (which == 0 ? k_scale_off() : v_scale_off(ng)) + (tp * ng + g) * 4;
+        *reinterpret_cast<__half2*>(chunk + off) = dz;
+      }
+    }
+    __syncwarp();
+    // key words: 8 per token
+    if (lane < 8) {
+      const int p = lane & 3, r2 = lane >> 2;
+      const uint8_t* c = cbuf[warp][0];
+      uint32_t wd = 0;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        wd |= (uint32_t)c[16 * s + 8 * r2 + 2 * p] << (2 * s);
+        wd |= (uint32_t)c[16 * s + 8 * r2 + 2 * p + 1] << (16 + 2 * s);
+      }
+      const int widx = (4 * (tp & 7) + p) * 4 + 2 * r2 + (tp >> 3);
+      reinterpret_cast<uint32_t*>(chunk)[widx] = wd;
+    }
+    // value half-words: 16 per token
+    if (lane < 16) {
+      const int rr = lane & 7, hh = lane >> 3;
+      const uint8_t* c = cbuf[warp][1];
+      uint32_t hw = 0;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) hw |= (uint32_t)c[16 * m + rr + 8 * hh] << (2 * m);
+      const int widx = (4 * rr + ((tp & 7) >> 1)) * 4 + 2 * (tp >> 3) + hh;
+      reinterpret_cast<uint16_t*>(chunk + kCodeBytes)[2 * widx + (tp & 1)] = (uint16_t)hw;
+    }
+    if (bad && lane == 0) set_status(P.status, KVQ_ERR_NONFINITE);
+    __syncwarp();
+  }
+  // the last CTA of this sequence publishes the new s_quant and re-zeroes the ticket
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    int ticket = atomicAdd(P.counters + b, 1);
+    if (ticket == (int)gridDim.x - 1) {
+      P.s_quant[b] = sq + n;
+      P.counters[b] = 0;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+static void kappa_pos(int g, double kappa, int& i, float& f) {
+  double pos = (double)(g - 1) * kappa;
+  double fl = floor(pos);
+  i = (int)fl;
+  f = (float)(pos - fl);
+}
+
+static int kvq_flush_extractions(int g, double kappa, int* n_lo, int* n_hi) {
+  int ilo, ihi;
+  float f;
+  kappa_pos(g, 1.0 - kappa, ilo, f);
+  kappa_pos(g, kappa, ihi, f);
+  *n_hi = ihi >= g - 1 ? 1 : g - ihi;
+  *n_lo = ilo + 2 > g ? g : ilo + 2;
+  return 0;
+}
+
+extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens,
+                                int32_t* d_status, cudaStream_t stream) {
+  FlushParams P{};
+  P.pages = (uint8_t*)cache->pages;
+  P.page_table = cache->page_table;
+  P.seq_len = cache->seq_len;
+  P.s_quant = cache->s_quant;
+  P.ring_k = cache->ring_k;
+  P.ring_v = cache->ring_v;
+  P.counters = cache->counters;
+  P.status = d_status;
+  P.batch = cfg->batch;
+  P.hkv = cfg->n_kv_heads;
+  P.s_sink = cfg->s_sink;
+  P.s_keep = cfg->s_keep;
+  P.s_flush = cfg->s_flush;
+  P.ring_cap = cfg->ring_cap;
+  P.max_pages = cfg->max_pages_per_seq;
+  P.num_pages = cfg->num_pages;
+  P.max_tokens = max_tokens;
+  P.group = cfg->group_size;
+  P.quantizer = cfg->quantizer;
+  P.l2 = cfg->key_l2norm;
+  P.page_bytes = page_head_bytes(cfg->group_size, cfg->key_l2norm);
+  P.alpha = cfg->quest_alpha;
+  const double kap[2] = {cfg->kappa_k, cfg->kappa_v};
+  for (int w = 0; w < 2; ++w) {
+    kappa_pos(cfg->group_size, kap[w], P.i_hi[w], P.f_hi[w]);
+    kappa_pos(cfg->group_size, 1.0 - kap[w], P.i_lo[w], P.f_lo[w]);
+    kvq_flush_extractions(cfg->group_size, kap[w], &P.n_lo[w], &P.n_hi[w]);
+  }
+  int cap = (max_tokens / cfg->s_flush) * cfg->s_flush;
+  if (cap <= 0) return KVQ_OK;
+  // Small flushes: one (token, head) row per warp (8 rows per CTA) for latency; large
+  // (prefill-sized) flushes: 8 rows per warp.
+  const int rows = cap * cfg->n_kv_heads;
+  const int rows_per_cta = rows <= 8 * 304 ? 8 : 64;
+  int tpc = (rows_per_cta + cfg->n_kv_heads - 1) / cfg->n_kv_heads;
+  if (tpc < 1) tpc = 1;
+  P.tokens_per_cta = tpc;
+  int ctas = (cap + tpc - 1) / tpc;
+  dim3 grid(ctas, cfg->batch);
+  flush_kernel<<<grid, 256, 0, stream>>>(P);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}

@@ -1,0 +1,18 @@
+// Internal launchers shared between the translation units of the library (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include "../../include/kvq.h"
+
+extern "C" {
+int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr, const uint16_t* q, uint16_t* q_out,
+                      int32_t n_q_rows, const uint16_t* k, const uint16_t* v, const int32_t* seq_idx,
+                      const int32_t* pos, int32_t n_kv_rows, const kvq_cache* cache, int32_t* d_status,
+                      cudaStream_t stream);
+int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens, int32_t* d_status,
+                     cudaStream_t stream);
+int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, float* out,
+                    float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status, cudaStream_t stream);
+size_t kvq_attn_ws_bytes(const kvq_config* cfg, int32_t max_ctx);
+void kvq_attn_splits(const kvq_config* cfg, int32_t max_ctx, int* n_int2, int* n_win);
+}

@@ -1,0 +1,237 @@
+// kv_rotate_qk: per-head transform of new keys / values on write and compensation of
+// queries, every output the exact product rounded once to bf16.
+//
+// Source: WUSH-KV digest, core method and inference algorithm (online key transform
+// after RoPE, queries compensated with T^{-T}); OScaR reading note, step 1 "Canalized
+// Rotation" (online FHT of K and Q, H H^T = I, inner products preserved); OSCAR
+// summary, section 3 "Online Deployment" (fixed transforms applied while serving).
+//
+// Design (GB300): one launch covers queries, keys and values.  A dense row is a
+// 128x128 float32 matrix times a bf16 vector; it is computed in double-float (error-
+// free products and sums on the CUDA cores) so that the bf16 rounding of every output
+// is the correctly rounded exact value -- the flush quantizes these rows, so they must
+// not depend on summation order.  The matrices stay L2-resident across decode steps.
+// The Hadamard transform is a warp-wide butterfly (two in-thread stages, five shuffle
+// stages) in double-float, then one scaling by 1/sqrt(d).
+#include "common.cuh"
+#include "launch.h"
+
+namespace kvq {
+
+enum RotMode { ROT_DENSE = 0, ROT_WHT = 1, ROT_COPY = 2 };
+
+struct RotTensor {
+  const uint16_t* src;   // [rows][heads][d]
+  int rows, heads;
+  int mode;              // RotMode
+  const float* mat;      // [mat_heads][d][d] for ROT_DENSE
+  int head_div;          // matrix index = head / head_div
+  int is_query;          // 1: write to q_out; 0: write into the cache
+  uint16_t* dst_q;       // q_out
+  uint16_t* sink;        // cache destination (keys or values)
+  uint16_t* ring;
+  int update_len;        // raise seq_len (keys only)
+};
+
+struct RotParams {
+  RotTensor t[3];
+  int n_dense[3];        // dense items per tensor (0 when not dense)
+  int n_warp[3];         // warp items per tensor (0 when dense)
+  int dense_total, warp_total;
+  const int32_t* seq_idx;
+  const int32_t* pos;
+  int32_t* seq_len;
+  const int32_t* s_quant;
+  int s_sink, ring_cap, batch, hkv;
+  int32_t* status;
+};
+
+// Destination of row `row`, head `h` of tensor tt; nullptr when the row is skipped.
+__device__ __forceinline__ uint16_t* rot_dst(const RotParams& P, const RotTensor& T, int row, int h,
+                                             bool leader) {
+  if (T.is_query) return T.dst_q + ((size_t)row * T.heads + h) * kHeadDim;
+  int b = P.seq_idx[row];
+  int p = P.pos[row];
+  if (b < 0 || b >= P.batch || p < 0) {
+    if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+    return nullptr;
+  }
+  uint16_t* dst;
+  if (p < P.s_sink) {
+    dst = T.sink + (((size_t)b * P.hkv + h) * P.s_sink + p) * kHeadDim;
+  } else {
+    int sq = P.s_quant[b];
+    if (p < sq || p >= sq + P.ring_cap) {
+      if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+      return nullptr;
+    }
+    dst = T.ring + (((size_t)b * P.hkv + h) * P.ring_cap + (p % P.ring_cap)) * kHeadDim;
+  }
+  if (leader && T.update_len && h == 0) atomicMax(P.seq_len + b, p + 1);
+  return dst;
+}
+
+__device__ __forceinline__ void find_item(const int* counts, int idx, int& tt, int& item) {
+  tt = 0;
+  while (tt < 2 && idx >= counts[tt]) { idx -= counts[tt]; ++tt; }
+  item = idx;
+}
+
+// One dense (row, head) item per CTA of 256 threads: thread 2i + half accumulates output
+// i over channels [64 half, 64 half + 64) in double-float.
+__device__ void dense_item(const RotParams& P, int tt, int item) {
+  const RotTensor& T = P.t[tt];
+  int row = item / T.heads, h = item % T.heads;
+  __shared__ float xs[kHeadDim];
+  __shared__ uint16_t* dst_sh;
+  int tid = threadIdx.x;
+  const uint16_t* src = T.src + ((size_t)row * T.heads + h) * kHeadDim;
+  if (tid < kHeadDim) xs[tid] = bf16_bits_to_float(src[tid]);
+  if (tid == 0) dst_sh = rot_dst(P, T, row, h, true);
+  __syncthreads();
+  uint16_t* dst = dst_sh;
+  if (dst == nullptr) return;
+  int i = tid >> 1, half = tid & 1;
+  const float4* m4 = reinterpret_cast<const float4*>(
+      T.mat + ((size_t)(h / T.head_div) * kHeadDim + i) * kHeadDim + 64 * half);
+  const float* x = xs + 64 * half;
+  float hi = 0.f, lo = 0.f;
+#pragma unroll 4
+  for (int j4 = 0; j4 < 16; ++j4) {
+    float4 m = m4[j4];
+    ff_mac(hi, lo, m.x, x[4 * j4 + 0]);
+    ff_mac(hi, lo, m.y, x[4 * j4 + 1]);
+    ff_mac(hi, lo, m.z, x[4 * j4 + 2]);
+    ff_mac(hi, lo, m.w, x[4 * j4 + 3]);
+  }
+  float ohi = __shfl_xor_sync(0xffffffffu, hi, 1);
+  float olo = __shfl_xor_sync(0xffffffffu, lo, 1);
+  float sh, sl;
+  ff_add(hi, lo, ohi, olo, sh, sl);
+  if (half == 0) dst[i] = ff_to_bf16(sh, sl);
+}
+
+// One warp per (row, head): normalised Walsh-Hadamard transform or exact copy.
+__device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
+  const RotTensor& T = P.t[tt];
+  int row = item / T.heads, h = item % T.heads;
+  uint16_t* dst = rot_dst(P, T, row, h, lane == 0);
+  if (dst == nullptr) return;
+  const uint16_t* src = T.src + ((size_t)row * T.heads + h) * kHeadDim;
+  uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+  if (T.mode == ROT_COPY) {
+    *reinterpret_cast<uint2*>(dst + 4 * lane) = raw;
+    return;
+  }
+  float hi[4], lo[4];
+  hi[0] = __uint_as_float(raw.x << 16);
+  hi[1] = __uint_as_float(raw.x & 0xffff0000u);
+  hi[2] = __uint_as_float(raw.y << 16);
+  hi[3] = __uint_as_float(raw.y & 0xffff0000u);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) lo[m] = 0.f;
+  // in-thread stages: stride 1 then stride 2
+#pragma unroll
+  for (int st = 1; st <= 2; st <<= 1) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      if (m & st) continue;
+      float ah = hi[m], al = lo[m], bh = hi[m + st], bl = lo[m + st];
+      ff_add(ah, al, bh, bl, hi[m], lo[m]);
+      ff_add(ah, al, -bh, -bl, hi[m + st], lo[m + st]);
+    }
+  }
+  // cross-lane stages: element stride 4 .. 64 = lane stride 1 .. 16
+#pragma unroll
+  for (int ls = 1; ls < 32; ls <<= 1) {
+    bool upper = (lane & ls) != 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float ph = __shfl_xor_sync(0xffffffffu, hi[m], ls);
+      float pl = __shfl_xor_sync(0xffffffffu, lo[m], ls);
+      if (upper) ff_add(ph, pl, -hi[m], -lo[m], hi[m], lo[m]);   // a - b, b is mine
+      else       ff_add(hi[m], lo[m], ph, pl, hi[m], lo[m]);     // a + b, a is mine
+    }
+  }
+  // scale by 1/sqrt(128) held as a double-float constant
+  const double c = 0.088388347648318440550;  // 1/sqrt(128)
+  const float ch = (float)c;
+  const float cl = (float)(c - (double)ch);
+  uint16_t o[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    float p = __fmul_rn(hi[m], ch);
+    float e = __fmaf_rn(hi[m], ch, -p);
+    e = __fadd_rn(e, __fadd_rn(__fmul_rn(hi[m], cl), __fmul_rn(lo[m], ch)));
+    o[m] = ff_to_bf16(p, e);
+  }
+  uint2 outv;
+  outv.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+  outv.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
+  *reinterpret_cast<uint2*>(dst + 4 * lane) = outv;
+}
+
+__global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
+  // Work on a shared-memory copy of the parameters: device functions take references and
+  // index arrays of the struct at run time, which must never address the parameter space.
+  __shared__ RotParams Ps;
+  if (threadIdx.x == 0) Ps = Pk;
+  __syncthreads();
+  const RotParams& P = Ps;
+  int blk = blockIdx.x;
+  if (blk < P.dense_total) {
+    int tt, item;
+    find_item(P.n_dense, blk, tt, item);
+    dense_item(P, tt, item);
+    return;
+  }
+  int w = (blk - P.dense_total) * 8 + (threadIdx.x >> 5);
+  if (w >= P.warp_total) return;
+  int tt, item;
+  find_item(P.n_warp, w, tt, item);
+  warp_item(P, tt, item, threadIdx.x & 31);
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr, const uint16_t* q,
+                                 uint16_t* q_out, int32_t n_q_rows, const uint16_t* k,
+                                 const uint16_t* v, const int32_t* seq_idx, const int32_t* pos,
+                                 int32_t n_kv_rows, const kvq_cache* cache, int32_t* d_status,
+                                 cudaStream_t stream) {
+  RotParams P{};
+  int gqa = cfg->n_q_heads / cfg->n_kv_heads;
+  bool had = tr->kind == KVQ_TRANSFORM_HADAMARD;
+  // queries
+  P.t[0] = RotTensor{q, n_q_rows, cfg->n_q_heads, had ? ROT_WHT : ROT_DENSE, tr->t_k_inv_t, gqa, 1,
+                     q_out, nullptr, nullptr, 0};
+  // keys
+  P.t[1] = RotTensor{k, n_kv_rows, cfg->n_kv_heads, had ? ROT_WHT : ROT_DENSE, tr->t_k, 1, 0,
+                     nullptr, cache->sink_k, cache->ring_k, 1};
+  // values
+  P.t[2] = RotTensor{v, n_kv_rows, cfg->n_kv_heads, tr->t_v ? ROT_DENSE : ROT_COPY, tr->t_v, 1, 0,
+                     nullptr, cache->sink_v, cache->ring_v, 0};
+  for (int i = 0; i < 3; ++i) {
+    int items = P.t[i].rows * P.t[i].heads;
+    P.n_dense[i] = P.t[i].mode == ROT_DENSE ? items : 0;
+    P.n_warp[i] = P.t[i].mode == ROT_DENSE ? 0 : items;
+  }
+  P.dense_total = P.n_dense[0] + P.n_dense[1] + P.n_dense[2];
+  P.warp_total = P.n_warp[0] + P.n_warp[1] + P.n_warp[2];
+  P.seq_idx = seq_idx;
+  P.pos = pos;
+  P.seq_len = cache->seq_len;
+  P.s_quant = cache->s_quant;
+  P.s_sink = cfg->s_sink;
+  P.ring_cap = cfg->ring_cap;
+  P.batch = cfg->batch;
+  P.hkv = cfg->n_kv_heads;
+  P.status = d_status;
+  long long blocks = (long long)P.dense_total + (P.warp_total + 7) / 8;
+  if (blocks == 0) return KVQ_OK;
+  if (blocks > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
+  rotate_kernel<<<(unsigned)blocks, 256, 0, stream>>>(P);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}

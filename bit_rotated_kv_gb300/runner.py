@@ -1,0 +1,88 @@
+"""Drive the three C-ABI calls for a batch of sequences: chunked prefill of the cache and
+one serving step (append n_new tokens, flush, decode).  Argument marshalling only --
+torch is used for device buffers, gathers of input rows and streams; every step of the
+method runs in the library's kernels."""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import (KVCache, KVConfig, Transform, kv_attn_decode, kv_quant_flush, kv_rotate_qk, workspace)
+
+
+def _rows_for(k_all: torch.Tensor, lengths_lo, lengths_hi):
+    """Gather rows [lo_b, hi_b) of every sequence from k_all [B, T, H, d] into [rows, H, d]
+    plus int32 seq_idx / pos on the same device."""
+    idx_b, idx_t = [], []
+    for b, (lo, hi) in enumerate(zip(lengths_lo, lengths_hi)):
+        if hi > lo:
+            idx_b.append(np.full(hi - lo, b, np.int64))
+            idx_t.append(np.arange(lo, hi, dtype=np.int64))
+    if not idx_b:
+        return None, None
+    ib = torch.from_numpy(np.concatenate(idx_b)).to(k_all.device)
+    it = torch.from_numpy(np.concatenate(idx_t)).to(k_all.device)
+    return ib, it
+
+
+class DecodeRunner:
+    """Owns one cache plus the scratch of a decode step."""
+
+    def __init__(self, cfg: KVConfig, transform: Transform, max_ctx: int, device="cuda"):
+        self.cfg = cfg
+        self.tr = transform
+        self.device = torch.device(device)
+        self.cache = KVCache(cfg, device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.max_ctx = int(max_ctx)
+        self.ws = workspace(cfg, self.max_ctx, device)
+        self.q_out = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.bfloat16,
+                                 device=self.device)
+        self.out = torch.empty((cfg.batch, cfg.n_q_heads, cfg.head_dim), dtype=torch.float32,
+                               device=self.device)
+        self.sm_scale = 1.0 / math.sqrt(cfg.head_dim)
+
+    def set_page_table(self, table: np.ndarray) -> None:
+        self.cache.page_table.copy_(torch.from_numpy(np.ascontiguousarray(table, np.int32)))
+
+    def append(self, k_rows, v_rows, seq_idx, pos, q=None, q_out=None, stream=None) -> None:
+        kv_rotate_qk(self.cfg, self.tr, q, q_out, k_rows, v_rows, seq_idx, pos, self.cache, self.status, stream)
+
+    def flush(self, max_tokens: int, stream=None) -> None:
+        kv_quant_flush(self.cfg, self.cache, max_tokens, self.status, stream)
+
+    def decode(self, q_rot, out, stream=None) -> None:
+        kv_attn_decode(self.cfg, self.cache, q_rot, out, self.sm_scale, self.max_ctx, self.ws, self.status,
+                       stream)
+
+    def prefill(self, k_all: torch.Tensor, v_all: torch.Tensor, lengths, chunk: int) -> None:
+        """Append tokens [0, lengths[b]) of k_all / v_all [B, T, Hkv, d] (bf16, device) in chunks,
+        flushing after each chunk."""
+        lengths = [int(x) for x in lengths]
+        T = max(lengths) if lengths else 0
+        for c0 in range(0, T, chunk):
+            lo = [min(c0, L) for L in lengths]
+            hi = [min(c0 + chunk, L) for L in lengths]
+            ib, it = _rows_for(k_all, lo, hi)
+            if ib is None:
+                continue
+            k = k_all[ib, it].contiguous()
+            v = v_all[ib, it].contiguous()
+            self.append(k, v, ib.to(torch.int32), it.to(torch.int32))
+            self.flush(chunk + self.cfg.s_flush)
+
+    def step_inputs(self, k_all, v_all, ctx, n_new: int):
+        """(k_rows, v_rows, seq_idx, pos) of the n_new tokens after ctx[b] of every sequence."""
+        ctx = [int(x) for x in ctx]
+        ib, it = _rows_for(k_all, ctx, [c + n_new for c in ctx])
+        return (k_all[ib, it].contiguous(), v_all[ib, it].contiguous(), ib.to(torch.int32),
+                it.to(torch.int32))
+
+    def step(self, q, k_rows, v_rows, seq_idx, pos, n_new: int, stream=None) -> None:
+        """One serving step: rotate the new rows and the queries, flush, decode."""
+        self.append(k_rows, v_rows, seq_idx, pos, q, self.q_out, stream)
+        self.flush(n_new + self.cfg.s_flush, stream)
+        self.decode(self.q_out, self.out, stream)

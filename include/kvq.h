@@ -1,0 +1,238 @@
+/*
+ * kvq.h -- C ABI of the rotated INT2 paged KV cache for GB300 (sm_103a).
+ *
+ * Three calls make up the serving hot path shared by the methods on these pages:
+ *   [OSCAR] "OSCAR: Offline Spectral Covariance-Aware Rotation for 2-bit KV Cache
+ *           Quantization" (paperlayer summary)
+ *   [OScaR] "OScaR: The Occam's Razor for Extreme KV Cache Quantization in LLMs and
+ *           Beyond" (reading note, in Chinese)
+ *   [WUSH]  "WUSH-KV: KV Cache Quantization with Data-Adaptive Transforms" (digest)
+ *
+ *   kv_rotate_qk    fixed per-head transform of new keys/values on write and the
+ *                   matching compensation of queries ([WUSH] core method and
+ *                   inference algorithm; [OScaR] step 1 "Canalized Rotation";
+ *                   [OSCAR] section 3 "Online Deployment").
+ *   kv_quant_flush  quantize-on-write of the BF16 tokens that left the recent
+ *                   window into INT2 pages ([WUSH] inference algorithm, S_flush
+ *                   spans; [OSCAR] section 4 "KV Cache Update"; [OScaR] step 2
+ *                   "Omni-Token Scaling" and the integer-quantization basics).
+ *   kv_attn_decode  GQA decode attention reading the mixed BF16 / INT2 cache
+ *                   directly ([OSCAR] section 4 "Decoding Attention Kernel";
+ *                   [OScaR] "系统设计与 CUDA 实现"; [WUSH] GQA background).
+ *
+ * Conventions shared by every call
+ *   - Every pointer inside a struct or argument is a DEVICE pointer unless said
+ *     otherwise; the structs themselves live in host memory and are read during
+ *     the call only.  The caller allocates, owns and frees every buffer; the
+ *     library never allocates, frees, synchronizes, or keeps a pointer after it
+ *     returns.
+ *   - bf16 values are passed as uint16_t bit patterns; float16 scale data as
+ *     uint16_t bit patterns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).
+ *   - Return value: KVQ_OK, or a negative KVQ_ERR_* code for a fault found on
+ *     the host before anything is launched (bad argument, unsupported shape,
+ *     CUDA launch error).
+ *   - Faults found on the device (a page id or position out of range, a
+ *     non-finite scale, a bounded wait that ran out) never trap: the offending
+ *     unit of work is skipped and the first such code is stored into
+ *     *d_status (a device int32 the caller zeroes and reads when it likes).
+ *
+ * Supported shapes: head_dim 128; page_size 16; group_size 32, 64 or 128;
+ * GQA ratio Hq/Hkv in {1, 2, 4, 8}; 2-bit codes.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__) || defined(__clang__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------------- */
+#define KVQ_OK                 0
+#define KVQ_ERR_INVALID_ARG   (-1)  /* null pointer, inconsistent sizes, bad enum          */
+#define KVQ_ERR_UNSUPPORTED   (-2)  /* valid but not implemented (head_dim, G, GQA ratio)  */
+#define KVQ_ERR_CUDA          (-3)  /* a CUDA runtime call or launch failed                */
+#define KVQ_ERR_BOUNDS        (-4)  /* device: page id / position / ring slot out of range */
+#define KVQ_ERR_NONFINITE     (-5)  /* device: a scale, zero point or norm is not finite   */
+#define KVQ_ERR_TIMEOUT       (-6)  /* device: a bounded wait on an async copy ran out     */
+#define KVQ_ERR_WORKSPACE     (-7)  /* workspace smaller than kv_attn_workspace_bytes()    */
+
+/* ---- enums ----------------------------------------------------------------- */
+#define KVQ_QUANT_AFFINE_KAPPA 0  /* kappa-quantile clipped asymmetric affine (OSCAR / WUSH) */
+#define KVQ_QUANT_QUEST_RMS    1  /* QuEST RMS grid: Delta = 2 alpha rms / 3, z = 1.5 (WUSH) */
+
+#define KVQ_TRANSFORM_DENSE    0  /* dense per-head float32 matrices T_K, T_K^{-T}, T_V       */
+#define KVQ_TRANSFORM_HADAMARD 1  /* normalised Walsh-Hadamard on keys and queries (OScaR)    */
+
+/* ---- configuration ----------------------------------------------------------
+ * One POD struct, passed to every call (the pages' hyper-parameters plus shapes).
+ * kappa: the quantile level of the clipping range, in [0.5, 1]; the group range
+ * is [(1-kappa)-quantile, kappa-quantile] of the group's own values with linear
+ * interpolation; kappa = 1 is min/max.  Windows: tokens [0, s_sink) stay BF16,
+ * tokens [s_quant, L) are the BF16 recent window, [s_sink, s_quant) is INT2; the
+ * flush rule quantizes [s_quant, s_quant + s_flush) while L - s_quant >= s_keep +
+ * s_flush.  ring_cap: capacity of the BF16 recent ring in tokens (a multiple of
+ * page_size; at least s_keep + s_flush + the most tokens appended between two
+ * flushes).  attn_splits: INT2 splits per (sequence, kv head) in kv_attn_decode
+ * (0 = automatic). */
+typedef struct kvq_config {
+  int32_t head_dim;          /* d  (128)                               */
+  int32_t n_q_heads;         /* Hq                                     */
+  int32_t n_kv_heads;        /* Hkv; query head hq reads kv head hq / (Hq/Hkv) */
+  int32_t page_size;         /* P  (16 tokens per page)                */
+  int32_t group_size;        /* G  (32, 64, 128 channels per group)    */
+  int32_t quantizer;         /* KVQ_QUANT_*                            */
+  int32_t key_l2norm;        /* 1: keys are l2-scaled after the transform, norm kept as float16 */
+  int32_t s_sink;            /* BF16 sink tokens                       */
+  int32_t s_keep;            /* BF16 recent tokens kept after a flush  */
+  int32_t s_flush;           /* tokens quantized per flush span        */
+  int32_t ring_cap;          /* BF16 recent ring capacity (tokens)     */
+  int32_t batch;             /* B: sequences                           */
+  int32_t max_pages_per_seq; /* columns of the page table              */
+  int32_t num_pages;         /* physical pages in the pool             */
+  int32_t attn_splits;       /* 0 = automatic                          */
+  int32_t reserved;
+  double  kappa_k;           /* key clipping quantile                  */
+  double  kappa_v;           /* value clipping quantile                */
+  double  quest_alpha;       /* QuEST clip in RMS units                */
+} kvq_config;
+
+/* ---- the cache ----------------------------------------------------------------
+ * All device memory, owned by the caller.
+ *
+ * pages      [num_pages][Hkv][kvq_page_head_bytes(cfg)] bytes.  Logical INT2 page
+ *            p of sequence b holds tokens [s_sink + 16p, s_sink + 16p + 16) and
+ *            lives in physical page page_table[b * max_pages_per_seq + p].  One
+ *            (page, kv head) chunk, tokens t = 0..15 of the page:
+ *              [0, 512)      key codes in MMA-fragment order: u32 word 4*l + r
+ *                            (l = 0..31, r = 0..3) holds token (l/4) + 8*(r%2);
+ *                            its bits 2s and 16+2s (s = 0..7) hold the codes of
+ *                            channels 16s + 2*(l%4) + 8*(r/2) + e, e = 0 / 1.
+ *              [512, 1024)   value codes in MMA-fragment order: u32 word 4*l + r,
+ *                            bits 2m + 16e (m = 0..7) hold the code of channel
+ *                            16m + (l/4) + 8*(r%2) of token 2*(l%4) + 8*(r/2) + e.
+ *              [1024, ...)   key (Delta16, z16) float16 pairs [16][d/G], then
+ *                            value (Delta16, z16) pairs [16][d/G], then (only when
+ *                            key_l2norm) key norms s16 float16 [16]; the chunk is
+ *                            padded to a multiple of 32 bytes.
+ *            Token t dequantizes as x_hat_c = s16 * Delta16 * (code_c - z16), with
+ *            s16 = 1 without key_l2norm ([OScaR] step 2 dequantisation).
+ * page_table [B][max_pages_per_seq] int32 physical page ids (-1 = none).
+ * seq_len    [B] int32 tokens in each sequence; kv_rotate_qk raises it to
+ *            pos + 1 for every row it writes.
+ * s_quant    [B] int32 right edge of the INT2 region; must start at s_sink;
+ *            kv_quant_flush advances it.
+ * sink_k/v   [B][Hkv][s_sink][d] bf16 rows of tokens 0 .. s_sink-1.
+ * ring_k/v   [B][Hkv][ring_cap][d] bf16; token t >= s_sink lives in slot t % ring_cap
+ *            while it is in the recent window.
+ * counters   [B] int32, zero before the first call; every call leaves it zero.
+ */
+typedef struct kvq_cache {
+  void*          pages;
+  const int32_t* page_table;
+  int32_t*       seq_len;
+  int32_t*       s_quant;
+  uint16_t*      sink_k;
+  uint16_t*      sink_v;
+  uint16_t*      ring_k;
+  uint16_t*      ring_v;
+  int32_t*       counters;
+} kvq_cache;
+
+/* ---- the per-head transforms (device pointers, float32, row-major) -----------
+ * DENSE:    k' = T_K k, q' = T_K^{-T} q (so q'^T k' = q^T k for any invertible
+ *           T_K; for orthogonal T_K pass T_K itself), v' = T_V v (t_v NULL: values
+ *           are stored unchanged, T_V folded into the projection weights).
+ *           t_k, t_k_inv_t, t_v: [Hkv][d][d], element (i, j) at i*d + j.
+ * HADAMARD: k' = H k, q' = H q with the normalised Walsh-Hadamard matrix (entries
+ *           +-1/sqrt(d)); t_k and t_k_inv_t are ignored; t_v as for DENSE.
+ * Every output row is the exact product rounded once to bf16 (nearest-even). */
+typedef struct kvq_transform {
+  int32_t      kind;         /* KVQ_TRANSFORM_* */
+  int32_t      reserved;
+  const float* t_k;
+  const float* t_k_inv_t;
+  const float* t_v;
+} kvq_transform;
+
+/* Bytes of one (page, kv head) chunk, and of one physical page (all kv heads). */
+KVQ_API size_t kvq_page_head_bytes(const kvq_config* cfg);
+KVQ_API size_t kvq_page_bytes(const kvq_config* cfg);
+
+/* kv_rotate_qk: transform new rows on write, compensate queries on read.
+ *   q        [n_q_rows][Hq][d] bf16 queries (may be NULL when n_q_rows == 0)
+ *   q_out    [n_q_rows][Hq][d] bf16: q' (query head hq uses kv head hq/(Hq/Hkv))
+ *   k, v     [n_kv_rows][Hkv][d] bf16 new keys / values (NULL when n_kv_rows == 0)
+ *   seq_idx  [n_kv_rows] int32 sequence of each row; pos [n_kv_rows] int32 token
+ *            position.  Row r goes to the sink (pos < s_sink) or to ring slot
+ *            pos % ring_cap; pos must satisfy s_quant[b] <= pos < s_quant[b] +
+ *            ring_cap for pos >= s_sink, otherwise the row is skipped with
+ *            KVQ_ERR_BOUNDS in *d_status.  seq_len[b] is raised to pos + 1.
+ * Source: [WUSH] inference algorithm (transform each new key and query, append at
+ * full precision); [OScaR] Algorithm 1 steps 5 and 11 (online FHT of K and Q). */
+KVQ_API int kv_rotate_qk(const kvq_config* cfg, const kvq_transform* tr,
+                 const uint16_t* q, uint16_t* q_out, int32_t n_q_rows,
+                 const uint16_t* k, const uint16_t* v,
+                 const int32_t* seq_idx, const int32_t* pos, int32_t n_kv_rows,
+                 const kvq_cache* cache, int32_t* d_status, void* stream);
+
+/* kv_quant_flush: apply the flush rule to every sequence: while seq_len - s_quant
+ * >= s_keep + s_flush, quantize tokens [s_quant, s_quant + s_flush) of every kv
+ * head from the BF16 ring into their INT2 page and advance s_quant.  At most
+ * max_tokens_per_seq tokens (rounded down to whole spans) are quantized per
+ * sequence by one call; the rest wait for the next call.  Per token (all float
+ * operations IEEE round-to-nearest, none fused):
+ *   key_l2norm (keys only): s = sqrt(sum x^2) in float64, s16 = fp16(s),
+ *     y = x / s16 in float32 (y = 0 when s16 = 0);
+ *   per group of G values, AFFINE_KAPPA: sorted a[], pos = (G-1)*kappa in float64,
+ *     i = floor(pos), f = fp32(pos - i), hi = a[i] + f*(a[i+1] - a[i]) (a[G-1] when
+ *     i = G-1), lo likewise at (G-1)*(1-kappa); Delta = (hi - lo)/3,
+ *     Delta16 = fp16(Delta) (1 if it rounds to 0), z16 = fp16(-(lo / Delta16));
+ *   QUEST_RMS: rms = sqrt(sum y^2 / G) in float64, Delta16 = fp16(2*alpha*rms/3)
+ *     (1 if 0), z16 = 1.5 (not combined with key_l2norm);
+ *   code = clamp(round_half_even(y / Delta16 + z16), 0, 3).
+ * Source: [WUSH] inference algorithm (S_quant, S_flush-aligned spans, per-group
+ * quantizer in place); [OSCAR] section 4 "KV Cache Update"; [OScaR] Algorithm 1
+ * steps 6-9 and the integer-quantization formulas. */
+KVQ_API int kv_quant_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens_per_seq,
+                   int32_t* d_status, void* stream);
+
+/* kv_attn_decode: one decode step of GQA attention for every sequence.
+ *   q_rot   [B][Hq][d] bf16 compensated queries (kv_rotate_qk output)
+ *   out     [B][Hq][d] float32 attention output (in the T_V space)
+ *   sm_scale logit scale (1/sqrt(d) for standard attention)
+ *   max_ctx  an upper bound of seq_len over the batch (sizes the split grid)
+ *   workspace, ws_bytes: device scratch of at least kv_attn_workspace_bytes(cfg,
+ *            max_ctx) bytes; its first 4*B*Hkv bytes must be zero before the
+ *            first call and every call leaves them zero.
+ * Softmax over sink | INT2 | recent tokens with online (max, sum) merging across
+ * splits in one launch; all g = Hq/Hkv query heads of a kv head share one read.
+ * Source: [OSCAR] section 4 "Decoding Attention Kernel"; [OScaR] attention fused
+ * kernel (in-register dequantisation, split attention); [WUSH] GQA. */
+KVQ_API int kv_attn_decode(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
+                   float* out, float sm_scale, int32_t max_ctx,
+                   void* workspace, size_t ws_bytes, int32_t* d_status, void* stream);
+
+/* Workspace bytes kv_attn_decode needs for contexts up to max_ctx (host only). */
+KVQ_API size_t kv_attn_workspace_bytes(const kvq_config* cfg, int32_t max_ctx);
+
+/* Static description of a status code. */
+KVQ_API const char* kvq_status_string(int code);
+
+/* Library ABI version (major * 100 + minor). */
+KVQ_API int kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

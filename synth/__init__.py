@@ -80,7 +80,7 @@ class Workload:
     s_flush: int = 8
     transform: str = "orthogonal"      # "orthogonal" | "hadamard" | "invertible" | "identity"
     value_transform: str = "orthogonal"  # "orthogonal" | "identity"
-    key_dist: str = "outlier"          # "outlier" | "fixed_outlier" | "lognormal_norm"
+    key_dist: str = "outlier"          # "outlier" | "fixed_outlier" | "lognormal_norm" | "degenerate"
     outlier_scale: float = 15.0
     n_outlier: int = 2
     fixed_outlier_channels: tuple = ()
@@ -236,6 +236,12 @@ def key_rows(w: Workload, b: int, h: int, n_tokens: int) -> np.ndarray:
         x[:, _outlier_channels(w, h)] *= np.float32(w.outlier_scale)
         ns = min(w.sink_tokens, n_tokens)
         x[:ns] *= np.float32(w.sink_scale)
+    elif w.key_dist == "degenerate":
+        # outlier keys plus degenerate rows: tokens 10..17 constant, 18..25 all zero
+        x = rng.standard_normal((n_tokens, d), dtype=np.float32)
+        x[:, _outlier_channels(w, h)] *= np.float32(w.outlier_scale)
+        x[10:18] = np.float32(1.25)
+        x[18:26] = np.float32(0.0)
     elif w.key_dist == "lognormal_norm":
         dirs = rng.standard_normal((n_tokens, d), dtype=np.float32)
         dirs /= np.linalg.norm(dirs, axis=1, keepdims=True).astype(np.float32)
@@ -252,7 +258,10 @@ def key_rows(w: Workload, b: int, h: int, n_tokens: int) -> np.ndarray:
 
 def value_rows(w: Workload, b: int, h: int, n_tokens: int) -> np.ndarray:
     rng = _rng(w.seed, _TAG_V, b, h)
-    return f32_to_bf16_bits(rng.standard_normal((n_tokens, w.head_dim), dtype=np.float32))
+    x = rng.standard_normal((n_tokens, w.head_dim), dtype=np.float32)
+    if w.key_dist == "degenerate":
+        x[30:36] = np.float32(-0.5)
+    return f32_to_bf16_bits(x)
 
 
 def query_rows(w: Workload, b: int, h: int) -> np.ndarray:

@@ -1,0 +1,106 @@
+"""The C-ABI library without a GPU: it loads, exports exactly the symbols include/kvq.h
+declares, and rejects bad arguments on the host before any CUDA call."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import bit_rotated_kv_gb300 as m
+    if not os.path.exists(m.LIB_PATH):
+        from bit_rotated_kv_gb300 import build_lib
+        build_lib.build()
+    m.lib()
+    return m
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^KVQ_API\s+[\w\s\*]+?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_calls():
+    syms = declared_symbols()
+    for s in ("kv_rotate_qk", "kv_quant_flush", "kv_attn_decode"):
+        assert s in syms
+
+
+def test_exports_match_header(kvq):
+    out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH], capture_output=True, text=True).stdout
+    exported = sorted({line.split()[-1] for line in out.splitlines() if " T " in line})
+    assert exported == declared_symbols()
+    for s in declared_symbols():
+        assert hasattr(kvq.lib(), s)
+
+
+def _cfg(kvq, **kw):
+    base = dict(n_q_heads=32, n_kv_heads=8, batch=2, max_pages_per_seq=64, num_pages=128, ring_cap=272)
+    base.update(kw)
+    return kvq.KVConfig(**base)
+
+
+def test_sizes(kvq):
+    c = _cfg(kvq)
+    assert kvq.kvq_page_head_bytes(c) == 1152             # 512 + 512 + 16*1*4*2
+    assert kvq.kvq_page_bytes(c) == 8 * 1152
+    assert kvq.kvq_page_head_bytes(_cfg(kvq, group_size=64)) == 1280
+    assert kvq.kvq_page_head_bytes(_cfg(kvq, group_size=32, key_l2norm=True)) == 1568
+    assert kvq.kv_attn_workspace_bytes(c, 4096) > 0
+    assert kvq.kvq_page_head_bytes(_cfg(kvq, head_dim=64)) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(head_dim=64), -2), (dict(group_size=16), -2), (dict(n_q_heads=12, n_kv_heads=8), -1),
+    (dict(n_q_heads=24, n_kv_heads=2), -2), (dict(kappa_k=0.3), -1), (dict(kappa_v=1.5), -1),
+    (dict(ring_cap=100), -1), (dict(ring_cap=16), -1), (dict(s_flush=0), -1),
+    (dict(quantizer=1, key_l2norm=True), -2), (dict(quantizer=7), -1), (dict(batch=0), -1),
+])
+def test_config_validation(kvq, kw, code):
+    c = _cfg(kvq, **kw).c()
+    cache = kvq.CCache()
+    rc = kvq.lib().kv_quant_flush(ctypes.byref(c), ctypes.byref(cache), 8, None, None)
+    assert rc == code
+
+
+def test_null_cache_and_workspace_checks(kvq):
+    c = _cfg(kvq).c()
+    cache = kvq.CCache()                              # all NULL
+    assert kvq.lib().kv_quant_flush(ctypes.byref(c), ctypes.byref(cache), 8, None, None) == -1
+    assert kvq.lib().kv_attn_decode(ctypes.byref(c), None, None, None, 1.0, 10, None, 0, None, None) == -1
+    fake = kvq.CCache(*([4096] * 9))                  # non-null, aligned host addresses (never dereferenced)
+    rc = kvq.lib().kv_attn_decode(ctypes.byref(c), ctypes.byref(fake), 4096, 4096, 1.0, 4096, 4096, 16,
+                                  None, None)
+    assert rc == -7                                   # workspace too small: rejected before launch
+    rc = kvq.lib().kv_attn_decode(ctypes.byref(c), ctypes.byref(fake), 4100, 4096, 1.0, 4096, 4096, 1 << 30,
+                                  None, None)
+    assert rc == -1                                   # misaligned query pointer
+
+
+def test_rotate_validation(kvq):
+    c = _cfg(kvq).c()
+    t = kvq.CTransform(5, 0, None, None, None)
+    assert kvq.lib().kv_rotate_qk(ctypes.byref(c), ctypes.byref(t), None, None, 0, None, None, None, None, 0,
+                                  None, None, None) == -1
+    t = kvq.CTransform(0, 0, None, None, None)
+    # queries without T^{-T}
+    assert kvq.lib().kv_rotate_qk(ctypes.byref(c), ctypes.byref(t), 4096, 4096, 1, None, None, None, None, 0,
+                                  None, None, None) == -1
+    # nothing to do: returns OK without touching the device
+    assert kvq.lib().kv_rotate_qk(ctypes.byref(c), ctypes.byref(t), None, None, 0, None, None, None, None, 0,
+                                  None, None, None) == 0
+    assert kvq.lib().kv_rotate_qk(ctypes.byref(c), ctypes.byref(t), None, None, -1, None, None, None, None, 0,
+                                  None, None, None) == -1
+
+
+def test_status_strings(kvq):
+    for code in range(0, -8, -1):
+        assert kvq.kvq_status_string(code) != "unknown status"
+    assert kvq.lib().kvq_version() == 100
