@@ -36,7 +36,7 @@ KVQ_QUANT_QUEST_RMS = 1
 KVQ_TRANSFORM_DENSE = 0
 KVQ_TRANSFORM_HADAMARD = 1
 
-EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_attn_decode", "kv_attn_workspace_bytes",
+EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_attn_decode", "kv_attn_decode_noalloc", "kv_attn_workspace_bytes",
             "kvq_page_head_bytes", "kvq_page_bytes", "kvq_status_string", "kvq_version")
 
 
@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         l.kv_quant_flush.restype = ctypes.c_int
         l.kv_attn_decode.argtypes = [P(CConfig), P(CCache), vp, vp, ctypes.c_float, i32, vp, sz, vp, vp]
         l.kv_attn_decode.restype = ctypes.c_int
+        l.kv_attn_decode_noalloc.argtypes = [P(CConfig), P(CCache), vp, vp, ctypes.c_float, i32, vp, vp]
+        l.kv_attn_decode_noalloc.restype = ctypes.c_int
         l.kv_attn_workspace_bytes.argtypes = [P(CConfig), i32]
         l.kv_attn_workspace_bytes.restype = sz
         l.kvq_page_head_bytes.argtypes = [P(CConfig)]
@@ -231,6 +233,18 @@ def kv_attn_decode(cfg: KVConfig, cache: KVCache, q_rot, out, sm_scale: float, m
     rc = lib().kv_attn_decode(ctypes.byref(c), ctypes.byref(cc), _ptr(q_rot), _ptr(out), float(sm_scale),
                               int(max_ctx), _ptr(workspace), nbytes, _ptr(status), _stream(stream))
     _check(rc, "kv_attn_decode")
+
+
+NOALLOC_WORKSPACE_BYTES = 8 << 20
+
+
+def kv_attn_decode_noalloc(cfg: KVConfig, cache: KVCache, q_rot, out, sm_scale: float, max_ctx: int, status,
+                           stream=None) -> None:
+    """kv_attn_decode with the library's fixed internal scratch (no workspace argument)."""
+    c, cc = cfg.c(), cache.c()
+    rc = lib().kv_attn_decode_noalloc(ctypes.byref(c), ctypes.byref(cc), _ptr(q_rot), _ptr(out), float(sm_scale),
+                                      int(max_ctx), _ptr(status), _stream(stream))
+    _check(rc, "kv_attn_decode_noalloc")
 
 
 def workspace(cfg: KVConfig, max_ctx: int, device="cuda") -> torch.Tensor:

@@ -125,4 +125,15 @@ KVQ_API int kv_attn_decode(const kvq_config* cfg, const kvq_cache* cache, const 
   return kvq_launch_attn(cfg, cache, q_rot, out, sm_scale, max_ctx, workspace, d_status, (cudaStream_t)stream);
 }
 
+KVQ_API int kv_attn_decode_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
+                                   float* out, float sm_scale, int32_t max_ctx, int32_t* d_status, void* stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  rc = check_cache(cfg, cache);
+  if (rc) return rc;
+  if (!q_rot || !out || !aligned(q_rot, 16) || !aligned(out, 16) || max_ctx < 0) return KVQ_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
+  return kvq_launch_attn_noalloc(cfg, cache, q_rot, out, sm_scale, max_ctx, d_status, (cudaStream_t)stream);
+}
+
 }  // extern "C"

@@ -30,6 +30,8 @@
 #include "common.cuh"
 #include "launch.h"
 
+#include <mutex>
+
 namespace kvq {
 
 constexpr int kWarps = 8;
@@ -763,4 +765,36 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
   dim3 grid(P.n_split, cfg->n_kv_heads, cfg->batch);
   attn_decode_kernel<<<grid, kThreads, smem, stream>>>(P, ng);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+// ---- allocation-free variant ---------------------------------------------------------------
+// The workspace of kv_attn_decode_noalloc lives in this fixed array: 8 MiB of device memory
+// that every GPU which loads the library keeps until the process exits.  Host code must not
+// use the symbol itself as a pointer (it names a host-side shadow); its device address is
+// fetched once per device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) uint8_t g_noalloc_workspace[KVQ_NOALLOC_WORKSPACE_BYTES];
+
+extern "C" int kvq_launch_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
+                                       float* out, float sm_scale, int32_t max_ctx, int32_t* d_status,
+                                       cudaStream_t stream) {
+  const size_t need = kvq_attn_ws_bytes(cfg, max_ctx);
+  if (need > (size_t)KVQ_NOALLOC_WORKSPACE_BYTES) return KVQ_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+  static std::mutex mu;
+  static void* addr[64] = {};
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr) return KVQ_ERR_CUDA;
+      addr[dev] = p;
+    }
+    ws = addr[dev];
+  }
+  // the ticket counters at the head of the workspace must start at zero on every call
+  const size_t units = (size_t)cfg->batch * cfg->n_kv_heads;
+  if (cudaMemsetAsync(ws, 0, units * sizeof(int32_t), stream) != cudaSuccess) return KVQ_ERR_CUDA;
+  return kvq_launch_attn(cfg, cache, q_rot, out, sm_scale, max_ctx, ws, d_status, stream);
 }

@@ -223,6 +223,26 @@ KVQ_API int kv_attn_decode(const kvq_config* cfg, const kvq_cache* cache, const 
                    float* out, float sm_scale, int32_t max_ctx,
                    void* workspace, size_t ws_bytes, int32_t* d_status, void* stream);
 
+/* kv_attn_decode_noalloc: kv_attn_decode without a caller-supplied workspace, for callers
+ * that cannot allocate device memory on this path -- for example a plugin running inside a
+ * serving framework whose memory pool owns the whole device and forbids direct cudaMalloc,
+ * or code that must not call cudaMalloc because it can synchronize the device.  This call
+ * allocates nothing: its scratch is a fixed array of KVQ_NOALLOC_WORKSPACE_BYTES (8 MiB) of
+ * device memory inside the library, held by every GPU that loads the library until the
+ * process exits.  Arguments, results and errors are those of kv_attn_decode, except:
+ *   - KVQ_ERR_WORKSPACE when kv_attn_workspace_bytes(cfg, max_ctx) exceeds the fixed size;
+ *   - the first call on a device looks up the array's device address (set-up, once per
+ *     device, while that device is current), so make that first call before any stream
+ *     capture;
+ *   - every call shares the one array: it clears the ticket counters it needs (an async
+ *     memset on `stream`), and calls whose work overlaps on the GPU (other streams, other
+ *     threads) race on it and give wrong results -- serialize them.
+ * This entry point has no counterpart on the pages; it only changes where the scratch of
+ * kv_attn_decode lives. */
+#define KVQ_NOALLOC_WORKSPACE_BYTES (8u << 20)
+KVQ_API int kv_attn_decode_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
+                                   float* out, float sm_scale, int32_t max_ctx, int32_t* d_status, void* stream);
+
 /* Workspace bytes kv_attn_decode needs for contexts up to max_ctx (host only). */
 KVQ_API size_t kv_attn_workspace_bytes(const kvq_config* cfg, int32_t max_ctx);
 
