@@ -163,8 +163,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = synth.CONFIGS[args.config]
-    run = harness.GpuRun(w, device=dev, do_step=False, ring_extra=max(1024, w.n_new))
+    w = workload(args)
+    # the realistic ring capacity (S_keep + S_flush + n_new): window splits are sized by it
+    run = harness.GpuRun(w, device=dev, do_step=False, ring_extra=0)
     r = run.runner
     stream = torch.cuda.current_stream()
     seq0, sq0 = r.cache.seq_len.clone(), r.cache.s_quant.clone()
@@ -291,6 +292,14 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "device_status": status,
     }
     return res
+
+
+def workload(args) -> synth.Workload:
+    """The configuration, optionally shrunk (--batch) for a profiler capture of the same kernel."""
+    w = synth.CONFIGS[args.config]
+    if args.batch:
+        w = w.replace(batch=args.batch)
+    return w
 
 
 def synth_sq(w, ctx: int) -> int:
@@ -430,6 +439,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds on the step while clocks are sampled")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiler captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -38,6 +38,8 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 8;
 constexpr long long kWaitLimit = 1LL << 22;
+constexpr int kRow = 4 + kHeadDim;      // one (m, l, -, -, o[d]) record; o 16-byte aligned
+constexpr int kGroup = 8;               // splits merged together at the first merge level
 
 struct AttnParams {
   const uint8_t* pages;
@@ -50,11 +52,13 @@ struct AttnParams {
   const uint16_t* ring_v;
   const uint16_t* q;
   float* out;
-  float* part;        // [B][Hkv][n_split][g][2 + d]
-  int32_t* count;     // [B][Hkv]
+  float* part;        // [B * Hkv][n_split][g][kRow]   per-CTA partials
+  float* part2;       // [B * Hkv][n_groups][g][kRow]  merged groups of kGroup splits
+  int32_t* count;     // [B * Hkv][n_groups + 1]       tickets of the merge tree
   int32_t* status;
   int batch, hkv, gqa, s_sink, ring_cap, max_pages, num_pages, group, l2, page_bytes;
   int n_int2, n_win, n_split;
+  int mp;             // INT2 pages per sequence covered by the splits (host-known bound)
   float scale_log2;   // sm_scale * log2(e)
 };
 
@@ -104,6 +108,14 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// d = a * b (accumulator starts at zero)
+__device__ __forceinline__ void mma_f16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -127,6 +139,10 @@ __device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
 __device__ __forceinline__ float2 unpack_half2(uint32_t x) {
   __half2 h = *reinterpret_cast<__half2*>(&x);
   return __half22float2(h);
+}
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
 }
 __device__ __forceinline__ float2 unpack_bf162(uint32_t x) {
   return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
@@ -175,43 +191,105 @@ __device__ __forceinline__ float* warp_result(float* base, int warp, size_t wstr
 }
 
 // ---- INT2 pages ----------------------------------------------------------------------------
+// Scale data of one token for all NG groups: NG (Delta16, z16) pairs in one vector load.
+template <int NG>
+__device__ __forceinline__ void load_scales(const uint8_t* p, uint32_t (&o)[NG]) {
+  if constexpr (NG == 1) {
+    o[0] = *reinterpret_cast<const uint32_t*>(p);
+  } else if constexpr (NG == 2) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    o[0] = v.x; o[1] = v.y;
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+}
+
 template <int NG>
 __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int split, float* res,
                            size_t wstride) {
+  // accumulators per group; with fewer than 4 groups the k-steps alternate between two
+  // accumulators so that consecutive MMAs do not wait on each other
+  constexpr int NS = NG == 1 ? 2 : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = P.gqa;
-  const int L = P.seq_len[b];
-  const int sq = min(P.s_quant[b], L);
-  const int n_tok = max(0, sq - P.s_sink);
-  const int np = (n_tok + kPage - 1) / kPage;
-  const int p0 = (int)((long long)np * split / P.n_int2);
-  const int p1 = (int)((long long)np * (split + 1) / P.n_int2);
+  // The splits cover the host-known page range [0, mp) so that every warp fetches its first
+  // page-table entries without waiting for the sequence length; pages beyond the sequence's
+  // INT2 region are then skipped.
+  const int p0 = (int)((long long)P.mp * split / P.n_int2);
+  const int p1 = (int)((long long)P.mp * (split + 1) / P.n_int2);
+  const int first = p0 + warp;
+  const int nk_max = first < p1 ? (p1 - first + kWarps - 1) / kWarps : 0;
+  const int32_t* ptab = P.page_table + (size_t)b * P.max_pages;
+  // page-table entries of this warp's pages, 32 at a time: lane i of chunk c holds page 32c + i
+  auto load_pids = [&](int c) -> int {
+    const int k = 32 * c + lane;
+    const int lp = first + k * kWarps;
+    return (k < nk_max && lp < P.max_pages) ? ptab[lp] : -1;
+  };
+  int pid_a = load_pids(0), pid_b = load_pids(1);
+  const int Lraw = P.seq_len[b];
+  const int sqraw = P.s_quant[b];
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [kWarps][kStages]
   int* slot_pid = reinterpret_cast<int*>(smem + kWarps * kStages * 8);     // [kWarps][kStages]
   QShared* qs = reinterpret_cast<QShared*>(smem + kWarps * kStages * 12);
-  uint8_t* ring = smem + 1024;                                             // [kWarps][kStages][page_bytes]
   const int pb = P.page_bytes;
-  uint8_t* my_ring = ring + (size_t)warp * kStages * pb;
+  uint8_t* my_ring = smem + 1024 + (size_t)warp * kStages * pb;            // [kStages][page_bytes]
   uint64_t* my_bars = bars + warp * kStages;
   int* my_pid = slot_pid + warp * kStages;
+  if (lane < kStages) mbar_init(my_bars + lane, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 
-  // ---- queries: B fragments scaled to fp16 range, per-head multipliers and group sums
+  // ---- this warp's pages inside the INT2 region, and the first copies
+  const int L = Lraw;
+  const int sq = min(sqraw, L);
+  const int n_tok = max(0, sq - P.s_sink);
+  const int np = (n_tok + kPage - 1) / kPage;
+  if (split == 0 && threadIdx.x == 0 && np > P.mp) set_status(P.status, KVQ_ERR_BOUNDS);
+  const int pend = min(p1, np);
+  const int nk = first < pend ? (pend - first + kWarps - 1) / kWarps : 0;
+  auto issue = [&](int k, int pid) {       // lane 0 only
+    const int slot = k % kStages;
+    if (pid < 0 || pid >= P.num_pages) {
+      set_status(P.status, KVQ_ERR_BOUNDS);
+      my_pid[slot] = -1;
+      mbar_arrive(my_bars + slot);
+    } else {
+      my_pid[slot] = pid;
+      mbar_arrive_tx(my_bars + slot, (uint32_t)pb);
+      tma_load_1d(my_ring + (size_t)slot * pb, P.pages + ((size_t)pid * P.hkv + h) * pb, (uint32_t)pb,
+                  my_bars + slot);
+    }
+  };
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < kStages; ++k) {
+    const int pid = __shfl_sync(0xffffffffu, pid_a, k);
+    if (lane == 0 && k < nk) issue(k, pid);
+  }
+
+  // ---- queries (their loads fly while the first pages are copied): B fragments scaled into
+  // fp16 range, per-head multipliers and group sums
   const uint16_t* qb = P.q + ((size_t)b * P.hkv * g + (size_t)h * g) * kHeadDim;
   const int hrow = lane >> 2, quad = lane & 3;
+  uint32_t qraw[8][2];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint16_t* src = qb + (size_t)hrow * kHeadDim + 16 * s + 2 * quad;
+    qraw[s][0] = (hrow < g) ? *reinterpret_cast<const uint32_t*>(src) : 0u;
+    qraw[s][1] = (hrow < g) ? *reinterpret_cast<const uint32_t*>(src + 8) : 0u;
+  }
   uint32_t bq[8][2];
   {
     float qv[8][4];
     float amax = 0.f;
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
+      const float2 lo = unpack_bf162(qraw[s][0]), hi2 = unpack_bf162(qraw[s][1]);
+      qv[s][0] = lo.x; qv[s][1] = lo.y; qv[s][2] = hi2.x; qv[s][3] = hi2.y;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int ch = 16 * s + 2 * quad + (e & 1) + 8 * (e >> 1);
-        float x = (hrow < g) ? bf16_bits_to_float(qb[(size_t)hrow * kHeadDim + ch]) : 0.f;
-        qv[s][e] = x;
-        amax = fmaxf(amax, fabsf(x));
-      }
+      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(qv[s][e]));
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
@@ -223,11 +301,10 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     }
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
-      float f = ldexpf(1.0f, sigma - 2 * slot_pow(s));
+      const float f = ldexpf(1.0f, sigma - 2 * slot_pow(s));
       bq[s][0] = pack_half2(qv[s][0] * f, qv[s][1] * f);
       bq[s][1] = pack_half2(qv[s][2] * f, qv[s][3] * f);
     }
-    // group sums: lanes of one head cover all channels
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
       float acc = 0.f;
@@ -240,8 +317,6 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     }
     if (warp == 0 && quad == 0) qs->mult[hrow] = ldexpf(1.0f, 24 - sigma);
   }
-  if (lane < kStages) mbar_init(my_bars + lane, 1);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
   const int hA = 2 * quad, hB = 2 * quad + 1;
@@ -250,45 +325,22 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
 #pragma unroll
   for (int gi = 0; gi < NG; ++gi) { qsA[gi] = qs->qsum[hA][gi]; qsB[gi] = qs->qsum[hB][gi]; }
 
-  // ---- this warp's pages: p0 + warp + k * kWarps
-  const int first = p0 + warp;
-  const int nk = first < p1 ? (p1 - first + kWarps - 1) / kWarps : 0;
-  const int32_t* ptab = P.page_table + (size_t)b * P.max_pages;
-  auto issue = [&](int k) {
-    int slot = k % kStages;
-    int lp = first + k * kWarps;
-    int pid = (lp < P.max_pages) ? ptab[lp] : -1;
-    if (pid < 0 || pid >= P.num_pages) {
-      set_status(P.status, KVQ_ERR_BOUNDS);
-      my_pid[slot] = -1;
-      mbar_arrive(my_bars + slot);
-    } else {
-      my_pid[slot] = pid;
-      fence_proxy_async();
-      mbar_arrive_tx(my_bars + slot, (uint32_t)pb);
-      tma_load_1d(my_ring + (size_t)slot * pb, P.pages + ((size_t)pid * P.hkv + h) * pb, (uint32_t)pb,
-                  my_bars + slot);
-    }
-  };
-  if (lane == 0)
-    for (int k = 0; k < min(nk, kStages); ++k) issue(k);
-  __syncwarp();
-
+  // the reference maximum starts at a finite "minus infinity" so that fully masked pages
+  // (scores -inf) give p = 0 on the lazy path
   Softmax sm;
-  sm.m[0] = sm.m[1] = -INFINITY;
+  sm.m[0] = sm.m[1] = -1e30f;
   sm.l[0] = sm.l[1] = 0.f;
   float o[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int c = 0; c < 4; ++c) o[mt][c] = 0.f;
-  float zc[2][NG];
-#pragma unroll
-  for (int gi = 0; gi < NG; ++gi) zc[0][gi] = zc[1][gi] = 0.f;
+  // zero-point correction sum_t W_g z_g: row g (group) of one m16n8 accumulator, columns = heads
+  float corr[4] = {0.f, 0.f, 0.f, 0.f};
 
   const int tA = lane >> 2, tB = tA + 8;
-  const int ng_off_v = v_scale_off(NG);
   bool timed_out = false;
+  int chunk_a = 0;               // page-table chunk held in pid_a
   int k = 0;
   for (; k < nk; ++k) {
     const int slot = k % kStages;
@@ -300,21 +352,12 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     const int pid = my_pid[slot];
     const int lp = first + k * kWarps;
     const int valid_tok = (pid < 0) ? 0 : min(kPage, n_tok - kPage * lp);
+    const bool vA = tA < valid_tok, vB = tB < valid_tok;
     // fragments and scales
-    uint4 wk = *reinterpret_cast<const uint4*>(pg + 16 * lane);
-    uint4 wv = *reinterpret_cast<const uint4*>(pg + kCodeBytes + 16 * lane);
-    float dkA[NG], zkA[NG], dkB[NG], zkB[NG], dvA[NG], zvA[NG], dvB[NG], zvB[NG];
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      float2 a = unpack_half2(*reinterpret_cast<const uint32_t*>(pg + k_scale_off() + (tA * NG + gi) * 4));
-      float2 bb = unpack_half2(*reinterpret_cast<const uint32_t*>(pg + k_scale_off() + (tB * NG + gi) * 4));
-      float2 c = unpack_half2(*reinterpret_cast<const uint32_t*>(pg + ng_off_v + (tA * NG + gi) * 4));
-      float2 d = unpack_half2(*reinterpret_cast<const uint32_t*>(pg + ng_off_v + (tB * NG + gi) * 4));
-      dkA[gi] = a.x; zkA[gi] = a.y; dkB[gi] = bb.x; zkB[gi] = bb.y;
-      const bool vA = tA < valid_tok, vB = tB < valid_tok;
-      dvA[gi] = vA ? c.x : 0.f; zvA[gi] = vA ? c.y : 0.f;
-      dvB[gi] = vB ? d.x : 0.f; zvB[gi] = vB ? d.y : 0.f;
-    }
+    const uint4 wk = *reinterpret_cast<const uint4*>(pg + 16 * lane);
+    uint32_t skA[NG], skB[NG];
+    load_scales<NG>(pg + k_scale_off() + tA * NG * 4, skA);
+    load_scales<NG>(pg + k_scale_off() + tB * NG * 4, skB);
     float nA = 1.f, nB = 1.f;
     if (P.l2) {
       const __half* nrm = reinterpret_cast<const __half*>(pg + norm_off(NG));
@@ -324,57 +367,93 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     // ---- scores: codes x q' per group
     const uint32_t kw[4] = {wk.x, wk.y, wk.z, wk.w};
     const uint32_t kw10[4] = {wk.x >> 10, wk.y >> 10, wk.z >> 10, wk.w >> 10};
-    float acc[NG][4];
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[gi][c] = 0.f;
+    float acc[NG][NS][4];
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
       uint32_t a[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) a[r] = code_pair(kw[r], kw10[r], s);
-      mma_f16(acc[(16 * s) / (kHeadDim / NG)], a, bq[s][0], bq[s][1]);
+      const int gi = (16 * s) / (kHeadDim / NG), u = s % NS;
+      const int first_of = gi * (8 / NG) + u;            // first k-step feeding acc[gi][u]
+      if (s == first_of) mma_f16_z(acc[gi][u], a, bq[s][0], bq[s][1]);
+      else mma_f16(acc[gi][u], a, bq[s][0], bq[s][1]);
     }
     float sc[4];
     {
-      float sA0 = 0.f, sA1 = 0.f, sB0 = 0.f, sB1 = 0.f;
+      // s = scale * norm * (mult_h * sum_g Delta_g acc_g - sum_g Delta_g z_g qsum_g)
+      float sA0 = 0.f, sA1 = 0.f, sB0 = 0.f, sB1 = 0.f, cA0 = 0.f, cA1 = 0.f, cB0 = 0.f, cB1 = 0.f;
 #pragma unroll
       for (int gi = 0; gi < NG; ++gi) {
-        sA0 += dkA[gi] * (acc[gi][0] * multA - zkA[gi] * qsA[gi]);
-        sA1 += dkA[gi] * (acc[gi][1] * multB - zkA[gi] * qsB[gi]);
-        sB0 += dkB[gi] * (acc[gi][2] * multA - zkB[gi] * qsA[gi]);
-        sB1 += dkB[gi] * (acc[gi][3] * multB - zkB[gi] * qsB[gi]);
+        float a0 = acc[gi][0][0], a1 = acc[gi][0][1], a2 = acc[gi][0][2], a3 = acc[gi][0][3];
+        if constexpr (NS == 2) {
+          a0 += acc[gi][1][0]; a1 += acc[gi][1][1]; a2 += acc[gi][1][2]; a3 += acc[gi][1][3];
+        }
+        const float2 dzA = unpack_half2(skA[gi]), dzB = unpack_half2(skB[gi]);
+        const float pzA = dzA.x * dzA.y, pzB = dzB.x * dzB.y;      // exact: 11 x 11 bits
+        sA0 = fmaf(dzA.x, a0, sA0); sA1 = fmaf(dzA.x, a1, sA1);
+        sB0 = fmaf(dzB.x, a2, sB0); sB1 = fmaf(dzB.x, a3, sB1);
+        cA0 = fmaf(pzA, qsA[gi], cA0); cA1 = fmaf(pzA, qsB[gi], cA1);
+        cB0 = fmaf(pzB, qsA[gi], cB0); cB1 = fmaf(pzB, qsB[gi], cB1);
       }
-      const float cA = P.scale_log2 * nA, cB = P.scale_log2 * nB;
-      const bool vA = tA < valid_tok, vB = tB < valid_tok;
-      sc[0] = vA ? sA0 * cA : -INFINITY;
-      sc[1] = vA ? sA1 * cA : -INFINITY;
-      sc[2] = vB ? sB0 * cB : -INFINITY;
-      sc[3] = vB ? sB1 * cB : -INFINITY;
+      const float xA = P.scale_log2 * nA, xB = P.scale_log2 * nB;
+      sc[0] = vA ? (sA0 * multA - cA0) * xA : -INFINITY;
+      sc[1] = vA ? (sA1 * multB - cA1) * xA : -INFINITY;
+      sc[2] = vB ? (sB0 * multA - cB0) * xB : -INFINITY;
+      sc[3] = vB ? (sB1 * multB - cB1) * xB : -INFINITY;
     }
-    float p[4], alpha[2];
-    softmax_step(sm, sc, p, alpha);
-    if (alpha[0] != 1.f || alpha[1] != 1.f) {
+    // Lazy reference maximum: probabilities are exp2(s - m) with m moved only when a score
+    // exceeds it by more than 8, so p <= 2^8 (the B operand carries p * 2^-8).
+    float p[4];
+    {
+      const bool up = (fmaxf(sc[0], sc[2]) > sm.m[0] + 8.f) || (fmaxf(sc[1], sc[3]) > sm.m[1] + 8.f);
+      if (__any_sync(0xffffffffu, up)) {
+        float alpha[2];
+        softmax_step(sm, sc, p, alpha);
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= alpha[0]; o[mt][2] *= alpha[0];
-        o[mt][1] *= alpha[1]; o[mt][3] *= alpha[1];
+        for (int mt = 0; mt < 8; ++mt) {
+          o[mt][0] *= alpha[0]; o[mt][2] *= alpha[0];
+          o[mt][1] *= alpha[1]; o[mt][3] *= alpha[1];
+        }
+        corr[0] *= alpha[0];
+        corr[1] *= alpha[1];
+      } else {
+        p[0] = exp2f(sc[0] - sm.m[0]);
+        p[1] = exp2f(sc[1] - sm.m[1]);
+        p[2] = exp2f(sc[2] - sm.m[0]);
+        p[3] = exp2f(sc[3] - sm.m[1]);
+        sm.l[0] += p[0] + p[2];
+        sm.l[1] += p[1] + p[3];
       }
-#pragma unroll
-      for (int gi = 0; gi < NG; ++gi) { zc[0][gi] *= alpha[0]; zc[1][gi] *= alpha[1]; }
     }
     // ---- P V: per value group, W = P * Delta_v as the B operand (fp16)
+    // P in the B-fragment layout (tokens 2q, 2q+1 | 2q+8, 2q+9 of head lane/4), then one
+    // HMUL2 per group with the Delta_v pairs of the same tokens
+    const uint32_t pb0 = movmatrix_trans(pack_half2(p[0] * 0.00390625f, p[1] * 0.00390625f));
+    const uint32_t pb1 = movmatrix_trans(pack_half2(p[2] * 0.00390625f, p[3] * 0.00390625f));
+    const uint4 wv = *reinterpret_cast<const uint4*>(pg + kCodeBytes + 16 * lane);
+    uint32_t dv0[NG], dv1[NG];
+    load_scales<NG>(pg + v_delta_off(NG, 2 * quad, 0), dv0);
+    load_scales<NG>(pg + v_delta_off(NG, 2 * quad + 8, 0), dv1);
+    uint32_t zp0 = 0u, zp1 = 0u;                       // z_v pairs of group lane/4
+    if (hrow < NG) {
+      zp0 = *reinterpret_cast<const uint32_t*>(pg + v_zero_off(NG, 2 * quad, hrow));
+      zp1 = *reinterpret_cast<const uint32_t*>(pg + v_zero_off(NG, 2 * quad + 8, hrow));
+    }
+    if (valid_tok < kPage) {                           // partial or skipped page: clear dead tokens
+      const uint32_t m0 = (2 * quad < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 1 < valid_tok ? 0xffff0000u : 0u);
+      const uint32_t m1 = (2 * quad + 8 < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 9 < valid_tok ? 0xffff0000u : 0u);
+#pragma unroll
+      for (int gi = 0; gi < NG; ++gi) { dv0[gi] &= m0; dv1[gi] &= m1; }
+      zp0 &= m0;
+      zp1 &= m1;
+    }
     uint32_t bw[NG][2];
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
-      uint32_t wa = pack_half2(p[0] * dvA[gi], p[1] * dvA[gi]);   // token tA, heads hA, hB
-      uint32_t wb = pack_half2(p[2] * dvB[gi], p[3] * dvB[gi]);   // token tB
-      float2 fa = unpack_half2(wa), fb = unpack_half2(wb);
-      zc[0][gi] += fa.x * zvA[gi] + fb.x * zvB[gi];
-      zc[1][gi] += fa.y * zvA[gi] + fb.y * zvB[gi];
-      bw[gi][0] = movmatrix_trans(wa);
-      bw[gi][1] = movmatrix_trans(wb);
+      bw[gi][0] = hmul2_bits(pb0, dv0[gi]);
+      bw[gi][1] = hmul2_bits(pb1, dv1[gi]);
+      const uint32_t az[4] = {hrow == gi ? zp0 : 0u, 0u, hrow == gi ? zp1 : 0u, 0u};
+      mma_f16(corr, az, bw[gi][0], bw[gi][1]);
     }
     const uint32_t vw[4] = {wv.x, wv.y, wv.z, wv.w};
     const uint32_t vw10[4] = {wv.x >> 10, wv.y >> 10, wv.z >> 10, wv.w >> 10};
@@ -386,9 +465,17 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
       const int gi = (16 * mt) / (kHeadDim / NG);
       mma_f16(o[mt], a, bw[gi][0], bw[gi][1]);
     }
-    // every lane has consumed this slot: refill it with the page kStages ahead
+    // every lane has consumed this slot: refill it with the page kStages ahead, whose
+    // page-table entry was fetched a chunk earlier
+    const int kk = k + kStages;
+    if ((kk >> 5) > chunk_a) {
+      pid_a = pid_b;
+      ++chunk_a;
+      pid_b = load_pids(chunk_a + 1);
+    }
+    const int pid_next = __shfl_sync(0xffffffffu, pid_a, kk & 31);
     __syncwarp();
-    if (lane == 0 && k + kStages < nk) issue(k + kStages);
+    if (lane == 0 && kk < nk) issue(kk, pid_next);
   }
   if (timed_out) {
     if (lane == 0) set_status(P.status, KVQ_ERR_TIMEOUT);
@@ -397,35 +484,34 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
       (void)mbar_wait(my_bars + kk % kStages, (uint32_t)((kk / kStages) & 1));
   }
 
-  // ---- per-warp result: reduce l and z-corrections over the 8 lanes of a column pair
+  // ---- per-warp result: reduce l over the 8 lanes of a column pair; the zero-point
+  // correction of group gi, heads (hA, hB) sits in lane 4 gi + quad
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
+  for (int c = 0; c < 2; ++c)
 #pragma unroll
-    for (int o2 = 4; o2 < 32; o2 <<= 1) {
-      sm.l[c] += __shfl_xor_sync(0xffffffffu, sm.l[c], o2);
+    for (int o2 = 4; o2 < 32; o2 <<= 1) sm.l[c] += __shfl_xor_sync(0xffffffffu, sm.l[c], o2);
+  float zcA[NG], zcB[NG];
 #pragma unroll
-      for (int gi = 0; gi < NG; ++gi) zc[c][gi] += __shfl_xor_sync(0xffffffffu, zc[c][gi], o2);
-    }
+  for (int gi = 0; gi < NG; ++gi) {
+    zcA[gi] = 256.f * __shfl_sync(0xffffffffu, corr[0], 4 * gi + quad);
+    zcB[gi] = 256.f * __shfl_sync(0xffffffffu, corr[1], 4 * gi + quad);
   }
   float* wr = warp_result(res, warp, wstride);
-  if (hA < g) {
-    if (tA == 0) { wr[hA * (2 + kHeadDim)] = sm.m[0]; wr[hA * (2 + kHeadDim) + 1] = sm.l[0]; }
-  }
-  if (hB < g) {
-    if (tA == 0) { wr[hB * (2 + kHeadDim)] = sm.m[1]; wr[hB * (2 + kHeadDim) + 1] = sm.l[1]; }
-  }
+  if (hA < g && tA == 0) { wr[hA * kRow] = sm.m[0]; wr[hA * kRow + 1] = sm.l[0]; }
+  if (hB < g && tA == 0) { wr[hB * kRow] = sm.m[1]; wr[hB * kRow + 1] = sm.l[1]; }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
-    const float f = ldexpf(1.0f, 24 - 2 * slot_pow(mt));
+    // codes carried 4^slot * 2^-24 and the weights 2^-8
+    const float f = ldexpf(1.0f, 32 - 2 * slot_pow(mt));
     const int gi = (16 * mt) / (kHeadDim / NG);
     const int ch0 = 16 * mt + tA, ch1 = ch0 + 8;
     if (hA < g) {
-      wr[hA * (2 + kHeadDim) + 2 + ch0] = o[mt][0] * f - zc[0][gi];
-      wr[hA * (2 + kHeadDim) + 2 + ch1] = o[mt][2] * f - zc[0][gi];
+      wr[hA * kRow + 4 + ch0] = o[mt][0] * f - zcA[gi];
+      wr[hA * kRow + 4 + ch1] = o[mt][2] * f - zcA[gi];
     }
     if (hB < g) {
-      wr[hB * (2 + kHeadDim) + 2 + ch0] = o[mt][1] * f - zc[1][gi];
-      wr[hB * (2 + kHeadDim) + 2 + ch1] = o[mt][3] * f - zc[1][gi];
+      wr[hB * kRow + 4 + ch0] = o[mt][1] * f - zcB[gi];
+      wr[hB * kRow + 4 + ch1] = o[mt][3] * f - zcB[gi];
     }
   }
 }
@@ -564,13 +650,13 @@ __device__ void window_split(const AttnParams& P, int b, int h, int wsplit, floa
 #pragma unroll
     for (int o2 = 4; o2 < 32; o2 <<= 1) sm.l[c] += __shfl_xor_sync(0xffffffffu, sm.l[c], o2);
   float* wr = warp_result(res, warp, wstride);
-  if (hA < g && tA == 0) { wr[hA * (2 + kHeadDim)] = sm.m[0]; wr[hA * (2 + kHeadDim) + 1] = sm.l[0]; }
-  if (hB < g && tA == 0) { wr[hB * (2 + kHeadDim)] = sm.m[1]; wr[hB * (2 + kHeadDim) + 1] = sm.l[1]; }
+  if (hA < g && tA == 0) { wr[hA * kRow] = sm.m[0]; wr[hA * kRow + 1] = sm.l[0]; }
+  if (hB < g && tA == 0) { wr[hB * kRow] = sm.m[1]; wr[hB * kRow + 1] = sm.l[1]; }
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     const int ch0 = 16 * hrow + 2 * mt, ch1 = ch0 + 1;
-    if (hA < g) { wr[hA * (2 + kHeadDim) + 2 + ch0] = o[mt][0]; wr[hA * (2 + kHeadDim) + 2 + ch1] = o[mt][2]; }
-    if (hB < g) { wr[hB * (2 + kHeadDim) + 2 + ch0] = o[mt][1]; wr[hB * (2 + kHeadDim) + 2 + ch1] = o[mt][3]; }
+    if (hA < g) { wr[hA * kRow + 4 + ch0] = o[mt][0]; wr[hA * kRow + 4 + ch1] = o[mt][2]; }
+    if (hB < g) { wr[hB * kRow + 4 + ch0] = o[mt][1]; wr[hB * kRow + 4 + ch1] = o[mt][3]; }
   }
 }
 
@@ -587,20 +673,73 @@ __device__ __forceinline__ void merge_warps(const float* src, size_t stride, flo
       const float mi = src[i * stride];
       const float f = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
       Lsum += src[i * stride + 1] * f;
-      acc += src[i * stride + 2 + j] * f;
+      acc += src[i * stride + 4 + j] * f;
     }
   }
-  dst[2 + j] = acc;
+  dst[4 + j] = acc;
   if (j == 0) { dst[0] = M; dst[1] = Lsum; }
+}
+
+// Merge n records (m, l, o[d]) per head from the workspace (other CTAs' writes: read past L1)
+// with all loads of a chunk of 8 records in flight: warp w handles head w, lane the channels
+// 4*lane .. 4*lane+3.  TO_OUT: dst[head][j] = o / l; otherwise dst holds merged records.
+__device__ __noinline__ void merge_global(const float* src, int n, int g, float* dst, bool to_out) {
+  const int lane = threadIdx.x & 31, hh = threadIdx.x >> 5;
+  if (hh >= g) return;
+  const size_t stride = (size_t)g * kRow;
+  const float* s0 = src + (size_t)hh * kRow;
+  float M = -INFINITY, L = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c0 = 0; c0 < n; c0 += 8) {
+    float m[8], l[8];
+    float4 o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (c0 + i < n) {
+        const float* r = s0 + (size_t)(c0 + i) * stride;
+        m[i] = __ldcg(r);
+        l[i] = __ldcg(r + 1);
+        o[i] = __ldcg(reinterpret_cast<const float4*>(r + 4) + lane);
+      } else {
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+        o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float Mc = M;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) Mc = fmaxf(Mc, m[i]);
+    const float f0 = (M == -INFINITY) ? 0.f : exp2f(M - Mc);
+    L *= f0;
+    O.x *= f0; O.y *= f0; O.z *= f0; O.w *= f0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float f = (m[i] == -INFINITY) ? 0.f : exp2f(m[i] - Mc);
+      L += l[i] * f;
+      O.x += o[i].x * f; O.y += o[i].y * f; O.z += o[i].z * f; O.w += o[i].w * f;
+    }
+    M = Mc;
+  }
+  if (to_out) {
+    const float inv = (L > 0.f) ? 1.f / L : 0.f;
+    reinterpret_cast<float4*>(dst + (size_t)hh * kHeadDim)[lane] =
+        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+  } else {
+    float* r = dst + (size_t)hh * kRow;
+    if (lane == 0) { r[0] = M; r[1] = L; }
+    reinterpret_cast<float4*>(r + 4)[lane] = O;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnParams Pk, int ng_sel) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_trigger();
   // shared-memory copy of the parameters (device functions take references to it)
   __shared__ AttnParams Ps;
   if (threadIdx.x == 0) Ps = Pk;
   __syncthreads();
   const AttnParams& P = Ps;
+  pdl_wait();
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = P.gqa;
   // per-warp results: an INT2 warp writes into its own (drained) page ring, a window warp
@@ -613,76 +752,57 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
     else if (ng_sel == 2) int2_split<2>(P, smem, b, h, split, res, wstride);
     else int2_split<4>(P, smem, b, h, split, res, wstride);
   } else {
-    wstride = (size_t)g * (2 + kHeadDim);
+    wstride = (size_t)g * kRow;
     window_split(P, b, h, split - P.n_int2, res, wstride);
   }
   __syncthreads();
   // ---- CTA partial: merge the warps, store to the workspace
-  float* part = P.part + (((size_t)b * P.hkv + h) * P.n_split + split) * g * (2 + kHeadDim);
+  float* part = P.part + (((size_t)b * P.hkv + h) * P.n_split + split) * g * kRow;
   for (int idx = threadIdx.x; idx < g * kHeadDim; idx += kThreads) {
     const int hh = idx / kHeadDim, j = idx % kHeadDim;
-    merge_warps(res + hh * (2 + kHeadDim), wstride, part + hh * (2 + kHeadDim), j);
+    merge_warps(res + hh * kRow, wstride, part + hh * kRow, j);
   }
-  __threadfence();
+  // ---- two-level merge tree over the splits of this (sequence, kv head): the last CTA of
+  // every group of kGroup splits merges the group, the last group merger merges the groups.
+  // Tickets are atomic counters (no waiting); every merge issues all its loads at once.
   __syncthreads();
-  __shared__ int last;
+  __shared__ int role;
+  const int unit = b * P.hkv + h;
+  const int n_grp = (P.n_split + kGroup - 1) / kGroup;
+  const int grp = split / kGroup;
+  const int gsize = min(kGroup, P.n_split - grp * kGroup);
+  int32_t* cnt = P.count + (size_t)unit * (n_grp + 1);
   if (threadIdx.x == 0) {
-    const int t = atomicAdd(P.count + b * P.hkv + h, 1);
-    last = (t == P.n_split - 1);
-    if (last) P.count[b * P.hkv + h] = 0;
-  }
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  // ---- final merge of the n_split partials of this (sequence, kv head), all loads
-  // independent: (1) every (split, head) max and sum into shared memory, (2) one warp per
-  // head turns them into rescale factors, (3) every thread sums its outputs over splits.
-  const float* base = P.part + ((size_t)b * P.hkv + h) * P.n_split * g * (2 + kHeadDim);
-  float* fs = reinterpret_cast<float*>(smem + 1024);             // [n_split][g] factors
-  float* ls = fs + (size_t)P.n_split * g;                         // [n_split][g] sums
-  float* Ls = ls + (size_t)P.n_split * g;                         // [g] totals
-  const int ns = P.n_split;
-  for (int idx = threadIdx.x; idx < ns * g; idx += kThreads) {
-    const float* pp = base + (size_t)idx * (2 + kHeadDim);        // idx = split * g + head
-    fs[idx] = __ldcg(pp);
-    ls[idx] = __ldcg(pp + 1);
-  }
-  __syncthreads();
-  {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (warp < g) {
-      float M = -INFINITY;
-      for (int s2 = lane; s2 < ns; s2 += 32) M = fmaxf(M, fs[s2 * g + warp]);
-      for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-      float L = 0.f;
-      for (int s2 = lane; s2 < ns; s2 += 32) {
-        const float m = fs[s2 * g + warp];
-        const float f = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
-        fs[s2 * g + warp] = f;
-        L += ls[s2 * g + warp] * f;
-      }
-      for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
-      if (lane == 0) Ls[warp] = L;
+    __threadfence();
+    const int t = atomicAdd(cnt + grp, 1);
+    role = (t == gsize - 1);
+    if (role) {
+      cnt[grp] = 0;
+      __threadfence();
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < g * kHeadDim; idx += kThreads) {
-    const int hh = idx / kHeadDim, j = idx % kHeadDim;
-    const float* src = base + (size_t)hh * (2 + kHeadDim) + 2 + j;
-    const size_t stride = (size_t)g * (2 + kHeadDim);
-    float acc = 0.f;
-    int s2 = 0;
-    for (; s2 + 16 <= ns; s2 += 16) {
-      float v[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) v[u] = __ldcg(src + (size_t)(s2 + u) * stride);
-#pragma unroll
-      for (int u = 0; u < 16; ++u) acc += v[u] * fs[(s2 + u) * g + hh];
-    }
-    for (; s2 < ns; ++s2) acc += __ldcg(src + (size_t)s2 * stride) * fs[s2 * g + hh];
-    const float L = Ls[hh];
-    P.out[(((size_t)b * P.hkv + h) * g + hh) * kHeadDim + j] = (L > 0.f) ? acc / L : 0.f;
+  if (!role) return;
+  float* out_unit = P.out + (size_t)unit * g * kHeadDim;
+  const float* gsrc = P.part + ((size_t)unit * P.n_split + (size_t)grp * kGroup) * g * kRow;
+  if (n_grp == 1) {
+    merge_global(gsrc, gsize, g, out_unit, true);
+    return;
   }
+  merge_global(gsrc, gsize, g, P.part2 + ((size_t)unit * n_grp + grp) * g * kRow, false);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int t = atomicAdd(cnt + n_grp, 1);
+    role = (t == n_grp - 1);
+    if (role) {
+      cnt[n_grp] = 0;
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  if (!role) return;
+  merge_global(P.part2 + (size_t)unit * n_grp * g * kRow, n_grp, g, out_unit, true);
 }
 
 }  // namespace kvq
@@ -690,20 +810,40 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
 using namespace kvq;
 
 // Split counts from sizes only (no device query), so the workspace size is a pure
-// function of (cfg, max_ctx).  Sized for 152 SMs with two resident CTAs each.
+// function of (cfg, max_ctx).  Aims at one wave of two CTAs per SM on 152 SMs: C CTAs per
+// (sequence, kv head), shared between INT2 splits and BF16-window splits in proportion to
+// their bytes (the window after a flush: S_sink + S_keep + S_flush tokens).
+// INT2 pages per sequence a call with contexts up to max_ctx can touch.
+static int kvq_attn_pages(const kvq_config* cfg, int32_t max_ctx) {
+  const int p = max(0, (max_ctx - cfg->s_sink + kPage - 1) / kPage);
+  return min(p, cfg->max_pages_per_seq);
+}
+
 extern "C" void kvq_attn_splits(const kvq_config* cfg, int32_t max_ctx, int* n_int2, int* n_win) {
-  const int units = cfg->batch * cfg->n_kv_heads;
-  const int pages = max(0, (max_ctx - cfg->s_sink + kPage - 1) / kPage);
-  int ni = cfg->attn_splits > 0 ? cfg->attn_splits : (304 + units - 1) / units;
-  ni = max(1, min(ni, max(1, pages / 8)));
-  const int pb = page_head_bytes(cfg->group_size, cfg->key_l2norm);
-  const long long per_cta = (long long)((pages + ni - 1) / ni) * pb;        // INT2 bytes per CTA
-  const int wtiles = (cfg->s_sink + kPage - 1) / kPage + cfg->ring_cap / kPage + 1;
-  const long long tile_b = kPage * kHeadDim * 2 * 2;
-  int nw = (int)((wtiles * tile_b + per_cta - 1) / max(per_cta, tile_b * kWarps));
-  nw = max(1, min(nw, wtiles));
+  const long long units = (long long)cfg->batch * cfg->n_kv_heads;
+  const int pages = kvq_attn_pages(cfg, max_ctx);
+  const long long pb = page_head_bytes(cfg->group_size, cfg->key_l2norm);
+  const long long tile_b = (long long)kPage * kHeadDim * 2 * 2;
+  const long long wtiles = (cfg->s_sink + kPage - 1) / kPage + (cfg->s_keep + cfg->s_flush + kPage - 1) / kPage + 1;
+  const double wbytes = (double)wtiles * tile_b, ibytes = (double)pages * pb;
+  int per_unit = (int)max(2LL, 304 / max(units, 1LL));
+  int nw = (int)(per_unit * wbytes / (wbytes + ibytes) + 0.5);
+  nw = max(1, min(nw, per_unit - 1));
+  int ni = per_unit - nw;
+  if (cfg->attn_splits > 0) ni = cfg->attn_splits;
+  ni = max(1, min(ni, max(1, pages)));
   *n_int2 = ni;
   *n_win = nw;
+}
+
+// Workspace: tickets [units][n_groups + 1] (int32, padded to 256 B), per-CTA partials
+// [units][n_split][g][kRow], merged groups [units][n_groups][g][kRow] (float32).
+extern "C" size_t kvq_attn_counter_bytes(const kvq_config* cfg, int32_t max_ctx) {
+  int ni, nw;
+  kvq_attn_splits(cfg, max_ctx, &ni, &nw);
+  const size_t units = (size_t)cfg->batch * cfg->n_kv_heads;
+  const size_t n_grp = (size_t)(ni + nw + kGroup - 1) / kGroup;
+  return (units * (n_grp + 1) * 4 + 255) / 256 * 256;
 }
 
 extern "C" size_t kvq_attn_ws_bytes(const kvq_config* cfg, int32_t max_ctx) {
@@ -711,8 +851,8 @@ extern "C" size_t kvq_attn_ws_bytes(const kvq_config* cfg, int32_t max_ctx) {
   kvq_attn_splits(cfg, max_ctx, &ni, &nw);
   const int g = cfg->n_q_heads / cfg->n_kv_heads;
   const size_t units = (size_t)cfg->batch * cfg->n_kv_heads;
-  const size_t counters = (units * 4 + 255) / 256 * 256;
-  return counters + units * (ni + nw) * g * (2 + kHeadDim) * sizeof(float);
+  const size_t ns = (size_t)(ni + nw), n_grp = (ns + kGroup - 1) / kGroup;
+  return kvq_attn_counter_bytes(cfg, max_ctx) + units * (ns + n_grp) * g * kRow * sizeof(float);
 }
 
 extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
@@ -742,17 +882,16 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
   P.page_bytes = page_head_bytes(cfg->group_size, cfg->key_l2norm);
   kvq_attn_splits(cfg, max_ctx, &P.n_int2, &P.n_win);
   P.n_split = P.n_int2 + P.n_win;
+  P.mp = kvq_attn_pages(cfg, max_ctx);
   P.scale_log2 = sm_scale * 1.4426950408889634f;
   const size_t units = (size_t)cfg->batch * cfg->n_kv_heads;
   P.count = (int32_t*)ws;
-  P.part = (float*)((char*)ws + (units * 4 + 255) / 256 * 256);
+  P.part = (float*)((char*)ws + kvq_attn_counter_bytes(cfg, max_ctx));
+  P.part2 = P.part + units * (size_t)P.n_split * P.gqa * kRow;
   const int ng = kHeadDim / cfg->group_size;
   const size_t ring_bytes = (size_t)kWarps * kStages * P.page_bytes;
-  const size_t res_bytes = (size_t)kWarps * P.gqa * (2 + kHeadDim) * sizeof(float);
-  const size_t merge_bytes = (size_t)(2 * P.n_split + 1) * P.gqa * sizeof(float);
-  size_t body = ring_bytes > res_bytes ? ring_bytes : res_bytes;
-  body = body > merge_bytes ? body : merge_bytes;
-  const size_t smem = 1024 + body;
+  const size_t res_bytes = (size_t)kWarps * P.gqa * kRow * sizeof(float);
+  const size_t smem = 1024 + (ring_bytes > res_bytes ? ring_bytes : res_bytes);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   static unsigned long long attr_done = 0ull;
@@ -763,8 +902,8 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
     attr_done |= 1ull << dev;
   }
   dim3 grid(P.n_split, cfg->n_kv_heads, cfg->batch);
-  attn_decode_kernel<<<grid, kThreads, smem, stream>>>(P, ng);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  return launch_pdl(attn_decode_kernel, grid, dim3(kThreads), smem, stream, P, ng) == cudaSuccess ? KVQ_OK
+                                                                                             : KVQ_ERR_CUDA;
 }
 
 // ---- allocation-free variant ---------------------------------------------------------------
@@ -794,7 +933,6 @@ extern "C" int kvq_launch_attn_noalloc(const kvq_config* cfg, const kvq_cache* c
     ws = addr[dev];
   }
   // the ticket counters at the head of the workspace must start at zero on every call
-  const size_t units = (size_t)cfg->batch * cfg->n_kv_heads;
-  if (cudaMemsetAsync(ws, 0, units * sizeof(int32_t), stream) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, kvq_attn_counter_bytes(cfg, max_ctx), stream) != cudaSuccess) return KVQ_ERR_CUDA;
   return kvq_launch_attn(cfg, cache, q_rot, out, sm_scale, max_ctx, ws, d_status, stream);
 }

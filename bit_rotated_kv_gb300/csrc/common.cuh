@@ -25,6 +25,12 @@ __host__ __device__ inline int page_head_bytes(int group_size, int key_l2norm) {
 __host__ __device__ inline int k_scale_off() { return 2 * kCodeBytes; }
 __host__ __device__ inline int v_scale_off(int ng) { return 2 * kCodeBytes + kPage * ng * 4; }
 __host__ __device__ inline int norm_off(int ng) { return 2 * kCodeBytes + 2 * kPage * ng * 4; }
+// Value scales: Delta16 then z16, each laid out [token pair][group][2 tokens] (fp16), so one
+// load gives the two tokens (2i, 2i+1) of every group.
+__host__ __device__ inline int v_delta_off(int ng, int tp, int g) {
+  return v_scale_off(ng) + (((tp >> 1) * ng + g) * 2 + (tp & 1)) * 2;
+}
+__host__ __device__ inline int v_zero_off(int ng, int tp, int g) { return v_delta_off(ng, tp, g) + kPage * ng * 2; }
 
 // First device fault wins; never traps.
 __device__ __forceinline__ void set_status(int32_t* st, int code) {
@@ -91,6 +97,28 @@ __device__ __forceinline__ __half double_to_half_rn(double d) {
     f = __uint_as_float(u);
   }
   return __float2half_rn(f);
+}
+
+// Programmatic dependent launch: a kernel lets the next kernel of the stream start launching
+// as soon as it begins (trigger), and waits for its predecessors' results (wait) before it
+// reads anything they wrote.  Kernels that do not trigger simply complete first.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 }  // namespace kvq

@@ -72,6 +72,47 @@ __device__ __forceinline__ void extract(const float s[4], int n, int nl, unsigne
   }
 }
 
+// The K most extreme values of the group (largest when TOP), most extreme first, on every
+// lane of the group: each lane starts from its own 4 sorted values and merges with its
+// butterfly partner at every stage; the k-th most extreme of two sorted lists v, w is
+// ext_{i=0..k+1} inner(v[i-1], w[k-i]) with v[-1] = w[-1] = the most extreme value.
+template <int K, bool TOP>
+__device__ __forceinline__ void group_topk(const float s[4], int nl, float (&r)[K]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i) r[i] = TOP ? s[3 - i] : s[i];
+  for (int o = nl >> 1; o > 0; o >>= 1) {
+    float w[K], m[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) w[i] = __shfl_xor_sync(0xffffffffu, r[i], o);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      float best = TOP ? fmaxf(r[k], w[k]) : fminf(r[k], w[k]);
+#pragma unroll
+      for (int i = 1; i <= k; ++i) {
+        const float t = TOP ? fminf(r[i - 1], w[k - i]) : fmaxf(r[i - 1], w[k - i]);
+        best = TOP ? fmaxf(best, t) : fminf(best, t);
+      }
+      m[k] = best;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) r[k] = m[k];
+  }
+}
+
+// n-th and (n-1)-th most extreme values of the group (butterfly merge for n <= 4, repeated
+// extraction beyond).
+template <bool TOP>
+__device__ __forceinline__ void order_stats(const float s[4], int n, int nl, unsigned gmask, int lane,
+                                            float& cur, float& prev) {
+  switch (n) {
+    case 1: { float r[1]; group_topk<1, TOP>(s, nl, r); cur = prev = r[0]; break; }
+    case 2: { float r[2]; group_topk<2, TOP>(s, nl, r); cur = r[1]; prev = r[0]; break; }
+    case 3: { float r[3]; group_topk<3, TOP>(s, nl, r); cur = r[2]; prev = r[1]; break; }
+    case 4: { float r[4]; group_topk<4, TOP>(s, nl, r); cur = r[3]; prev = r[2]; break; }
+    default: extract<TOP>(s, n, nl, gmask, lane, cur, prev); break;
+  }
+}
+
 // Quantize one row held as 4 float32 values per lane; writes 4 codes per lane into cbuf
 // (one byte per channel) and returns the group's Delta16 / z16 in dz (valid on all lanes).
 __device__ __forceinline__ void quant_row(const FlushParams& P, int which, const float y[4], int lane,
@@ -83,8 +124,8 @@ __device__ __forceinline__ void quant_row(const FlushParams& P, int which, const
     float s[4] = {y[0], y[1], y[2], y[3]};
     sort4(s[0], s[1], s[2], s[3]);
     float hc, hp, lc, lp;
-    extract<true>(s, P.n_hi[which], nl, gmask, lane, hc, hp);
-    extract<false>(s, P.n_lo[which], nl, gmask, lane, lc, lp);
+    order_stats<true>(s, P.n_hi[which], nl, gmask, lane, hc, hp);
+    order_stats<false>(s, P.n_lo[which], nl, gmask, lane, lc, lp);
     const int g = P.group;
     float hi = (P.i_hi[which] >= g - 1) ? hc
                                         : __fadd_rn(hc, __fmul_rn(P.f_hi[which], __fsub_rn(hp, hc)));
@@ -118,15 +159,18 @@ __device__ __forceinline__ void quant_row(const FlushParams& P, int which, const
   dz = __halves2half2(d16, z16);
 }
 
-__global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
+__global__ void __launch_bounds__(1024) flush_kernel(const FlushParams Pk) {
   // shared-memory copy of the parameters (see rotate_kernel)
+  pdl_trigger();
   __shared__ FlushParams Ps;
   if (threadIdx.x == 0) Ps = Pk;
   __syncthreads();
   const FlushParams& P = Ps;
+  pdl_wait();
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __shared__ uint8_t cbuf[8][2][kHeadDim];
+  __shared__ uint8_t cbuf[32][2][kHeadDim];
+  const int nwarps = blockDim.x >> 5;
   __shared__ int sh_sq, sh_n;
   if (threadIdx.x == 0) {
     int L = P.seq_len[b], sq = P.s_quant[b];
@@ -146,7 +190,7 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
   const int t0 = blockIdx.x * P.tokens_per_cta;
   const int t1 = min(n, t0 + P.tokens_per_cta);
   const int ng = kHeadDim / P.group;
-  for (int row = t0 * P.hkv + warp; row < t1 * P.hkv; row += 8) {
+  for (int row = t0 * P.hkv + warp; row < t1 * P.hkv; row += nwarps) {
     const int tok = sq + row / P.hkv, h = row % P.hkv;
     const int rel = tok - P.s_sink;
     const int pidx = rel / kPage, tp = rel % kPage;
@@ -184,8 +228,12 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
       const int nl = P.group >> 2;
       if ((lane & (nl - 1)) == 0) {
         const int g = lane / nl;
-        const int off = (which == 0 ? k_scale_off() : v_scale_off(ng)) + (tp * ng + g) * 4;
-        *reinterpret_cast<__half2*>(chunk + off) = dz;
+        if (which == 0) {
+          *reinterpret_cast<__half2*>(chunk + k_scale_off() + (tp * ng + g) * 4) = dz;
+        } else {
+          *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g)) = __low2half(dz);
+          *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g)) = __high2half(dz);
+        }
       }
     }
     __syncwarp();
@@ -215,9 +263,12 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
     if (bad && lane == 0) set_status(P.status, KVQ_ERR_NONFINITE);
     __syncwarp();
   }
-  // the last CTA of this sequence publishes the new s_quant and re-zeroes the ticket
+  // the last CTA of this sequence publishes the new s_quant and re-zeroes the ticket; a
+  // sequence handled by a single CTA needs no ticket
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && gridDim.x == 1) {
+    P.s_quant[b] = sq + n;
+  } else if (threadIdx.x == 0) {
     __threadfence();
     int ticket = atomicAdd(P.counters + b, 1);
     if (ticket == (int)gridDim.x - 1) {
@@ -282,15 +333,21 @@ extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, i
   }
   int cap = (max_tokens / cfg->s_flush) * cfg->s_flush;
   if (cap <= 0) return KVQ_OK;
-  // Small flushes: one (token, head) row per warp (8 rows per CTA) for latency; large
-  // (prefill-sized) flushes: 8 rows per warp.
-  const int rows = cap * cfg->n_kv_heads;
-  const int rows_per_cta = rows <= 8 * 304 ? 8 : 64;
-  int tpc = (rows_per_cta + cfg->n_kv_heads - 1) / cfg->n_kv_heads;
+  // Decode-sized flushes (up to 128 rows per sequence): one CTA of 32 warps per sequence, at
+  // most 4 rows per warp and no cross-CTA ticket.  Prefill-sized flushes: CTAs of 8 warps with
+  // 8 rows each, the last CTA of a sequence publishing s_quant.
+  const long long rows = (long long)cap * cfg->n_kv_heads;
+  int threads, tpc;
+  if (rows <= 128) {
+    threads = 1024;
+    tpc = cap;
+  } else {
+    threads = 256;
+    tpc = (64 + cfg->n_kv_heads - 1) / cfg->n_kv_heads;
+  }
   if (tpc < 1) tpc = 1;
   P.tokens_per_cta = tpc;
-  int ctas = (cap + tpc - 1) / tpc;
+  const int ctas = (cap + tpc - 1) / tpc;
   dim3 grid(ctas, cfg->batch);
-  flush_kernel<<<grid, 256, 0, stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  return launch_pdl(flush_kernel, grid, dim3(threads), 0, stream, P) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -35,7 +35,8 @@ struct RotTensor {
 
 struct RotParams {
   RotTensor t[3];
-  int n_dense[3];        // dense items per tensor (0 when not dense)
+  int rt;                // rows per dense tile (rows that share one matrix)
+  int n_dense[3];        // dense tiles per tensor (0 when not dense)
   int n_warp[3];         // warp items per tensor (0 when dense)
   int dense_total, warp_total;
   const int32_t* seq_idx;
@@ -77,38 +78,64 @@ __device__ __forceinline__ void find_item(const int* counts, int idx, int& tt, i
   item = idx;
 }
 
-// One dense (row, head) item per CTA of 256 threads: thread 2i + half accumulates output
-// i over channels [64 half, 64 half + 64) in double-float.
-__device__ void dense_item(const RotParams& P, int tt, int item) {
+// (row, head) of the p-th pair that uses matrix mh: heads [mh * head_div, (mh + 1) * head_div)
+// share it, so pairs run over rows x those heads.
+__device__ __forceinline__ void tile_row(const RotTensor& T, int mh, int p, int& row, int& head) {
+  row = p / T.head_div;
+  head = mh * T.head_div + p % T.head_div;
+}
+
+// One dense tile per CTA of 256 threads: up to RT rows that share matrix mh.  Thread 2i + half
+// keeps its 64 matrix entries T[mh][i][64 half .. 64 half + 63] in registers and, for every row
+// of the tile, accumulates output i over those channels in double-float; partners combine with
+// one shuffle.
+constexpr int kMaxRT = 16;
+__device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const RotTensor& T = P.t[tt];
-  int row = item / T.heads, h = item % T.heads;
-  __shared__ float xs[kHeadDim];
-  __shared__ uint16_t* dst_sh;
-  int tid = threadIdx.x;
-  const uint16_t* src = T.src + ((size_t)row * T.heads + h) * kHeadDim;
-  if (tid < kHeadDim) xs[tid] = bf16_bits_to_float(src[tid]);
-  if (tid == 0) dst_sh = rot_dst(P, T, row, h, true);
-  __syncthreads();
-  uint16_t* dst = dst_sh;
-  if (dst == nullptr) return;
-  int i = tid >> 1, half = tid & 1;
-  const float4* m4 = reinterpret_cast<const float4*>(
-      T.mat + ((size_t)(h / T.head_div) * kHeadDim + i) * kHeadDim + 64 * half);
-  const float* x = xs + 64 * half;
-  float hi = 0.f, lo = 0.f;
-#pragma unroll 4
-  for (int j4 = 0; j4 < 16; ++j4) {
-    float4 m = m4[j4];
-    ff_mac(hi, lo, m.x, x[4 * j4 + 0]);
-    ff_mac(hi, lo, m.y, x[4 * j4 + 1]);
-    ff_mac(hi, lo, m.z, x[4 * j4 + 2]);
-    ff_mac(hi, lo, m.w, x[4 * j4 + 3]);
+  const int pairs = T.rows * T.head_div;                 // (row, head) pairs per matrix
+  const int tiles_per_mat = (pairs + P.rt - 1) / P.rt;
+  const int mh = tile / tiles_per_mat;
+  const int p0 = (tile % tiles_per_mat) * P.rt;
+  const int np = min(P.rt, pairs - p0);
+  __shared__ float xs[kMaxRT][kHeadDim];
+  __shared__ uint16_t* dst_sh[kMaxRT];
+  const int tid = threadIdx.x;
+  // matrix entries first: the longest-latency loads of the tile
+  const int i = tid >> 1, half = tid & 1;
+  const float4* m4 = reinterpret_cast<const float4*>(T.mat + ((size_t)mh * kHeadDim + i) * kHeadDim + 64 * half);
+  float4 m[16];
+#pragma unroll
+  for (int j4 = 0; j4 < 16; ++j4) m[j4] = m4[j4];
+  for (int e = tid; e < np * kHeadDim; e += blockDim.x) {
+    int row, head;
+    tile_row(T, mh, p0 + e / kHeadDim, row, head);
+    xs[e / kHeadDim][e % kHeadDim] =
+        bf16_bits_to_float(T.src[((size_t)row * T.heads + head) * kHeadDim + e % kHeadDim]);
   }
-  float ohi = __shfl_xor_sync(0xffffffffu, hi, 1);
-  float olo = __shfl_xor_sync(0xffffffffu, lo, 1);
-  float sh, sl;
-  ff_add(hi, lo, ohi, olo, sh, sl);
-  if (half == 0) dst[i] = ff_to_bf16(sh, sl);
+  if (tid < np) {
+    int row, head;
+    tile_row(T, mh, p0 + tid, row, head);
+    dst_sh[tid] = rot_dst(P, T, row, head, true);
+  }
+  __syncthreads();
+  for (int r = 0; r < np; ++r) {
+    uint16_t* dst = dst_sh[r];
+    if (dst == nullptr) continue;
+    const float* x = xs[r] + 64 * half;
+    float hi = 0.f, lo = 0.f;
+#pragma unroll
+    for (int j4 = 0; j4 < 16; ++j4) {
+      ff_mac(hi, lo, m[j4].x, x[4 * j4 + 0]);
+      ff_mac(hi, lo, m[j4].y, x[4 * j4 + 1]);
+      ff_mac(hi, lo, m[j4].z, x[4 * j4 + 2]);
+      ff_mac(hi, lo, m[j4].w, x[4 * j4 + 3]);
+    }
+    const float ohi = __shfl_xor_sync(0xffffffffu, hi, 1);
+    const float olo = __shfl_xor_sync(0xffffffffu, lo, 1);
+    float sh, sl;
+    ff_add(hi, lo, ohi, olo, sh, sl);
+    if (half == 0) dst[i] = ff_to_bf16(sh, sl);
+  }
 }
 
 // One warp per (row, head): normalised Walsh-Hadamard transform or exact copy.
@@ -174,15 +201,17 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
 __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
   // Work on a shared-memory copy of the parameters: device functions take references and
   // index arrays of the struct at run time, which must never address the parameter space.
+  pdl_trigger();
   __shared__ RotParams Ps;
   if (threadIdx.x == 0) Ps = Pk;
   __syncthreads();
   const RotParams& P = Ps;
+  pdl_wait();
   int blk = blockIdx.x;
   if (blk < P.dense_total) {
     int tt, item;
     find_item(P.n_dense, blk, tt, item);
-    dense_item(P, tt, item);
+    dense_tile(P, tt, item);
     return;
   }
   int w = (blk - P.dense_total) * 8 + (threadIdx.x >> 5);
@@ -213,10 +242,21 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
   // values
   P.t[2] = RotTensor{v, n_kv_rows, cfg->n_kv_heads, tr->t_v ? ROT_DENSE : ROT_COPY, tr->t_v, 1, 0,
                      nullptr, cache->sink_v, cache->ring_v, 0};
+  // rows per dense tile: one tile per row while that still fills two CTAs per SM, more rows
+  // per tile (fewer matrix reads) for prefill-sized calls
+  long long dense_pairs = 0;
+  for (int i = 0; i < 3; ++i)
+    if (P.t[i].mode == ROT_DENSE) dense_pairs += (long long)P.t[i].rows * P.t[i].heads;
+  long long rt = (dense_pairs + 303) / 304;
+  P.rt = (int)(rt < 1 ? 1 : (rt > kMaxRT ? kMaxRT : rt));
   for (int i = 0; i < 3; ++i) {
-    int items = P.t[i].rows * P.t[i].heads;
-    P.n_dense[i] = P.t[i].mode == ROT_DENSE ? items : 0;
-    P.n_warp[i] = P.t[i].mode == ROT_DENSE ? 0 : items;
+    const long long items = (long long)P.t[i].rows * P.t[i].heads;
+    const int n_mats = P.t[i].heads / P.t[i].head_div;
+    const long long pairs = (long long)P.t[i].rows * P.t[i].head_div;
+    const long long tiles = (long long)n_mats * ((pairs + P.rt - 1) / P.rt);
+    if (tiles > 0x3fffffffLL || items > 0x3fffffffLL) return KVQ_ERR_UNSUPPORTED;
+    P.n_dense[i] = P.t[i].mode == ROT_DENSE ? (int)tiles : 0;
+    P.n_warp[i] = P.t[i].mode == ROT_DENSE ? 0 : (int)items;
   }
   P.dense_total = P.n_dense[0] + P.n_dense[1] + P.n_dense[2];
   P.warp_total = P.n_warp[0] + P.n_warp[1] + P.n_warp[2];
@@ -232,6 +272,6 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
   long long blocks = (long long)P.dense_total + (P.warp_total + 7) / 8;
   if (blocks == 0) return KVQ_OK;
   if (blocks > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
-  rotate_kernel<<<(unsigned)blocks, 256, 0, stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  return launch_pdl(rotate_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, P) == cudaSuccess ? KVQ_OK
+                                                                                       : KVQ_ERR_CUDA;
 }

@@ -121,10 +121,11 @@ typedef struct kvq_config {
  *              [512, 1024)   value codes in MMA-fragment order: u32 word 4*l + r,
  *                            bits 2m + 16e (m = 0..7) hold the code of channel
  *                            16m + (l/4) + 8*(r%2) of token 2*(l%4) + 8*(r/2) + e.
- *              [1024, ...)   key (Delta16, z16) float16 pairs [16][d/G], then
- *                            value (Delta16, z16) pairs [16][d/G], then (only when
- *                            key_l2norm) key norms s16 float16 [16]; the chunk is
- *                            padded to a multiple of 32 bytes.
+ *              [1024, ...)   key (Delta16, z16) float16 pairs [16 tokens][d/G]; then
+ *                            value Delta16 [8 token pairs][d/G][2] and value z16
+ *                            [8 token pairs][d/G][2] (token t at pair t/2, slot t%2);
+ *                            then (only when key_l2norm) key norms s16 float16 [16];
+ *                            the chunk is padded to a multiple of 32 bytes.
  *            Token t dequantizes as x_hat_c = s16 * Delta16 * (code_c - z16), with
  *            s16 = 1 without key_l2norm ([OScaR] step 2 dequantisation).
  * page_table [B][max_pages_per_seq] int32 physical page ids (-1 = none).
@@ -213,8 +214,8 @@ KVQ_API int kv_quant_flush(const kvq_config* cfg, const kvq_cache* cache, int32_
  *   sm_scale logit scale (1/sqrt(d) for standard attention)
  *   max_ctx  an upper bound of seq_len over the batch (sizes the split grid)
  *   workspace, ws_bytes: device scratch of at least kv_attn_workspace_bytes(cfg,
- *            max_ctx) bytes; its first 4*B*Hkv bytes must be zero before the
- *            first call and every call leaves them zero.
+ *            max_ctx) bytes, zero-filled before its first use; every call leaves the
+ *            ticket counters at its head zero again (the rest is overwritten).
  * Softmax over sink | INT2 | recent tokens with online (max, sum) merging across
  * splits in one launch; all g = Hq/Hkv query heads of a kv head share one read.
  * Source: [OSCAR] section 4 "Decoding Attention Kernel"; [OScaR] attention fused

@@ -49,9 +49,11 @@ def decode_chunk(chunk: np.ndarray, group: int, l2: bool) -> dict:
     cv = np.zeros((P, D), np.uint8)
     ck[KT, KC] = codes[:128]
     cv[VT, VC] = codes[128:]
-    sc = chunk[1024:1024 + 2 * P * ng * 4].view(np.float16).reshape(2, P, ng, 2)
-    out = {"ck": ck, "cv": cv, "dk": sc[0, :, :, 0], "zk": sc[0, :, :, 1],
-           "dv": sc[1, :, :, 0], "zv": sc[1, :, :, 1], "nk": None}
+    ks = chunk[1024:1024 + P * ng * 4].view(np.float16).reshape(P, ng, 2)          # [token][group](D, z)
+    vs = chunk[1024 + P * ng * 4:1024 + 2 * P * ng * 4].view(np.float16).reshape(2, P // 2, ng, 2)
+    vd = vs[0].transpose(0, 2, 1).reshape(P, ng)                                     # [pair][group][2] -> [token][group]
+    vz = vs[1].transpose(0, 2, 1).reshape(P, ng)
+    out = {"ck": ck, "cv": cv, "dk": ks[:, :, 0], "zk": ks[:, :, 1], "dv": vd, "zv": vz, "nk": None}
     if l2:
         o = 1024 + 2 * P * ng * 4
         out["nk"] = chunk[o:o + 2 * P].view(np.float16)
