@@ -165,7 +165,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(dev)
     w = workload(args)
     # the realistic ring capacity (S_keep + S_flush + n_new): window splits are sized by it
-    run = harness.GpuRun(w, device=dev, do_step=False, ring_extra=0)
+    run = harness.GpuRun(w, device=dev, do_step=False, ring_extra=0, attn_splits=args.splits)
     r = run.runner
     stream = torch.cuda.current_stream()
     seq0, sq0 = r.cache.seq_len.clone(), r.cache.s_quant.clone()
@@ -440,6 +440,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak", type=float, default=1.0, help="untimed seconds on the step while clocks are sampled")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (smaller profiler captures)")
+    ap.add_argument("--splits", type=int, default=0, help="INT2 splits per (sequence, kv head); 0 = library default")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
