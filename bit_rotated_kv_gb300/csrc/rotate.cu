@@ -7,10 +7,11 @@
 // summary, section 3 "Online Deployment" (fixed transforms applied while serving).
 //
 // Design (GB300): one launch covers queries, keys and values.  A dense row is a
-// 128x128 float32 matrix times a bf16 vector; it is computed in double-float (error-
-// free products and sums on the CUDA cores) so that the bf16 rounding of every output
-// is the correctly rounded exact value -- the flush quantizes these rows, so they must
-// not depend on summation order.  The matrices stay L2-resident across decode steps.
+// 128x128 float32 matrix times a bf16 vector; every output must be the correctly rounded
+// bf16 of the exact value -- the flush quantizes these rows, so they must not depend on
+// summation order.  The fp32 FMA sum plus a rigorous error bound decides the rounding for
+// almost every output; the rest are recomputed in double-float (error-free products and
+// sums).  The matrices stay L2-resident across decode steps.
 // The Hadamard transform is a warp-wide butterfly (two in-thread stages, five shuffle
 // stages) in double-float, then one scaling by 1/sqrt(d).
 #include "common.cuh"
@@ -85,10 +86,24 @@ __device__ __forceinline__ void tile_row(const RotTensor& T, int mh, int p, int&
   head = mh * T.head_div + p % T.head_div;
 }
 
+// bf16 bits of the exact value y, decided from an fp32 value v with |v - y| <= e: the result
+// when no bf16 rounding midpoint lies within e of v, else -1 (y must be computed exactly).
+__device__ __forceinline__ int bf16_if_decided(float v, float e) {
+  const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
+  const float bv = __uint_as_float(b << 16);
+  const float lo = __uint_as_float(((b - 1u) & 0xffffu) << 16);   // adjacent bf16 values
+  const float hi = __uint_as_float(((b + 1u) & 0xffffu) << 16);
+  const float m1 = 0.5f * (bv + lo), m2 = 0.5f * (bv + hi);        // exact midpoints
+  return (fabsf(v - m1) > e && fabsf(v - m2) > e) ? (int)b : -1;   // NaN compares false
+}
+
 // One dense tile per CTA of 256 threads: up to RT rows that share matrix mh.  Thread 2i + half
-// keeps its 64 matrix entries T[mh][i][64 half .. 64 half + 63] in registers and, for every row
-// of the tile, accumulates output i over those channels in double-float; partners combine with
-// one shuffle.
+// keeps its 64 matrix entries T[mh][i][64 half .. 64 half + 63] in registers.  For every row it
+// forms the fp32 FMA sum v of its half and the sum a of |T_ij x_j|; for y = sum_j T_ij x_j the
+// standard bound |fl(sum) - y| <= gamma_65 sum|T_ij x_j| (gamma_n = n u / (1 - n u), u = 2^-24)
+// gives |v - y| <= 2^-17 a, so bf16(v) is the correctly rounded result unless a rounding midpoint
+// lies within that distance.  Those few outputs are recomputed exactly (double-float) by a warp
+// each after the tile.
 constexpr int kMaxRT = 16;
 __device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const RotTensor& T = P.t[tt];
@@ -99,10 +114,13 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const int np = min(P.rt, pairs - p0);
   __shared__ float xs[kMaxRT][kHeadDim];
   __shared__ uint16_t* dst_sh[kMaxRT];
+  __shared__ uint16_t fallback[kMaxRT * kHeadDim];      // (row << 7) | output, undecided outputs
+  __shared__ int n_fallback;
   const int tid = threadIdx.x;
   // matrix entries first: the longest-latency loads of the tile
   const int i = tid >> 1, half = tid & 1;
-  const float4* m4 = reinterpret_cast<const float4*>(T.mat + ((size_t)mh * kHeadDim + i) * kHeadDim + 64 * half);
+  const float* mrow = T.mat + ((size_t)mh * kHeadDim + i) * kHeadDim;
+  const float4* m4 = reinterpret_cast<const float4*>(mrow + 64 * half);
   float4 m[16];
 #pragma unroll
   for (int j4 = 0; j4 < 16; ++j4) m[j4] = m4[j4];
@@ -117,24 +135,48 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
     tile_row(T, mh, p0 + tid, row, head);
     dst_sh[tid] = rot_dst(P, T, row, head, true);
   }
+  if (tid == 0) n_fallback = 0;
   __syncthreads();
   for (int r = 0; r < np; ++r) {
     uint16_t* dst = dst_sh[r];
     if (dst == nullptr) continue;
     const float* x = xs[r] + 64 * half;
-    float hi = 0.f, lo = 0.f;
+    float v = 0.f, a = 0.f;
 #pragma unroll
     for (int j4 = 0; j4 < 16; ++j4) {
-      ff_mac(hi, lo, m[j4].x, x[4 * j4 + 0]);
-      ff_mac(hi, lo, m[j4].y, x[4 * j4 + 1]);
-      ff_mac(hi, lo, m[j4].z, x[4 * j4 + 2]);
-      ff_mac(hi, lo, m[j4].w, x[4 * j4 + 3]);
+      const float4 xv = *reinterpret_cast<const float4*>(x + 4 * j4);
+      v = fmaf(m[j4].x, xv.x, v); a = fmaf(fabsf(m[j4].x), fabsf(xv.x), a);
+      v = fmaf(m[j4].y, xv.y, v); a = fmaf(fabsf(m[j4].y), fabsf(xv.y), a);
+      v = fmaf(m[j4].z, xv.z, v); a = fmaf(fabsf(m[j4].z), fabsf(xv.z), a);
+      v = fmaf(m[j4].w, xv.w, v); a = fmaf(fabsf(m[j4].w), fabsf(xv.w), a);
     }
-    const float ohi = __shfl_xor_sync(0xffffffffu, hi, 1);
-    const float olo = __shfl_xor_sync(0xffffffffu, lo, 1);
-    float sh, sl;
-    ff_add(hi, lo, ohi, olo, sh, sl);
-    if (half == 0) dst[i] = ff_to_bf16(sh, sl);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    a += __shfl_xor_sync(0xffffffffu, a, 1);
+    if (half == 0) {
+      const int b = bf16_if_decided(v, a * 0x1p-17f);
+      if (b >= 0) dst[i] = (uint16_t)b;
+      else fallback[atomicAdd(&n_fallback, 1)] = (uint16_t)((r << 7) | i);
+    }
+  }
+  __syncthreads();
+  // exact recomputation of the undecided outputs: one warp per output, 4 terms per lane
+  const int lane = tid & 31, warp = tid >> 5;
+  for (int f = warp; f < n_fallback; f += (int)(blockDim.x >> 5)) {
+    const int r = fallback[f] >> 7, o = fallback[f] & 127;
+    const float4 t4 = reinterpret_cast<const float4*>(T.mat + ((size_t)mh * kHeadDim + o) * kHeadDim)[lane];
+    const float4 x4 = reinterpret_cast<const float4*>(xs[r])[lane];
+    float hi = 0.f, lo = 0.f;
+    ff_mac(hi, lo, t4.x, x4.x);
+    ff_mac(hi, lo, t4.y, x4.y);
+    ff_mac(hi, lo, t4.z, x4.z);
+    ff_mac(hi, lo, t4.w, x4.w);
+#pragma unroll
+    for (int s2 = 16; s2 > 0; s2 >>= 1) {
+      const float oh = __shfl_xor_sync(0xffffffffu, hi, s2);
+      const float ol = __shfl_xor_sync(0xffffffffu, lo, s2);
+      ff_add(hi, lo, oh, ol, hi, lo);
+    }
+    if (lane == 0) dst_sh[r][o] = ff_to_bf16(hi, lo);
   }
 }
 
