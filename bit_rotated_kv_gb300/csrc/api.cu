@@ -84,14 +84,14 @@ KVQ_API int kv_rotate_qk(const kvq_config* cfg, const kvq_transform* tr, const u
   if (!tr || (tr->kind != KVQ_TRANSFORM_DENSE && tr->kind != KVQ_TRANSFORM_HADAMARD)) return KVQ_ERR_INVALID_ARG;
   if (n_q_rows < 0 || n_kv_rows < 0) return KVQ_ERR_INVALID_ARG;
   if (n_q_rows > 0) {
-    if (!q || !q_out || !aligned(q, 8) || !aligned(q_out, 8)) return KVQ_ERR_INVALID_ARG;
+    if (!q || !q_out || !aligned(q, 16) || !aligned(q_out, 8)) return KVQ_ERR_INVALID_ARG;
     if (tr->kind == KVQ_TRANSFORM_DENSE && (!tr->t_k_inv_t || !aligned(tr->t_k_inv_t, 16)))
       return KVQ_ERR_INVALID_ARG;
   }
   if (n_kv_rows > 0) {
     rc = check_cache(cfg, cache);
     if (rc) return rc;
-    if (!k || !v || !seq_idx || !pos || !aligned(k, 8) || !aligned(v, 8)) return KVQ_ERR_INVALID_ARG;
+    if (!k || !v || !seq_idx || !pos || !aligned(k, 16) || !aligned(v, 16)) return KVQ_ERR_INVALID_ARG;
     if (tr->kind == KVQ_TRANSFORM_DENSE && (!tr->t_k || !aligned(tr->t_k, 16))) return KVQ_ERR_INVALID_ARG;
     if (tr->t_v && !aligned(tr->t_v, 16)) return KVQ_ERR_INVALID_ARG;
   }

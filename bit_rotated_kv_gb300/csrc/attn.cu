@@ -5,7 +5,7 @@
 // BF16 and INT2 segments, unpack INT2 and accumulate in floating point; existing kernels
 // needed two launches plus a merge); OScaR reading note, "系统设计与 CUDA 实现"
 // (INT2 tiles dequantized in registers: x Delta, - z, x s_t, inside split attention) and
-// Algorithm 1 steps 14-17; WUSH-KV digest, GQA background (n_q/n_kv query heads read
+// the algorithm's attention phase; WUSH-KV digest, GQA background (n_q/n_kv query heads read
 // one kv head); decode attention softmax(q K^T / sqrt(d)) V.
 //
 // Design (GB300, sm_103a):

@@ -14,6 +14,7 @@ constexpr int kHeadDim = 128;
 constexpr int kPage = 16;
 constexpr int kCodeBytes = 512;      // 16 tokens x 128 channels x 2 bits, per K or V
 constexpr int kMaxGqa = 8;
+constexpr int kSms = 152;          // SMs of one GB300 (two dies of 76): launch shapes aim at waves of it
 
 // Bytes of one (page, kv head) chunk: K codes, V codes, K scales, V scales, [K norms],
 // padded to 32 bytes.

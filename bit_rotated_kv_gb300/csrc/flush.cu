@@ -9,13 +9,15 @@
 // (Q(x), Delta = (max - min)/(2^b - 1)), KIVI background (z = -min/Delta) and step 2
 // "Omni-Token Scaling" (s = ||k||, k / s quantized, s stored).
 //
-// Design (GB300): one warp per (token, kv head) handles its key row and value row;
-// lane l owns channels 4l..4l+3, a group of G channels is G/4 lanes.  The quantile
-// needs only a few order statistics near the ends, found by repeated warp-level max
-// (min) extraction with exact tie handling -- no sort.  Codes are staged in shared
-// memory and re-packed into the MMA-fragment layout the decode kernel reads with one
-// 128-bit load per thread.  Every float operation is an explicit IEEE round-to-nearest
-// intrinsic, so the results are bit-identical to the float32 / float64 definition.
+// Design (GB300): one warp per (token, kv head, K|V) row; lane l owns channels 4l..4l+3,
+// a group of G channels is G/4 lanes.  The quantile needs only a few order statistics
+// near the ends: up to the 4th most extreme by a butterfly merge of per-lane sorted
+// quadruples, beyond that by repeated warp-level extraction with exact ties -- no sort.
+// Codes are OR-reduced across lanes straight into the MMA-fragment layout the decode
+// kernel reads with one 128-bit load per thread.  Every float operation is an explicit
+// IEEE round-to-nearest intrinsic (divisions by a scale use a correctly rounded
+// reciprocal and one exact-remainder correction), so the results are bit-identical to the
+// float32 / float64 definition.
 #include "common.cuh"
 #include "launch.h"
 
@@ -31,7 +33,7 @@ struct FlushParams {
   int32_t* counters;
   int32_t* status;
   int batch, hkv, s_sink, s_keep, s_flush, ring_cap, max_pages, num_pages, max_tokens;
-  int group, quantizer, l2, page_bytes, tokens_per_cta;
+  int group, quantizer, l2, page_bytes, items_per_cta;
   int i_lo[2], i_hi[2], n_lo[2], n_hi[2];   // [0] keys, [1] values
   float f_lo[2], f_hi[2];
   double alpha;
@@ -113,10 +115,25 @@ __device__ __forceinline__ void order_stats(const float s[4], int n, int nl, uns
   }
 }
 
-// Quantize one row held as 4 float32 values per lane; writes 4 codes per lane into cbuf
-// (one byte per channel) and returns the group's Delta16 / z16 in dz (valid on all lanes).
+// y / d for a positive float16 scale d, correctly rounded.  With r = RN(1/d) and
+// q0 = RN(y r) (within one ulp of y / d), Markstein's theorem gives RN(y / d) =
+// RN(q0 + (y - q0 d) r), the remainder exact by FMA -- as long as nothing underflows or
+// overflows, which holds for 2^-96 <= |y| <= 2^96 since 2^-24 <= d <= 65504.  Other y (and
+// y = 0, NaN or infinity) take the IEEE division.
+__device__ __forceinline__ float div_by_scale(float y, float d, float r) {
+  const float ay = fabsf(y);
+  if (ay >= 0x1p-96f && ay <= 0x1p96f) {
+    const float q0 = __fmul_rn(y, r);
+    const float rem = __fmaf_rn(-q0, d, y);
+    return __fmaf_rn(rem, r, q0);
+  }
+  return __fdiv_rn(y, d);
+}
+
+// Quantize one row held as 4 float32 values per lane; returns the lane's 4 codes and the
+// group's Delta16 / z16 in dz (valid on all lanes).
 __device__ __forceinline__ void quant_row(const FlushParams& P, int which, const float y[4], int lane,
-                                          uint8_t* cbuf, __half2& dz, bool& bad) {
+                                          uint32_t (&code)[4], __half2& dz, bool& bad) {
   const int nl = P.group >> 2;
   const unsigned gmask = nl == 32 ? 0xffffffffu : (((1u << nl) - 1u) << (lane & ~(nl - 1)));
   __half d16, z16;
@@ -149,17 +166,17 @@ __device__ __forceinline__ void quant_row(const FlushParams& P, int which, const
   }
   float df = __half2float(d16), zf = __half2float(z16);
   if (!isfinite(df) || !isfinite(zf)) bad = true;
+  const float rf = __frcp_rn(df);
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    float u = __fadd_rn(__fdiv_rn(y[m], df), zf);
+    float u = __fadd_rn(div_by_scale(y[m], df, rf), zf);
     int c = __float2int_rn(u);
-    c = c < 0 ? 0 : (c > 3 ? 3 : c);
-    cbuf[4 * lane + m] = (uint8_t)c;
+    code[m] = (uint32_t)(c < 0 ? 0 : (c > 3 ? 3 : c));
   }
   dz = __halves2half2(d16, z16);
 }
 
-__global__ void __launch_bounds__(1024) flush_kernel(const FlushParams Pk) {
+__global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
   // shared-memory copy of the parameters (see rotate_kernel)
   pdl_trigger();
   __shared__ FlushParams Ps;
@@ -169,102 +186,130 @@ __global__ void __launch_bounds__(1024) flush_kernel(const FlushParams Pk) {
   pdl_wait();
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __shared__ uint8_t cbuf[32][2][kHeadDim];
   const int nwarps = blockDim.x >> 5;
-  __shared__ int sh_sq, sh_n;
-  if (threadIdx.x == 0) {
-    int L = P.seq_len[b], sq = P.s_quant[b];
-    int avail = L - sq - P.s_keep;
-    int n = avail >= P.s_flush ? (avail / P.s_flush) * P.s_flush : 0;
-    int cap = (P.max_tokens / P.s_flush) * P.s_flush;
+  // every warp derives the span itself (no block barrier before the first load)
+  const int L = P.seq_len[b], sq = P.s_quant[b];
+  int n;
+  {
+    const int avail = L - sq - P.s_keep;
+    n = avail >= P.s_flush ? (avail / P.s_flush) * P.s_flush : 0;
+    const int cap = (P.max_tokens / P.s_flush) * P.s_flush;
     n = n < cap ? n : cap;
     if (sq < P.s_sink || L < 0) {
-      set_status(P.status, KVQ_ERR_BOUNDS);
+      if (lane == 0 && warp == 0) set_status(P.status, KVQ_ERR_BOUNDS);
       n = 0;
     }
-    sh_sq = sq;
-    sh_n = n;
   }
-  __syncthreads();
-  const int sq = sh_sq, n = sh_n;
-  const int t0 = blockIdx.x * P.tokens_per_cta;
-  const int t1 = min(n, t0 + P.tokens_per_cta);
   const int ng = kHeadDim / P.group;
-  for (int row = t0 * P.hkv + warp; row < t1 * P.hkv; row += nwarps) {
-    const int tok = sq + row / P.hkv, h = row % P.hkv;
-    const int rel = tok - P.s_sink;
-    const int pidx = rel / kPage, tp = rel % kPage;
-    int pid = (pidx < P.max_pages) ? P.page_table[(size_t)b * P.max_pages + pidx] : -1;
+  // work items: (token, kv head, K|V) in that order, a contiguous range per CTA, strided over
+  // the CTA's warps.  Ranges and strides are even, so a warp always handles keys (even warps)
+  // or values (odd warps), and its (token, head, ring slot) advance without divisions.  The
+  // page-table entry and ring row of a warp's next item are fetched while the current one is
+  // quantized.
+  const int n_items = n * P.hkv * 2;
+  const int i0 = blockIdx.x * P.items_per_cta;
+  const int i1 = min(n_items, i0 + P.items_per_cta);
+  const int which = warp & 1;
+  const uint16_t* ring = which ? P.ring_v : P.ring_k;
+  const int hkv = P.hkv, rcap = P.ring_cap, dh = nwarps >> 1;
+  int it = i0 + warp;
+  int nx_h = 0, nx_tok = 0, nx_slot = 0, pid_n = -1;
+  uint2 raw_n = make_uint2(0u, 0u);
+  auto fetch = [&]() {
+    const int pidx = (nx_tok - P.s_sink) >> 4;
+    pid_n = (pidx < P.max_pages) ? P.page_table[(size_t)b * P.max_pages + pidx] : -1;
+    raw_n = *reinterpret_cast<const uint2*>(
+        ring + (((size_t)b * hkv + nx_h) * rcap + nx_slot) * kHeadDim + 4 * lane);
+  };
+  if (it < i1) {
+    const int r0 = it >> 1, t = r0 / hkv;
+    nx_h = r0 - t * hkv;
+    nx_tok = sq + t;
+    nx_slot = nx_tok % rcap;
+    fetch();
+  }
+  for (; it < i1; it += nwarps) {
+    const int tok = nx_tok, h = nx_h, pid = pid_n;
+    const uint2 raw = raw_n;
+    nx_h += dh;
+    while (nx_h >= hkv) {
+      nx_h -= hkv;
+      ++nx_tok;
+      if (++nx_slot == rcap) nx_slot = 0;
+    }
+    if (it + nwarps < i1) fetch();
+    const int tp = (tok - P.s_sink) & (kPage - 1);
     if (pid < 0 || pid >= P.num_pages) {
       if (lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
       continue;
     }
-    uint8_t* chunk = P.pages + ((size_t)pid * P.hkv + h) * P.page_bytes;
-    const size_t roff = (((size_t)b * P.hkv + h) * P.ring_cap + (tok % P.ring_cap)) * kHeadDim;
+    uint8_t* chunk = P.pages + ((size_t)pid * hkv + h) * P.page_bytes;
     bool bad = false;
+    float y[4];
+    y[0] = __uint_as_float(raw.x << 16);
+    y[1] = __uint_as_float(raw.x & 0xffff0000u);
+    y[2] = __uint_as_float(raw.y << 16);
+    y[3] = __uint_as_float(raw.y & 0xffff0000u);
+    if (which == 0 && P.l2) {
+      double ss = 0.0;
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint16_t* src = (which == 0 ? P.ring_k : P.ring_v) + roff;
-      uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
-      float y[4];
-      y[0] = __uint_as_float(raw.x << 16);
-      y[1] = __uint_as_float(raw.x & 0xffff0000u);
-      y[2] = __uint_as_float(raw.y << 16);
-      y[3] = __uint_as_float(raw.y & 0xffff0000u);
-      if (which == 0 && P.l2) {
-        double ss = 0.0;
+      for (int m = 0; m < 4; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[m], (double)y[m]));
+      for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+      __half s16 = double_to_half_rn(__dsqrt_rn(ss));
+      float sf = __half2float(s16);
+      if (!isfinite(sf)) bad = true;
+      const float rs = __frcp_rn(sf);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[m], (double)y[m]));
-        for (int o = 16; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-        __half s16 = double_to_half_rn(__dsqrt_rn(ss));
-        float sf = __half2float(s16);
-        if (!isfinite(sf)) bad = true;
-#pragma unroll
-        for (int m = 0; m < 4; ++m) y[m] = (sf == 0.0f) ? 0.0f : __fdiv_rn(y[m], sf);
-        if (lane == 0) reinterpret_cast<__half*>(chunk + norm_off(ng))[tp] = s16;
-      }
-      __half2 dz;
-      quant_row(P, which, y, lane, cbuf[warp][which], dz, bad);
-      const int nl = P.group >> 2;
-      if ((lane & (nl - 1)) == 0) {
-        const int g = lane / nl;
-        if (which == 0) {
-          *reinterpret_cast<__half2*>(chunk + k_scale_off() + (tp * ng + g) * 4) = dz;
-        } else {
-          *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g)) = __low2half(dz);
-          *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g)) = __high2half(dz);
-        }
+      for (int m = 0; m < 4; ++m) y[m] = (sf == 0.0f) ? 0.0f : div_by_scale(y[m], sf, rs);
+      if (lane == 0) reinterpret_cast<__half*>(chunk + norm_off(ng))[tp] = s16;
+    }
+    __half2 dz;
+    uint32_t c[4];
+    quant_row(P, which, y, lane, c, dz, bad);
+    const int nl = P.group >> 2;
+    if ((lane & (nl - 1)) == 0) {
+      const int g = lane / nl;
+      if (which == 0) {
+        *reinterpret_cast<__half2*>(chunk + k_scale_off() + (tp * ng + g) * 4) = dz;
+      } else {
+        *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g)) = __low2half(dz);
+        *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g)) = __high2half(dz);
       }
     }
-    __syncwarp();
-    // key words: 8 per token
-    if (lane < 8) {
-      const int p = lane & 3, r2 = lane >> 2;
-      const uint8_t* c = cbuf[warp][0];
-      uint32_t wd = 0;
+    // Pack the codes with shuffles.  Lane l holds channels 4l..4l+3; with s = l / 4 its pairs
+    // (4l, 4l+1) and (4l+2, 4l+3) land at bits 2s and 16 + 2s of two 32-bit words (keys) or
+    // of two pairs of 16-bit half-words (values), OR-ed over the 8 lanes of equal l % 4.
+    const int sh = 2 * (lane >> 2);
+    uint32_t u0 = (c[0] << sh) | (c[1] << (16 + sh));
+    uint32_t u1 = (c[2] << sh) | (c[3] << (16 + sh));
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        wd |= (uint32_t)c[16 * s + 8 * r2 + 2 * p] << (2 * s);
-        wd |= (uint32_t)c[16 * s + 8 * r2 + 2 * p + 1] << (16 + 2 * s);
-      }
-      const int widx = (4 * (tp & 7) + p) * 4 + 2 * r2 + (tp >> 3);
-      reinterpret_cast<uint32_t*>(chunk)[widx] = wd;
+    for (int o = 4; o < 32; o <<= 1) {
+      u0 |= __shfl_xor_sync(0xffffffffu, u0, o);
+      u1 |= __shfl_xor_sync(0xffffffffu, u1, o);
     }
-    // value half-words: 16 per token
-    if (lane < 16) {
-      const int rr = lane & 7, hh = lane >> 3;
-      const uint8_t* c = cbuf[warp][1];
-      uint32_t hw = 0;
-#pragma unroll
-      for (int m = 0; m < 8; ++m) hw |= (uint32_t)c[16 * m + rr + 8 * hh] << (2 * m);
-      const int widx = (4 * rr + ((tp & 7) >> 1)) * 4 + 2 * (tp >> 3) + hh;
-      reinterpret_cast<uint16_t*>(chunk + kCodeBytes)[2 * widx + (tp & 1)] = (uint16_t)hw;
+    if (lane < 4) {
+      const int hi = lane >> 1, lo = lane & 1;
+      if (which == 0) {
+        // key word (p, r2) = (2 lo + {0, 1}, hi): u0, u1
+        uint32_t* kw = reinterpret_cast<uint32_t*>(chunk);
+        const int base = (4 * (tp & 7) + 2 * lo) * 4 + 2 * hi + (tp >> 3);
+        kw[base] = u0;
+        kw[base + 4] = u1;
+      } else {
+        // value half-words (rr, hh) = (4 lo + {0, 1, 2, 3}, hi): u0 low / high, u1 low / high
+        uint16_t* vw = reinterpret_cast<uint16_t*>(chunk + kCodeBytes);
+        const int off = 2 * (((tp & 7) >> 1) * 4 + 2 * (tp >> 3) + hi) + (tp & 1);
+        const int rr = 4 * lo;
+        vw[2 * (4 * rr) * 4 + off] = (uint16_t)(u0 & 0xffffu);
+        vw[2 * (4 * (rr + 1)) * 4 + off] = (uint16_t)(u0 >> 16);
+        vw[2 * (4 * (rr + 2)) * 4 + off] = (uint16_t)(u1 & 0xffffu);
+        vw[2 * (4 * (rr + 3)) * 4 + off] = (uint16_t)(u1 >> 16);
+      }
     }
     if (bad && lane == 0) set_status(P.status, KVQ_ERR_NONFINITE);
-    __syncwarp();
   }
-  // the last CTA of this sequence publishes the new s_quant and re-zeroes the ticket; a
-  // sequence handled by a single CTA needs no ticket
+  // every warp has read s_quant by now; the last CTA of this sequence publishes the new value
+  // and re-zeroes the ticket (a sequence handled by a single CTA needs no ticket)
   __syncthreads();
   if (threadIdx.x == 0 && gridDim.x == 1) {
     P.s_quant[b] = sq + n;
@@ -331,23 +376,30 @@ extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, i
     kappa_pos(cfg->group_size, 1.0 - kap[w], P.i_lo[w], P.f_lo[w]);
     kvq_flush_extractions(cfg->group_size, kap[w], &P.n_lo[w], &P.n_hi[w]);
   }
-  int cap = (max_tokens / cfg->s_flush) * cfg->s_flush;
+  // no call can quantize more than the ring holds beyond S_keep (tokens [s_quant, L) live in
+  // the ring), which bounds the launch whatever max_tokens says
+  const int ring_limit = cfg->ring_cap - cfg->s_keep;
+  if (max_tokens > ring_limit) max_tokens = ring_limit;
+  int cap = max_tokens > 0 ? (max_tokens / cfg->s_flush) * cfg->s_flush : 0;
   if (cap <= 0) return KVQ_OK;
-  // Decode-sized flushes (up to 128 rows per sequence): one CTA of 32 warps per sequence, at
-  // most 4 rows per warp and no cross-CTA ticket.  Prefill-sized flushes: CTAs of 8 warps with
-  // 8 rows each, the last CTA of a sequence publishing s_quant.
-  const long long rows = (long long)cap * cfg->n_kv_heads;
-  int threads, tpc;
-  if (rows <= 128) {
-    threads = 1024;
-    tpc = cap;
-  } else {
+  P.max_tokens = cap;
+  // Work items are (token, kv head, K|V) rows, one warp each.  Decode-sized flushes: CTAs of
+  // 4 warps with one item per warp, spread over many SMs so the flush costs about one row's
+  // latency.  Prefill-sized flushes: CTAs of 8 warps, enough items per warp to fill one wave
+  // of the GPU, each warp prefetching its next row.  The last CTA of a sequence publishes
+  // s_quant.
+  const long long items = 2LL * cap * cfg->n_kv_heads;
+  const long long total = items * cfg->batch;
+  int threads = 128, ipw = 1;
+  if (total > 4LL * kSms * 16) {
     threads = 256;
-    tpc = (64 + cfg->n_kv_heads - 1) / cfg->n_kv_heads;
+    const long long slots = (long long)kSms * 4 * (threads / 32);   // 4 resident CTAs per SM at 52 registers
+    ipw = (int)((total + slots - 1) / slots);
   }
-  if (tpc < 1) tpc = 1;
-  P.tokens_per_cta = tpc;
-  const int ctas = (cap + tpc - 1) / tpc;
+  const long long ipc = (long long)ipw * (threads / 32);
+  if (ipc > (1LL << 30) || (items + ipc - 1) / ipc > 0x7fffffffLL || cfg->batch > 65535) return KVQ_ERR_UNSUPPORTED;
+  P.items_per_cta = (int)ipc;
+  const int ctas = (int)((items + ipc - 1) / ipc);
   dim3 grid(ctas, cfg->batch);
   return launch_pdl(flush_kernel, grid, dim3(threads), 0, stream, P) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -48,12 +48,11 @@ struct RotParams {
   int32_t* status;
 };
 
-// Destination of row `row`, head `h` of tensor tt; nullptr when the row is skipped.
-__device__ __forceinline__ uint16_t* rot_dst(const RotParams& P, const RotTensor& T, int row, int h,
-                                             bool leader) {
+// Destination of row `row`, head `h` of tensor tt (b = seq_idx[row], p = pos[row] for cache
+// rows, loaded by the caller); nullptr when the row is skipped.
+__device__ __forceinline__ uint16_t* rot_dst(const RotParams& P, const RotTensor& T, int row, int h, int b,
+                                             int p, bool leader) {
   if (T.is_query) return T.dst_q + ((size_t)row * T.heads + h) * kHeadDim;
-  int b = P.seq_idx[row];
-  int p = P.pos[row];
   if (b < 0 || b >= P.batch || p < 0) {
     if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
     return nullptr;
@@ -98,12 +97,15 @@ __device__ __forceinline__ int bf16_if_decided(float v, float e) {
 }
 
 // One dense tile per CTA of 256 threads: up to RT rows that share matrix mh.  Thread 2i + half
-// keeps its 64 matrix entries T[mh][i][64 half .. 64 half + 63] in registers.  For every row it
-// forms the fp32 FMA sum v of its half and the sum a of |T_ij x_j|; for y = sum_j T_ij x_j the
-// standard bound |fl(sum) - y| <= gamma_65 sum|T_ij x_j| (gamma_n = n u / (1 - n u), u = 2^-24)
-// gives |v - y| <= 2^-17 a, so bf16(v) is the correctly rounded result unless a rounding midpoint
-// lies within that distance.  Those few outputs are recomputed exactly (double-float) by a warp
-// each after the tile.
+// keeps its 64 matrix entries T[mh][i][64 half .. 64 half + 63] in registers and forms, for
+// every row, the fp32 FMA chain v_k = RN(v_{k-1} + T_ik x_k) over its half.  Each step adds an
+// error of at most u |v_k| (u = 2^-24), so with the halves' sums A = sum_k |v_k| and the final
+// v = RN(v_A + v_B), |v - y| <= u (A_A + A_B + |v|) for y = sum_j T_ij x_j (plus at most 2^-142
+// from underflow; the fp32 evaluation of the bound is covered by a factor 1 + 2^-16).  bf16(v)
+// is then the correctly rounded result unless a rounding midpoint lies within that distance;
+// those few outputs are recomputed exactly (double-float) by a warp each after the tile.
+// Loads are issued in the order that overlaps them: the destination's sequence index and
+// position, the matrix, the rows, and only then the dependent s_quant check.
 constexpr int kMaxRT = 16;
 __device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const RotTensor& T = P.t[tt];
@@ -112,28 +114,40 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const int mh = tile / tiles_per_mat;
   const int p0 = (tile % tiles_per_mat) * P.rt;
   const int np = min(P.rt, pairs - p0);
-  __shared__ float xs[kMaxRT][kHeadDim];
+  __shared__ __align__(16) float xs[kMaxRT][kHeadDim];
   __shared__ uint16_t* dst_sh[kMaxRT];
   __shared__ uint16_t fallback[kMaxRT * kHeadDim];      // (row << 7) | output, undecided outputs
   __shared__ int n_fallback;
   const int tid = threadIdx.x;
-  // matrix entries first: the longest-latency loads of the tile
+  int d_row = 0, d_head = 0, d_b = 0, d_p = 0;
+  if (tid < np) {
+    tile_row(T, mh, p0 + tid, d_row, d_head);
+    if (!T.is_query) {
+      d_b = P.seq_idx[d_row];
+      d_p = P.pos[d_row];
+    }
+  }
   const int i = tid >> 1, half = tid & 1;
   const float* mrow = T.mat + ((size_t)mh * kHeadDim + i) * kHeadDim;
   const float4* m4 = reinterpret_cast<const float4*>(mrow + 64 * half);
   float4 m[16];
 #pragma unroll
   for (int j4 = 0; j4 < 16; ++j4) m[j4] = m4[j4];
-  for (int e = tid; e < np * kHeadDim; e += blockDim.x) {
+  // rows: one 16-byte piece (8 bf16) per thread, 16 pieces per row
+  uint4 xr = make_uint4(0u, 0u, 0u, 0u);
+  const int xrow = tid >> 4, xpart = tid & 15;
+  if (xrow < np) {
     int row, head;
-    tile_row(T, mh, p0 + e / kHeadDim, row, head);
-    xs[e / kHeadDim][e % kHeadDim] =
-        bf16_bits_to_float(T.src[((size_t)row * T.heads + head) * kHeadDim + e % kHeadDim]);
+    tile_row(T, mh, p0 + xrow, row, head);
+    xr = reinterpret_cast<const uint4*>(T.src + ((size_t)row * T.heads + head) * kHeadDim)[xpart];
   }
-  if (tid < np) {
-    int row, head;
-    tile_row(T, mh, p0 + tid, row, head);
-    dst_sh[tid] = rot_dst(P, T, row, head, true);
+  if (tid < np) dst_sh[tid] = rot_dst(P, T, d_row, d_head, d_b, d_p, true);
+  if (xrow < np) {
+    float4* xd = reinterpret_cast<float4*>(&xs[xrow][8 * xpart]);
+    xd[0] = make_float4(__uint_as_float(xr.x << 16), __uint_as_float(xr.x & 0xffff0000u),
+                        __uint_as_float(xr.y << 16), __uint_as_float(xr.y & 0xffff0000u));
+    xd[1] = make_float4(__uint_as_float(xr.z << 16), __uint_as_float(xr.z & 0xffff0000u),
+                        __uint_as_float(xr.w << 16), __uint_as_float(xr.w & 0xffff0000u));
   }
   if (tid == 0) n_fallback = 0;
   __syncthreads();
@@ -145,15 +159,16 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
 #pragma unroll
     for (int j4 = 0; j4 < 16; ++j4) {
       const float4 xv = *reinterpret_cast<const float4*>(x + 4 * j4);
-      v = fmaf(m[j4].x, xv.x, v); a = fmaf(fabsf(m[j4].x), fabsf(xv.x), a);
-      v = fmaf(m[j4].y, xv.y, v); a = fmaf(fabsf(m[j4].y), fabsf(xv.y), a);
-      v = fmaf(m[j4].z, xv.z, v); a = fmaf(fabsf(m[j4].z), fabsf(xv.z), a);
-      v = fmaf(m[j4].w, xv.w, v); a = fmaf(fabsf(m[j4].w), fabsf(xv.w), a);
+      v = fmaf(m[j4].x, xv.x, v); a += fabsf(v);
+      v = fmaf(m[j4].y, xv.y, v); a += fabsf(v);
+      v = fmaf(m[j4].z, xv.z, v); a += fabsf(v);
+      v = fmaf(m[j4].w, xv.w, v); a += fabsf(v);
     }
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     a += __shfl_xor_sync(0xffffffffu, a, 1);
     if (half == 0) {
-      const int b = bf16_if_decided(v, a * 0x1p-17f);
+      const float e = fmaf(a + fabsf(v), 0x1.0001p-24f, 0x1p-140f);
+      const int b = bf16_if_decided(v, e);
       if (b >= 0) dst[i] = (uint16_t)b;
       else fallback[atomicAdd(&n_fallback, 1)] = (uint16_t)((r << 7) | i);
     }
@@ -184,7 +199,12 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
 __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   const RotTensor& T = P.t[tt];
   int row = item / T.heads, h = item % T.heads;
-  uint16_t* dst = rot_dst(P, T, row, h, lane == 0);
+  int b = 0, p = 0;
+  if (!T.is_query) {
+    b = P.seq_idx[row];
+    p = P.pos[row];
+  }
+  uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
   if (dst == nullptr) return;
   const uint16_t* src = T.src + ((size_t)row * T.heads + h) * kHeadDim;
   uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);

@@ -179,8 +179,10 @@ KVQ_API size_t kvq_page_bytes(const kvq_config* cfg);
  *            pos % ring_cap; pos must satisfy s_quant[b] <= pos < s_quant[b] +
  *            ring_cap for pos >= s_sink, otherwise the row is skipped with
  *            KVQ_ERR_BOUNDS in *d_status.  seq_len[b] is raised to pos + 1.
+ * q, k, v and the matrices must be 16-byte aligned, q_out 8-byte aligned
+ * (KVQ_ERR_INVALID_ARG otherwise).
  * Source: [WUSH] inference algorithm (transform each new key and query, append at
- * full precision); [OScaR] Algorithm 1 steps 5 and 11 (online FHT of K and Q). */
+ * full precision); [OScaR] algorithm, key and query processing (online FHT of K and Q). */
 KVQ_API int kv_rotate_qk(const kvq_config* cfg, const kvq_transform* tr,
                  const uint16_t* q, uint16_t* q_out, int32_t n_q_rows,
                  const uint16_t* k, const uint16_t* v,
@@ -190,8 +192,9 @@ KVQ_API int kv_rotate_qk(const kvq_config* cfg, const kvq_transform* tr,
 /* kv_quant_flush: apply the flush rule to every sequence: while seq_len - s_quant
  * >= s_keep + s_flush, quantize tokens [s_quant, s_quant + s_flush) of every kv
  * head from the BF16 ring into their INT2 page and advance s_quant.  At most
- * max_tokens_per_seq tokens (rounded down to whole spans) are quantized per
- * sequence by one call; the rest wait for the next call.  Per token (all float
+ * min(max_tokens_per_seq, ring_cap - s_keep) tokens (rounded down to whole
+ * spans) are quantized per sequence by one call; the rest wait for the next call
+ * (the ring never holds more than ring_cap - s_keep tokens past S_keep).  Per token (all float
  * operations IEEE round-to-nearest, none fused):
  *   key_l2norm (keys only): s = sqrt(sum x^2) in float64, s16 = fp16(s),
  *     y = x / s16 in float32 (y = 0 when s16 = 0);
@@ -203,8 +206,9 @@ KVQ_API int kv_rotate_qk(const kvq_config* cfg, const kvq_transform* tr,
  *     (1 if 0), z16 = 1.5 (not combined with key_l2norm);
  *   code = clamp(round_half_even(y / Delta16 + z16), 0, 3).
  * Source: [WUSH] inference algorithm (S_quant, S_flush-aligned spans, per-group
- * quantizer in place); [OSCAR] section 4 "KV Cache Update"; [OScaR] Algorithm 1
- * steps 6-9 and the integer-quantization formulas. */
+ * quantizer in place); [OSCAR] section 4 "KV Cache Update"; [OScaR] algorithm,
+ * key processing (norm, residual buffer quantized when full) and the
+ * integer-quantization formulas. */
 KVQ_API int kv_quant_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens_per_seq,
                    int32_t* d_status, void* stream);
 

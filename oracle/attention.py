@@ -5,7 +5,7 @@ query token ([OScaR] "KV 缓存的工作原理", decode-step attention; [OSCAR] 
 "Attention and KV cache"), with grouped-query attention: query head (h, i)
 reads kv head h, i.e. query head index h*g + i for g = Hq / Hkv ([WUSH]
 "分组查询注意力(GQA)").  Keys and values are the dequantized cache
-([OScaR] Algorithm 1 steps 14-17).  The output stays in the value
+([OScaR] algorithm, attention phase).  The output stays in the value
 transform's space; the caller's folded output projection undoes T_V ([WUSH]
 "方法步骤详情", W_O^c = W_O T_V^{-1}).
 """

@@ -5,7 +5,7 @@ Oracle module (test infrastructure only).
 Regions ([OSCAR] section 4 "KV Cache Layout": BF16 sink of the first S0 tokens,
 BF16 recent window, INT2 middle; [WUSH] "方法步骤详情": full-precision S_sink and
 S_keep windows, quantization right edge S_quant advanced over S_flush-aligned
-spans; [OScaR] Algorithm 1 steps 8-9: residual buffer quantized when full):
+spans; [OScaR] algorithm, key processing: residual buffer quantized when full):
 
     tokens [0, S_sink)          BF16 sink, never quantized
     tokens [S_sink, s_quant)    INT2 (codes + scale/zero-point [+ norm])

@@ -3,7 +3,7 @@
 Oracle module (test infrastructure only).  Follows the serving flow of the
 pages ([WUSH] "方法步骤详情" inference algorithm: transform new keys and
 queries, append at full precision, quantize S_flush-aligned spans beyond the
-windows, mixed-precision attention; [OScaR] Algorithm 1; [OSCAR] section 4):
+windows, mixed-precision attention; [OScaR] algorithm; [OSCAR] section 4):
 
 1. rotate every key row with T_K (or H), every value row with T_V (or keep it),
    and the decode query with T_K^{-T} (or H), each rounded once to BF16;

@@ -80,7 +80,7 @@ class Workload:
     s_flush: int = 8
     transform: str = "orthogonal"      # "orthogonal" | "hadamard" | "invertible" | "identity"
     value_transform: str = "orthogonal"  # "orthogonal" | "identity"
-    key_dist: str = "outlier"          # "outlier" | "fixed_outlier" | "lognormal_norm" | "degenerate"
+    key_dist: str = "outlier"          # "outlier" | "fixed_outlier" | "lognormal_norm" | "degenerate" | "wide_exponent"
     outlier_scale: float = 15.0
     n_outlier: int = 2
     fixed_outlier_channels: tuple = ()
@@ -251,6 +251,13 @@ def key_rows(w: Workload, b: int, h: int, n_tokens: int) -> np.ndarray:
             low = rng.choice(n_tokens, size=n_low, replace=False)
             norms[low] *= w.low_norm_scale
         x = dirs * norms.astype(np.float32)[:, None]
+    elif w.key_dist == "wide_exponent":
+        # every token at its own binary scale 2^e, e in [-120, 8]; half the channels of a row
+        # pushed down a further 2^0 .. 2^-110, so rows mix normal and tiny magnitudes
+        x = rng.standard_normal((n_tokens, d), dtype=np.float32).astype(np.float64)
+        e = rng.integers(-120, 9, size=n_tokens)
+        f = np.where(rng.random((n_tokens, d)) < 0.5, rng.integers(-110, 1, size=(n_tokens, d)), 0)
+        x = np.ldexp(x, e[:, None] + f).astype(np.float32)
     else:
         raise ValueError(w.key_dist)
     return f32_to_bf16_bits(x)

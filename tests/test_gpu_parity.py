@@ -98,6 +98,11 @@ EDGES = {
     "degenerate_rows": BASE.replace(key_dist="degenerate", group_size=32),
     "degenerate_rows_l2": BASE.replace(key_dist="degenerate", group_size=32, key_l2norm=True, kappa_k=1.0),
     "oscar_window_64_256": BASE.replace(s_sink=64, s_keep=256, ctx_lo=700, ctx_hi=700),
+    # magnitudes from 2^-230 (flushed to zero) to 2^10 reach the quantizer unrotated: scale
+    # divisions of tiny and huge quotients, subnormal codes and zero-scale rows
+    "wide_exponent": BASE.replace(key_dist="wide_exponent", transform="identity", group_size=32),
+    "wide_exponent_l2": BASE.replace(key_dist="wide_exponent", transform="identity", group_size=32,
+                                     key_l2norm=True, kappa_k=1.0),
 }
 
 

@@ -98,6 +98,13 @@ def test_rotate_validation(kvq):
                                   None, None, None) == 0
     assert kvq.lib().kv_rotate_qk(ctypes.byref(c), ctypes.byref(t), None, None, -1, None, None, None, None, 0,
                                   None, None, None) == -1
+    # rows are read 16 bytes at a time: an 8-byte aligned query or key pointer is rejected on the host
+    t = kvq.CTransform(0, 0, 4096, 4096, None)
+    fake = kvq.CCache(*([4096] * 9))
+    assert kvq.lib().kv_rotate_qk(ctypes.byref(c), ctypes.byref(t), 4104, 4096, 1, None, None, None, None, 0,
+                                  ctypes.byref(fake), None, None) == -1
+    assert kvq.lib().kv_rotate_qk(ctypes.byref(c), ctypes.byref(t), None, None, 0, 4104, 4096, 4096, 4096, 1,
+                                  ctypes.byref(fake), None, None) == -1
 
 
 def test_status_strings(kvq):
