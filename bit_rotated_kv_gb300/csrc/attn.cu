@@ -40,6 +40,9 @@ constexpr int kStages = 8;
 constexpr long long kWaitLimit = 1LL << 22;
 constexpr int kRow = 4 + kHeadDim;      // one (m, l, -, -, o[d]) record; o 16-byte aligned
 constexpr int kGroup = 8;               // splits merged together at the first merge level
+// partials of one (sequence, kv head) up to this size are merged in one level from shared memory
+// (two CTAs still fit on an SM); larger ones go through the two-level tree
+constexpr size_t kMerge1Bytes = 96 * 1024;
 
 struct AttnParams {
   const uint8_t* pages;
@@ -59,6 +62,7 @@ struct AttnParams {
   int batch, hkv, gqa, s_sink, ring_cap, max_pages, num_pages, group, l2, page_bytes;
   int n_int2, n_win, n_split;
   int mp;             // INT2 pages per sequence covered by the splits (host-known bound)
+  int merge1;         // 1: the last CTA of a unit merges every split partial from shared memory
   float scale_log2;   // sm_scale * log2(e)
 };
 
@@ -101,6 +105,9 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's earlier (acquired) view of global memory before its later bulk copies.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
@@ -227,10 +234,15 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     const int lp = first + k * kWarps;
     return (k < nk_max && lp < P.max_pages) ? ptab[lp] : -1;
   };
+  // Before waiting for the producer kernels (programmatic dependent launch): the page table is
+  // not written by them, so its entries are read now, and the first pages of this warp are
+  // pulled into L2 (a prefetch only -- the copies that the results use start after the wait).
   int pid_a = load_pids(0), pid_b = load_pids(1);
-  const int Lraw = P.seq_len[b];
-  const int sqraw = P.s_quant[b];
-
+  {
+    const int pid0 = __shfl_sync(0xffffffffu, pid_a, lane & (kStages - 1));
+    if (lane < kStages && lane < nk_max && pid0 >= 0 && pid0 < P.num_pages)
+      prefetch_l2_bulk(P.pages + ((size_t)pid0 * P.hkv + h) * P.page_bytes, (uint32_t)P.page_bytes);
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [kWarps][kStages]
   int* slot_pid = reinterpret_cast<int*>(smem + kWarps * kStages * 8);     // [kWarps][kStages]
   QShared* qs = reinterpret_cast<QShared*>(smem + kWarps * kStages * 12);
@@ -240,19 +252,11 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   int* my_pid = slot_pid + warp * kStages;
   if (lane < kStages) mbar_init(my_bars + lane, 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-
-  // ---- this warp's pages inside the INT2 region, and the first copies
-  const int L = Lraw;
-  const int sq = min(sqraw, L);
-  const int n_tok = max(0, sq - P.s_sink);
-  const int np = (n_tok + kPage - 1) / kPage;
-  if (split == 0 && threadIdx.x == 0 && np > P.mp) set_status(P.status, KVQ_ERR_BOUNDS);
-  const int pend = min(p1, np);
-  const int nk = first < pend ? (pend - first + kWarps - 1) / kWarps : 0;
-  auto issue = [&](int k, int pid) {       // lane 0 only
+  // copy page k of this warp into its slot (lane 0 only); an entry that is not a page id
+  // completes the slot without data and is reported when (if) the page is consumed
+  auto issue = [&](int k, int pid) {
     const int slot = k % kStages;
     if (pid < 0 || pid >= P.num_pages) {
-      set_status(P.status, KVQ_ERR_BOUNDS);
       my_pid[slot] = -1;
       mbar_arrive(my_bars + slot);
     } else {
@@ -263,11 +267,26 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     }
   };
   __syncwarp();
+  pdl_wait();
+  // the first kStages pages of the host-known range are copied at once, before the sequence's
+  // own extent is known; copies past the extent are waited for and dropped
+  const int n_first = min(kStages, nk_max);
 #pragma unroll
   for (int k = 0; k < kStages; ++k) {
     const int pid = __shfl_sync(0xffffffffu, pid_a, k);
-    if (lane == 0 && k < nk) issue(k, pid);
+    if (lane == 0 && k < n_first) issue(k, pid);
   }
+  const int Lraw = P.seq_len[b];
+  const int sqraw = P.s_quant[b];
+
+  // ---- this warp's pages inside the INT2 region
+  const int L = Lraw;
+  const int sq = min(sqraw, L);
+  const int n_tok = max(0, sq - P.s_sink);
+  const int np = (n_tok + kPage - 1) / kPage;
+  if (split == 0 && threadIdx.x == 0 && np > P.mp) set_status(P.status, KVQ_ERR_BOUNDS);
+  const int pend = min(p1, np);
+  const int nk = first < pend ? (pend - first + kWarps - 1) / kWarps : 0;
 
   // ---- queries (their loads fly while the first pages are copied): B fragments scaled into
   // fp16 range, per-head multipliers and group sums
@@ -350,6 +369,7 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     }
     const uint8_t* pg = my_ring + (size_t)slot * pb;
     const int pid = my_pid[slot];
+    if (pid < 0 && lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
     const int lp = first + k * kWarps;
     const int valid_tok = (pid < 0) ? 0 : min(kPage, n_tok - kPage * lp);
     const bool vA = tA < valid_tok, vB = tB < valid_tok;
@@ -477,12 +497,11 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     __syncwarp();
     if (lane == 0 && kk < nk) issue(kk, pid_next);
   }
-  if (timed_out) {
-    if (lane == 0) set_status(P.status, KVQ_ERR_TIMEOUT);
-    // let copies still in flight land before the CTA can exit (bounded)
-    for (int kk = k; kk < min(nk, k + kStages); ++kk)
-      (void)mbar_wait(my_bars + kk % kStages, (uint32_t)((kk / kStages) & 1));
-  }
+  if (timed_out && lane == 0) set_status(P.status, KVQ_ERR_TIMEOUT);
+  // copies not consumed (first copies past the extent; after a time-out, everything still in
+  // flight) land before the slots are reused or the CTA exits (bounded)
+  for (int kk = k; kk < max(min(nk, k + kStages), n_first); ++kk)
+    (void)mbar_wait(my_bars + kk % kStages, (uint32_t)((kk / kStages) & 1));
 
   // ---- per-warp result: reduce l over the 8 lanes of a column pair; the zero-point
   // correction of group gi, heads (hA, hB) sits in lane 4 gi + quad
@@ -520,6 +539,7 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
 __device__ void window_split(const AttnParams& P, int b, int h, int wsplit, float* res, size_t wstride) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = P.gqa;
+  pdl_wait();
   const int L = P.seq_len[b];
   const int n_sink = min(P.s_sink, max(L, 0));
   const int r0 = max(min(P.s_quant[b], L), P.s_sink);     // first recent token
@@ -739,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
   if (threadIdx.x == 0) Ps = Pk;
   __syncthreads();
   const AttnParams& P = Ps;
-  pdl_wait();
+  // (each branch below waits for the producer kernels itself, after its independent loads)
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int g = P.gqa;
   // per-warp results: an INT2 warp writes into its own (drained) page ring, a window warp
@@ -762,24 +782,72 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
     const int hh = idx / kHeadDim, j = idx % kHeadDim;
     merge_warps(res + hh * kRow, wstride, part + hh * kRow, j);
   }
-  // ---- two-level merge tree over the splits of this (sequence, kv head): the last CTA of
-  // every group of kGroup splits merges the group, the last group merger merges the groups.
-  // Tickets are atomic counters (no waiting); every merge issues all its loads at once.
   __syncthreads();
   __shared__ int role;
   const int unit = b * P.hkv + h;
+  if (P.merge1) {
+    // ---- one-level merge: the last CTA of this (sequence, kv head) -- an atomic ticket, no
+    // waiting -- pulls every split partial into shared memory with one bulk copy and merges.
+    int32_t* cnt1 = P.count + (size_t)unit;
+    if (threadIdx.x == 0) {
+      const int t = atomic_add_acq_rel_gpu(cnt1, 1);   // releases this CTA's partial
+      role = (t == P.n_split - 1);                      // ... and acquires the others'
+      if (role) *cnt1 = 0;
+    }
+    __syncthreads();
+    if (!role) return;
+    __shared__ __align__(8) uint64_t mbar;
+    float* buf = reinterpret_cast<float*>(smem + 1024);
+    const uint32_t bytes = (uint32_t)((size_t)P.n_split * g * kRow * sizeof(float));
+    if (threadIdx.x == 0) {
+      fence_proxy_async_all();         // the acquired partials, seen by the bulk copy below
+      mbar_init(&mbar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      mbar_arrive_tx(&mbar, bytes);
+      tma_load_1d(buf, P.part + (size_t)unit * P.n_split * g * kRow, bytes, &mbar);
+    }
+    __syncthreads();
+    bool ok = mbar_wait(&mbar, 0u);
+    if (!ok) {
+      if (threadIdx.x == 0) set_status(P.status, KVQ_ERR_TIMEOUT);
+      (void)mbar_wait(&mbar, 0u);      // the copy must land before the CTA can exit (bounded)
+      return;
+    }
+    // warp hh merges head hh, lane the channels 4*lane .. 4*lane + 3
+    const int lane = threadIdx.x & 31, hh = threadIdx.x >> 5;
+    if (hh >= g) return;
+    float M = -INFINITY;
+    for (int i = lane; i < P.n_split; i += 32) M = fmaxf(M, buf[((size_t)i * g + hh) * kRow]);
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float Ls = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int i = 0; i < P.n_split; ++i) {
+        const float* r = buf + ((size_t)i * g + hh) * kRow;
+        const float mi = r[0];
+        const float f = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
+        const float4 oi = reinterpret_cast<const float4*>(r + 4)[lane];
+        Ls += r[1] * f;
+        O.x += oi.x * f; O.y += oi.y * f; O.z += oi.z * f; O.w += oi.w * f;
+      }
+    }
+    const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
+    reinterpret_cast<float4*>(P.out + ((size_t)unit * g + hh) * kHeadDim)[lane] =
+        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    return;
+  }
+  // ---- two-level merge tree over the splits of this (sequence, kv head): the last CTA of
+  // every group of kGroup splits merges the group, the last group merger merges the groups.
+  // Tickets are atomic counters (no waiting); every merge issues all its loads at once.
   const int n_grp = (P.n_split + kGroup - 1) / kGroup;
   const int grp = split / kGroup;
   const int gsize = min(kGroup, P.n_split - grp * kGroup);
   int32_t* cnt = P.count + (size_t)unit * (n_grp + 1);
   if (threadIdx.x == 0) {
-    __threadfence();
-    const int t = atomicAdd(cnt + grp, 1);
+    const int t = atomic_add_acq_rel_gpu(cnt + grp, 1);
     role = (t == gsize - 1);
-    if (role) {
-      cnt[grp] = 0;
-      __threadfence();
-    }
+    if (role) cnt[grp] = 0;
   }
   __syncthreads();
   if (!role) return;
@@ -792,13 +860,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
   merge_global(gsrc, gsize, g, P.part2 + ((size_t)unit * n_grp + grp) * g * kRow, false);
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const int t = atomicAdd(cnt + n_grp, 1);
+    const int t = atomic_add_acq_rel_gpu(cnt + n_grp, 1);
     role = (t == n_grp - 1);
-    if (role) {
-      cnt[n_grp] = 0;
-      __threadfence();
-    }
+    if (role) cnt[n_grp] = 0;
   }
   __syncthreads();
   if (!role) return;
@@ -891,7 +955,10 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
   const int ng = kHeadDim / cfg->group_size;
   const size_t ring_bytes = (size_t)kWarps * kStages * P.page_bytes;
   const size_t res_bytes = (size_t)kWarps * P.gqa * kRow * sizeof(float);
-  const size_t smem = 1024 + (ring_bytes > res_bytes ? ring_bytes : res_bytes);
+  const size_t merge_bytes = (size_t)P.n_split * P.gqa * kRow * sizeof(float);
+  P.merge1 = merge_bytes <= kMerge1Bytes;
+  size_t smem = 1024 + (ring_bytes > res_bytes ? ring_bytes : res_bytes);
+  if (P.merge1 && 1024 + merge_bytes > smem) smem = 1024 + merge_bytes;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   static unsigned long long attr_done = 0ull;

@@ -106,6 +106,24 @@ __device__ __forceinline__ __half double_to_half_rn(double d) {
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Ticket counter: atomic add with release (this CTA's prior writes, ordered before by a CTA
+// barrier) and acquire (the writes released by earlier tickets) semantics at GPU scope.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Warm L2 with [src, src + bytes) (16-byte aligned, multiple of 16) or with the line holding
+// src: no data reaches the SM and nothing is ordered, so a kernel may issue these before its
+// producer kernel has finished (before pdl_wait); the reads that count come after the wait.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_line(const void* src) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(src) : "memory");
+}
+
 template <typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                               Args... args) {

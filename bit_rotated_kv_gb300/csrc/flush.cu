@@ -183,9 +183,24 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
   if (threadIdx.x == 0) Ps = Pk;
   __syncthreads();
   const FlushParams& P = Ps;
-  pdl_wait();
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  {
+    // Before waiting for the producer kernels: warm L2 with this warp's first ring row and
+    // page-table entry, located from the s_quant seen now (a prefetch only: everything that
+    // counts is read again after the wait).
+    const int sq_g = P.s_quant[b];
+    const int r0 = (blockIdx.x * P.items_per_cta + warp) >> 1;
+    const int t = r0 / P.hkv, hh = r0 - t * P.hkv;
+    const int tok = sq_g + t;
+    if (lane < 2 && tok >= P.s_sink) {
+      const uint16_t* ring = (warp & 1) ? P.ring_v : P.ring_k;
+      prefetch_l2_line(ring + (((size_t)b * P.hkv + hh) * P.ring_cap + tok % P.ring_cap) * kHeadDim + 64 * lane);
+      const int pidx = (tok - P.s_sink) >> 4;
+      if (lane == 0 && pidx < P.max_pages) prefetch_l2_line(P.page_table + (size_t)b * P.max_pages + pidx);
+    }
+  }
+  pdl_wait();
   const int nwarps = blockDim.x >> 5;
   // every warp derives the span itself (no block barrier before the first load)
   const int L = P.seq_len[b], sq = P.s_quant[b];
@@ -314,12 +329,10 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
   if (threadIdx.x == 0 && gridDim.x == 1) {
     P.s_quant[b] = sq + n;
   } else if (threadIdx.x == 0) {
-    __threadfence();
-    int ticket = atomicAdd(P.counters + b, 1);
+    const int ticket = atomic_add_acq_rel_gpu(P.counters + b, 1);
     if (ticket == (int)gridDim.x - 1) {
       P.s_quant[b] = sq + n;
       P.counters[b] = 0;
-      __threadfence();
     }
   }
 }

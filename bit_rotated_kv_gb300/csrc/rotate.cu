@@ -141,6 +141,9 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
     tile_row(T, mh, p0 + xrow, row, head);
     xr = reinterpret_cast<const uint4*>(T.src + ((size_t)row * T.heads + head) * kHeadDim)[xpart];
   }
+  // everything above reads only the caller's inputs, which the kernels of this library never
+  // write: it overlaps the producer kernel; the cache state (s_quant, seq_len) comes after
+  pdl_wait();
   if (tid < np) dst_sh[tid] = rot_dst(P, T, d_row, d_head, d_b, d_p, true);
   if (xrow < np) {
     float4* xd = reinterpret_cast<float4*>(&xs[xrow][8 * xpart]);
@@ -204,10 +207,11 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
     b = P.seq_idx[row];
     p = P.pos[row];
   }
-  uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
-  if (dst == nullptr) return;
   const uint16_t* src = T.src + ((size_t)row * T.heads + h) * kHeadDim;
   uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
+  pdl_wait();                           // (the caller's inputs above: see dense_tile)
+  uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
+  if (dst == nullptr) return;
   if (T.mode == ROT_COPY) {
     *reinterpret_cast<uint2*>(dst + 4 * lane) = raw;
     return;
@@ -268,8 +272,8 @@ __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
   if (threadIdx.x == 0) Ps = Pk;
   __syncthreads();
   const RotParams& P = Ps;
-  pdl_wait();
   int blk = blockIdx.x;
+  // each path waits for the producer kernels itself, after loading the caller's inputs
   if (blk < P.dense_total) {
     int tt, item;
     find_item(P.n_dense, blk, tt, item);
@@ -277,7 +281,10 @@ __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
     return;
   }
   int w = (blk - P.dense_total) * 8 + (threadIdx.x >> 5);
-  if (w >= P.warp_total) return;
+  if (w >= P.warp_total) {
+    pdl_wait();
+    return;
+  }
   int tt, item;
   find_item(P.n_warp, w, tt, item);
   warp_item(P, tt, item, threadIdx.x & 31);
