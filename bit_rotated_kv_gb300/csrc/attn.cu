@@ -31,6 +31,7 @@
 #include "launch.h"
 
 #include <mutex>
+#include <type_traits>
 
 namespace kvq {
 
@@ -130,6 +131,12 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// 2^x (MUFU; about 2 ulp, -inf -> 0): the softmax weights need no more
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -212,7 +219,7 @@ __device__ __forceinline__ void load_scales(const uint8_t* p, uint32_t (&o)[NG])
   }
 }
 
-template <int NG>
+template <int NG, bool L2>
 __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int split, float* res,
                            size_t wstride) {
   // accumulators per group; with fewer than 4 groups the k-steps alternate between two
@@ -339,16 +346,38 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   __syncthreads();
 
   const int hA = 2 * quad, hB = 2 * quad + 1;
-  const float multA = qs->mult[hA], multB = qs->mult[hB];
+  // Loop constants in registers: the parameter block lives in shared memory and would be
+  // re-read after every barrier operation.  Scores are
+  //   s = x_t (mult_h sum_g Delta_g acc_g - sum_g Delta_g z_g qsum_g),
+  // x_t = scale_log2 * norm_t with key norms, else scale_log2 folded into mult and qsum here.
+  const float xs = P.scale_log2;
+  const float fx = L2 ? 1.f : xs;
+  const float multA = qs->mult[hA] * fx, multB = qs->mult[hB] * fx;
   float qsA[NG], qsB[NG];
 #pragma unroll
-  for (int gi = 0; gi < NG; ++gi) { qsA[gi] = qs->qsum[hA][gi]; qsB[gi] = qs->qsum[hB][gi]; }
+  for (int gi = 0; gi < NG; ++gi) { qsA[gi] = qs->qsum[hA][gi] * fx; qsB[gi] = qs->qsum[hB][gi] * fx; }
+  const int num_pages = P.num_pages;
+  const uint8_t* const page_base = P.pages + (size_t)h * pb;
+  const int page_stride = P.hkv * pb;
+  auto refill = [&](int kk, int pid) {     // lane 0 only: page kk of this warp into its slot
+    const int slot = kk & (kStages - 1);
+    if ((unsigned)pid >= (unsigned)num_pages) {
+      my_pid[slot] = -1;
+      mbar_arrive(my_bars + slot);
+    } else {
+      my_pid[slot] = pid;
+      mbar_arrive_tx(my_bars + slot, (uint32_t)pb);
+      tma_load_1d(my_ring + slot * pb, page_base + (size_t)pid * page_stride, (uint32_t)pb, my_bars + slot);
+    }
+  };
 
-  // the reference maximum starts at a finite "minus infinity" so that fully masked pages
-  // (scores -inf) give p = 0 on the lazy path
-  Softmax sm;
-  sm.m[0] = sm.m[1] = -1e30f;
-  sm.l[0] = sm.l[1] = 0.f;
+  // Online softmax with a lazy reference maximum m: probabilities are p = exp2(s - m), with m
+  // moved only when a score exceeds it by more than 8, so p <= 2^8.  The loop keeps
+  // mb = m + 8 and works with p' = exp2(s - mb) = p 2^-8 <= 1 (the fp16 B operand of P V);
+  // l accumulates p' as well and is scaled back at the end.  mb starts at a finite "minus
+  // infinity" so that fully masked pages (scores -inf) give p' = 0 on the lazy path.
+  float mb[2] = {-1e30f, -1e30f};
+  float lsum[2] = {0.f, 0.f};
   float o[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt)
@@ -358,31 +387,25 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   float corr[4] = {0.f, 0.f, 0.f, 0.f};
 
   const int tA = lane >> 2, tB = tA + 8;
-  bool timed_out = false;
-  int chunk_a = 0;               // page-table chunk held in pid_a
-  int k = 0;
-  for (; k < nk; ++k) {
-    const int slot = k % kStages;
-    if (!mbar_wait(my_bars + slot, (uint32_t)((k / kStages) & 1))) {
-      timed_out = true;
-      break;
-    }
-    const uint8_t* pg = my_ring + (size_t)slot * pb;
-    const int pid = my_pid[slot];
-    if (pid < 0 && lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
-    const int lp = first + k * kWarps;
-    const int valid_tok = (pid < 0) ? 0 : min(kPage, n_tok - kPage * lp);
-    const bool vA = tA < valid_tok, vB = tB < valid_tok;
-    // fragments and scales
-    const uint4 wk = *reinterpret_cast<const uint4*>(pg + 16 * lane);
+  const int off_kw = 16 * lane, off_vw = kCodeBytes + 16 * lane;
+  const int off_skA = k_scale_off() + tA * NG * 4, off_skB = k_scale_off() + tB * NG * 4;
+  const int off_dv0 = v_delta_off(NG, 2 * quad, 0), off_dv1 = v_delta_off(NG, 2 * quad + 8, 0);
+  const int off_zp0 = v_zero_off(NG, 2 * quad, hrow < NG ? hrow : 0);
+  const int off_zp1 = v_zero_off(NG, 2 * quad + 8, hrow < NG ? hrow : 0);
+
+  // One page: scores, softmax, P V.  MASKED pages (the sequence's last, partial page, or an
+  // entry that is not a page id) keep only their first valid_tok tokens.
+  auto page = [&](const uint8_t* pg, int valid_tok, auto masked) {
+    constexpr bool MASKED = decltype(masked)::value;
+    const uint4 wk = *reinterpret_cast<const uint4*>(pg + off_kw);
     uint32_t skA[NG], skB[NG];
-    load_scales<NG>(pg + k_scale_off() + tA * NG * 4, skA);
-    load_scales<NG>(pg + k_scale_off() + tB * NG * 4, skB);
-    float nA = 1.f, nB = 1.f;
-    if (P.l2) {
+    load_scales<NG>(pg + off_skA, skA);
+    load_scales<NG>(pg + off_skB, skB);
+    float xA = 1.f, xB = 1.f;
+    if constexpr (L2) {
       const __half* nrm = reinterpret_cast<const __half*>(pg + norm_off(NG));
-      nA = __half2float(nrm[tA]);
-      nB = __half2float(nrm[tB]);
+      xA = xs * __half2float(nrm[tA]);
+      xB = xs * __half2float(nrm[tB]);
     }
     // ---- scores: codes x q' per group
     const uint32_t kw[4] = {wk.x, wk.y, wk.z, wk.w};
@@ -400,7 +423,6 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     }
     float sc[4];
     {
-      // s = scale * norm * (mult_h * sum_g Delta_g acc_g - sum_g Delta_g z_g qsum_g)
       float sA0 = 0.f, sA1 = 0.f, sB0 = 0.f, sB1 = 0.f, cA0 = 0.f, cA1 = 0.f, cB0 = 0.f, cB1 = 0.f;
 #pragma unroll
       for (int gi = 0; gi < NG; ++gi) {
@@ -415,51 +437,63 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
         cA0 = fmaf(pzA, qsA[gi], cA0); cA1 = fmaf(pzA, qsB[gi], cA1);
         cB0 = fmaf(pzB, qsA[gi], cB0); cB1 = fmaf(pzB, qsB[gi], cB1);
       }
-      const float xA = P.scale_log2 * nA, xB = P.scale_log2 * nB;
-      sc[0] = vA ? (sA0 * multA - cA0) * xA : -INFINITY;
-      sc[1] = vA ? (sA1 * multB - cA1) * xA : -INFINITY;
-      sc[2] = vB ? (sB0 * multA - cB0) * xB : -INFINITY;
-      sc[3] = vB ? (sB1 * multB - cB1) * xB : -INFINITY;
-    }
-    // Lazy reference maximum: probabilities are exp2(s - m) with m moved only when a score
-    // exceeds it by more than 8, so p <= 2^8 (the B operand carries p * 2^-8).
-    float p[4];
-    {
-      const bool up = (fmaxf(sc[0], sc[2]) > sm.m[0] + 8.f) || (fmaxf(sc[1], sc[3]) > sm.m[1] + 8.f);
-      if (__any_sync(0xffffffffu, up)) {
-        float alpha[2];
-        softmax_step(sm, sc, p, alpha);
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          o[mt][0] *= alpha[0]; o[mt][2] *= alpha[0];
-          o[mt][1] *= alpha[1]; o[mt][3] *= alpha[1];
-        }
-        corr[0] *= alpha[0];
-        corr[1] *= alpha[1];
-      } else {
-        p[0] = exp2f(sc[0] - sm.m[0]);
-        p[1] = exp2f(sc[1] - sm.m[1]);
-        p[2] = exp2f(sc[2] - sm.m[0]);
-        p[3] = exp2f(sc[3] - sm.m[1]);
-        sm.l[0] += p[0] + p[2];
-        sm.l[1] += p[1] + p[3];
+      sc[0] = fmaf(sA0, multA, -cA0);
+      sc[1] = fmaf(sA1, multB, -cA1);
+      sc[2] = fmaf(sB0, multA, -cB0);
+      sc[3] = fmaf(sB1, multB, -cB1);
+      if constexpr (L2) {
+        sc[0] *= xA; sc[1] *= xA; sc[2] *= xB; sc[3] *= xB;
+      }
+      if constexpr (MASKED) {
+        if (tA >= valid_tok) sc[0] = sc[1] = -INFINITY;
+        if (tB >= valid_tok) sc[2] = sc[3] = -INFINITY;
       }
     }
-    // ---- P V: per value group, W = P * Delta_v as the B operand (fp16)
-    // P in the B-fragment layout (tokens 2q, 2q+1 | 2q+8, 2q+9 of head lane/4), then one
+    float p[4];
+    {
+      const bool up = (fmaxf(sc[0], sc[2]) > mb[0]) || (fmaxf(sc[1], sc[3]) > mb[1]);
+      if (__any_sync(0xffffffffu, up)) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float mx = fmaxf(sc[c], sc[c + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          // the new reference: the running maximum (never below the old reference)
+          const float nb = fmaxf(mb[c], mx + 8.f);
+          const float alpha = ex2_approx(mb[c] - nb);
+          mb[c] = nb;
+          p[c] = ex2_approx(sc[c] - nb);
+          p[c + 2] = ex2_approx(sc[c + 2] - nb);
+          lsum[c] = fmaf(lsum[c], alpha, p[c] + p[c + 2]);
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) { o[mt][c] *= alpha; o[mt][c + 2] *= alpha; }
+          corr[c] *= alpha;
+        }
+      } else {
+        p[0] = ex2_approx(sc[0] - mb[0]);
+        p[1] = ex2_approx(sc[1] - mb[1]);
+        p[2] = ex2_approx(sc[2] - mb[0]);
+        p[3] = ex2_approx(sc[3] - mb[1]);
+        lsum[0] += p[0] + p[2];
+        lsum[1] += p[1] + p[3];
+      }
+    }
+    // ---- P V: per value group, W = P' * Delta_v as the B operand (fp16)
+    // P' in the B-fragment layout (tokens 2q, 2q+1 | 2q+8, 2q+9 of head lane/4), then one
     // HMUL2 per group with the Delta_v pairs of the same tokens
-    const uint32_t pb0 = movmatrix_trans(pack_half2(p[0] * 0.00390625f, p[1] * 0.00390625f));
-    const uint32_t pb1 = movmatrix_trans(pack_half2(p[2] * 0.00390625f, p[3] * 0.00390625f));
-    const uint4 wv = *reinterpret_cast<const uint4*>(pg + kCodeBytes + 16 * lane);
+    const uint32_t pb0 = movmatrix_trans(pack_half2(p[0], p[1]));
+    const uint32_t pb1 = movmatrix_trans(pack_half2(p[2], p[3]));
+    const uint4 wv = *reinterpret_cast<const uint4*>(pg + off_vw);
     uint32_t dv0[NG], dv1[NG];
-    load_scales<NG>(pg + v_delta_off(NG, 2 * quad, 0), dv0);
-    load_scales<NG>(pg + v_delta_off(NG, 2 * quad + 8, 0), dv1);
+    load_scales<NG>(pg + off_dv0, dv0);
+    load_scales<NG>(pg + off_dv1, dv1);
     uint32_t zp0 = 0u, zp1 = 0u;                       // z_v pairs of group lane/4
     if (hrow < NG) {
-      zp0 = *reinterpret_cast<const uint32_t*>(pg + v_zero_off(NG, 2 * quad, hrow));
-      zp1 = *reinterpret_cast<const uint32_t*>(pg + v_zero_off(NG, 2 * quad + 8, hrow));
+      zp0 = *reinterpret_cast<const uint32_t*>(pg + off_zp0);
+      zp1 = *reinterpret_cast<const uint32_t*>(pg + off_zp1);
     }
-    if (valid_tok < kPage) {                           // partial or skipped page: clear dead tokens
+    if constexpr (MASKED) {                            // clear the dead tokens' scale data
       const uint32_t m0 = (2 * quad < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 1 < valid_tok ? 0xffff0000u : 0u);
       const uint32_t m1 = (2 * quad + 8 < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 9 < valid_tok ? 0xffff0000u : 0u);
 #pragma unroll
@@ -485,6 +519,26 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
       const int gi = (16 * mt) / (kHeadDim / NG);
       mma_f16(o[mt], a, bw[gi][0], bw[gi][1]);
     }
+  };
+
+  bool timed_out = false;
+  int chunk_a = 0;               // page-table chunk held in pid_a
+  int k = 0;
+  for (; k < nk; ++k) {
+    const int slot = k & (kStages - 1);
+    if (!mbar_wait(my_bars + slot, ((unsigned)k / kStages) & 1u)) {
+      timed_out = true;
+      break;
+    }
+    const uint8_t* pg = my_ring + slot * pb;
+    const int pid = my_pid[slot];
+    const int lp = first + k * kWarps;
+    if (pid >= 0 && kPage * (lp + 1) <= n_tok) {
+      page(pg, kPage, std::false_type{});
+    } else {
+      if (pid < 0 && lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
+      page(pg, pid < 0 ? 0 : min(kPage, n_tok - kPage * lp), std::true_type{});
+    }
     // every lane has consumed this slot: refill it with the page kStages ahead, whose
     // page-table entry was fetched a chunk earlier
     const int kk = k + kStages;
@@ -495,8 +549,14 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     }
     const int pid_next = __shfl_sync(0xffffffffu, pid_a, kk & 31);
     __syncwarp();
-    if (lane == 0 && kk < nk) issue(kk, pid_next);
+    if (lane == 0 && kk < nk) refill(kk, pid_next);
   }
+  // l was accumulated in units of 2^-8 (see above); m is the reference without the bias
+  Softmax sm;
+  sm.m[0] = mb[0] - 8.f;
+  sm.m[1] = mb[1] - 8.f;
+  sm.l[0] = lsum[0] * 256.f;
+  sm.l[1] = lsum[1] * 256.f;
   if (timed_out && lane == 0) set_status(P.status, KVQ_ERR_TIMEOUT);
   // copies not consumed (first copies past the extent; after a time-out, everything still in
   // flight) land before the slots are reused or the CTA exits (bounded)
@@ -751,7 +811,10 @@ __device__ __noinline__ void merge_global(const float* src, int n, int g, float*
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnParams Pk, int ng_sel) {
+// One kernel per (groups per row, key norms) variant, so that each launch's code is only its own
+// page loop (a short loop per warp is sensitive to instruction-fetch misses).
+template <int NG, bool L2>
+__global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnParams Pk) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_trigger();
   // shared-memory copy of the parameters (device functions take references to it)
@@ -768,9 +831,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
   size_t wstride;
   if (split < P.n_int2) {
     wstride = (size_t)kStages * P.page_bytes / sizeof(float);
-    if (ng_sel == 1) int2_split<1>(P, smem, b, h, split, res, wstride);
-    else if (ng_sel == 2) int2_split<2>(P, smem, b, h, split, res, wstride);
-    else int2_split<4>(P, smem, b, h, split, res, wstride);
+    int2_split<NG, L2>(P, smem, b, h, split, res, wstride);
   } else {
     wstride = (size_t)g * kRow;
     window_split(P, b, h, split - P.n_int2, res, wstride);
@@ -959,18 +1020,30 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
   P.merge1 = merge_bytes <= kMerge1Bytes;
   size_t smem = 1024 + (ring_bytes > res_bytes ? ring_bytes : res_bytes);
   if (P.merge1 && 1024 + merge_bytes > smem) smem = 1024 + merge_bytes;
+  void (*kern)(const AttnParams) = nullptr;
+  int vi = 0;
+  if (cfg->key_l2norm) {
+    kern = ng == 1 ? attn_decode_kernel<1, true> : ng == 2 ? attn_decode_kernel<2, true> : attn_decode_kernel<4, true>;
+    vi = ng == 1 ? 3 : ng == 2 ? 4 : 5;
+  } else {
+    kern = ng == 1 ? attn_decode_kernel<1, false> : ng == 2 ? attn_decode_kernel<2, false> : attn_decode_kernel<4, false>;
+    vi = ng == 1 ? 0 : ng == 2 ? 1 : 2;
+  }
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
-  static unsigned long long attr_done = 0ull;
-  if (dev < 64 && !(attr_done & (1ull << dev))) {
-    if (cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) !=
-        cudaSuccess)
-      return KVQ_ERR_CUDA;
-    attr_done |= 1ull << dev;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
+  // the dynamic shared-memory limit is raised once per (device, kernel variant)
+  static std::mutex mu;
+  static unsigned long long attr_done[6] = {};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!(attr_done[vi] & (1ull << dev))) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) != cudaSuccess)
+        return KVQ_ERR_CUDA;
+      attr_done[vi] |= 1ull << dev;
+    }
   }
   dim3 grid(P.n_split, cfg->n_kv_heads, cfg->batch);
-  return launch_pdl(attn_decode_kernel, grid, dim3(kThreads), smem, stream, P, ng) == cudaSuccess ? KVQ_OK
-                                                                                             : KVQ_ERR_CUDA;
+  return launch_pdl(kern, grid, dim3(kThreads), smem, stream, P) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 // ---- allocation-free variant ---------------------------------------------------------------
