@@ -365,7 +365,7 @@ def oracle_step_sample(config: int, budget_s: float) -> dict:
     done = 0
     spent = 0.0
     i = 0
-    while spent < budget_s and i < 4 * len(units):
+    while spent < budget_s and i < 100000:
         b, h = units[i % len(units)]
         i += 1
         ui = synth.unit_inputs(w, b, h, lengths)

@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
         l.kvq_status_string.restype = ctypes.c_char_p
         l.kvq_version.argtypes = []
         l.kvq_version.restype = ctypes.c_int
+        l.kvq_selftest_scale_division.argtypes = [vp, vp]
+        l.kvq_selftest_scale_division.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -245,6 +247,13 @@ def kv_attn_decode_noalloc(cfg: KVConfig, cache: KVCache, q_rot, out, sm_scale: 
     rc = lib().kv_attn_decode_noalloc(ctypes.byref(c), ctypes.byref(cc), _ptr(q_rot), _ptr(out), float(sm_scale),
                                       int(max_ctx), _ptr(status), _stream(stream))
     _check(rc, "kv_attn_decode_noalloc")
+
+
+def kvq_selftest_scale_division(mismatches, stream=None) -> None:
+    """Device self-check of the quantizer's scale division against IEEE division; adds the
+    number of differing results to `mismatches` (a zeroed int64 device tensor of one element)."""
+    rc = lib().kvq_selftest_scale_division(_ptr(mismatches), _stream(stream))
+    _check(rc, "kvq_selftest_scale_division")
 
 
 def workspace(cfg: KVConfig, max_ctx: int, device="cuda") -> torch.Tensor:

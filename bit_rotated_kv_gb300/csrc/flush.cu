@@ -337,9 +337,48 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
   }
 }
 
+// ---- self-check of the scale division ------------------------------------------------------
+// div_by_scale against IEEE division for every finite bf16 y and every positive finite
+// float16 d (the whole domain of the unscaled quantizer: 65,280 x 31,743 pairs), plus 2^29
+// hashed float32 y (the l2-scaled keys); counts bitwise differences (NaN equals NaN).
+__device__ __forceinline__ void div_compare(float y, float d, float r, unsigned long long* bad) {
+  const float a = div_by_scale(y, d, r), b = __fdiv_rn(y, d);
+  if (__float_as_uint(a) != __float_as_uint(b) && !(isnan(a) && isnan(b))) atomicAdd(bad, 1ull);
+}
+__global__ void div_selftest_exhaustive(unsigned long long* bad) {
+  const float d = __half2float(__ushort_as_half((uint16_t)(blockIdx.x + 1)));   // 0x0001 .. 0x7bff
+  const float r = __frcp_rn(d);
+  for (uint32_t yb = threadIdx.x; yb < 65536u; yb += blockDim.x) {
+    if (((yb >> 7) & 0xffu) == 0xffu) continue;                                // bf16 inf / NaN
+    div_compare(__uint_as_float(yb << 16), d, r, bad);
+  }
+}
+__device__ __forceinline__ uint32_t mix32(uint32_t x) {
+  x ^= x >> 16; x *= 0x7feb352du; x ^= x >> 15; x *= 0x846ca68bu; x ^= x >> 16;
+  return x;
+}
+__global__ void div_selftest_random(unsigned long long* bad) {
+  const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+  for (uint32_t k = 0; k < 64; ++k) {
+    const uint32_t h1 = mix32(t * 64u + k), h2 = mix32(h1 ^ 0x5bd1e995u);
+    const float d = __half2float(__ushort_as_half((uint16_t)(1u + h2 % 0x7bffu)));
+    // half of the samples uniform over float32 bit patterns, half with exponents near 1
+    const uint32_t yb = (k & 1u) ? h1 : ((h1 & 0x807fffffu) | ((96u + (h1 >> 24) % 64u) << 23));
+    if (((yb >> 23) & 0xffu) == 0xffu) continue;
+    div_compare(__uint_as_float(yb), d, __frcp_rn(d), bad);
+  }
+}
+
 }  // namespace kvq
 
 using namespace kvq;
+
+extern "C" int kvq_launch_div_selftest(unsigned long long* d_mismatches, cudaStream_t stream) {
+  div_selftest_exhaustive<<<0x7bff, 256, 0, stream>>>(d_mismatches);
+  if (cudaGetLastError() != cudaSuccess) return KVQ_ERR_CUDA;
+  div_selftest_random<<<kSms * 64, 256, 0, stream>>>(d_mismatches);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
 
 static void kappa_pos(int g, double kappa, int& i, float& f) {
   double pos = (double)(g - 1) * kappa;

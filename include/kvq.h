@@ -263,6 +263,15 @@ KVQ_API size_t kv_attn_workspace_bytes(const kvq_config* cfg, int32_t max_ctx);
 /* Static description of a status code. */
 KVQ_API const char* kvq_status_string(int code);
 
+/* kvq_selftest_scale_division: the quantizer divides by a float16 scale with a
+ * correctly rounded reciprocal and one exact-remainder correction instead of an IEEE
+ * division.  This launches a check of that path against IEEE division on the device:
+ * every finite bf16 dividend with every positive finite float16 scale, plus 2^29 hashed
+ * float32 dividends (the l2-scaled keys); the number of bitwise differences is ADDED to
+ * *d_mismatches (a device uint64 the caller zeroes).  Not part of the method on the pages:
+ * a self-test of this implementation.  Returns KVQ_ERR_INVALID_ARG for a NULL pointer. */
+KVQ_API int kvq_selftest_scale_division(unsigned long long* d_mismatches, void* stream);
+
 /* Library ABI version (major * 100 + minor). */
 KVQ_API int kvq_version(void);
 

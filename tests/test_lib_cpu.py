@@ -107,6 +107,10 @@ def test_rotate_validation(kvq):
                                   ctypes.byref(fake), None, None) == -1
 
 
+def test_selftest_rejects_null(kvq):
+    assert kvq.lib().kvq_selftest_scale_division(None, None) == -1
+
+
 def test_status_strings(kvq):
     for code in range(0, -8, -1):
         assert kvq.kvq_status_string(code) != "unknown status"
