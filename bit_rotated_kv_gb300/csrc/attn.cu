@@ -91,10 +91,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait; false when the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (long long i = 0; i < kWaitLimit; ++i)
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
+  for (int i = 0; i < (int)kWaitLimit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity);
 }
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -253,7 +256,7 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [kWarps][kStages]
   int* slot_pid = reinterpret_cast<int*>(smem + kWarps * kStages * 8);     // [kWarps][kStages]
   QShared* qs = reinterpret_cast<QShared*>(smem + kWarps * kStages * 12);
-  const int pb = P.page_bytes;
+  constexpr int pb = (2 * kCodeBytes + 2 * kPage * NG * 4 + (L2 ? kPage * 2 : 0) + 31) / 32 * 32;
   uint8_t* my_ring = smem + 1024 + (size_t)warp * kStages * pb;            // [kStages][page_bytes]
   uint64_t* my_bars = bars + warp * kStages;
   int* my_pid = slot_pid + warp * kStages;
