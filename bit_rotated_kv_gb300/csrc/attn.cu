@@ -161,6 +161,12 @@ __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
+// a * b - c in one rounding (fp16x2)
+__device__ __forceinline__ uint32_t hfma2_neg_bits(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b),
+                      __hneg2(*reinterpret_cast<__half2*>(&c)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
 __device__ __forceinline__ float2 unpack_bf162(uint32_t x) {
   return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
 }
@@ -395,6 +401,8 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   const int off_dv0 = v_delta_off(NG, 2 * quad, 0), off_dv1 = v_delta_off(NG, 2 * quad + 8, 0);
   const int off_zp0 = v_zero_off(NG, 2 * quad, hrow < NG ? hrow : 0);
   const int off_zp1 = v_zero_off(NG, 2 * quad + 8, hrow < NG ? hrow : 0);
+  const int off_gd0 = v_delta_off(NG, 2 * quad, hrow < NG ? hrow : 0);
+  const int off_gd1 = v_delta_off(NG, 2 * quad + 8, hrow < NG ? hrow : 0);
 
   // One page: scores, softmax, P V.  MASKED pages (the sequence's last, partial page, or an
   // entry that is not a page id) keep only their first valid_tok tokens.
@@ -492,9 +500,14 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     load_scales<NG>(pg + off_dv0, dv0);
     load_scales<NG>(pg + off_dv1, dv1);
     uint32_t zp0 = 0u, zp1 = 0u;                       // z_v pairs of group lane/4
+    uint32_t gd0 = 0u, gd1 = 0u;                       // Delta_v pairs of group lane/4 (NG > 1)
     if (hrow < NG) {
       zp0 = *reinterpret_cast<const uint32_t*>(pg + off_zp0);
       zp1 = *reinterpret_cast<const uint32_t*>(pg + off_zp1);
+      if constexpr (NG > 1) {
+        gd0 = *reinterpret_cast<const uint32_t*>(pg + off_gd0);
+        gd1 = *reinterpret_cast<const uint32_t*>(pg + off_gd1);
+      }
     }
     if constexpr (MASKED) {                            // clear the dead tokens' scale data
       const uint32_t m0 = (2 * quad < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 1 < valid_tok ? 0xffff0000u : 0u);
@@ -509,8 +522,19 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     for (int gi = 0; gi < NG; ++gi) {
       bw[gi][0] = hmul2_bits(pb0, dv0[gi]);
       bw[gi][1] = hmul2_bits(pb1, dv1[gi]);
-      const uint32_t az[4] = {hrow == gi ? zp0 : 0u, 0u, hrow == gi ? zp1 : 0u, 0u};
-      mma_f16(corr, az, bw[gi][0], bw[gi][1]);
+    }
+    if constexpr (NG == 1) {
+      // row 0 of the correction: sum_t z_t W_t with the same W as the P V product
+      const uint32_t az[4] = {hrow == 0 ? zp0 : 0u, 0u, hrow == 0 ? zp1 : 0u, 0u};
+      mma_f16(corr, az, bw[0][0], bw[0][1]);
+    } else {
+      // all groups in one product: row g = sum_t (z Delta)_{t,g} P'_t, with z Delta carried as
+      // an fp16 hi + lo pair (the product is 22 bits; the lo part is exact by the fused HFMA2)
+      const uint32_t hi0 = hmul2_bits(zp0, gd0), hi1 = hmul2_bits(zp1, gd1);
+      const uint32_t lo0 = hfma2_neg_bits(zp0, gd0, hi0), lo1 = hfma2_neg_bits(zp1, gd1, hi1);
+      const uint32_t ah[4] = {hi0, 0u, hi1, 0u}, al[4] = {lo0, 0u, lo1, 0u};
+      mma_f16(corr, ah, pb0, pb1);
+      mma_f16(corr, al, pb0, pb1);
     }
     const uint32_t vw[4] = {wv.x, wv.y, wv.z, wv.w};
     const uint32_t vw10[4] = {wv.x >> 10, wv.y >> 10, wv.z >> 10, wv.w >> 10};
