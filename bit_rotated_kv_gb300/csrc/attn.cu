@@ -850,7 +850,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
   __syncthreads();
   const AttnParams& P = Ps;
   // (each branch below waits for the producer kernels itself, after its independent loads)
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // split index slowest: every unit's first INT2 split (always full) is dispatched before the
+  // later, partly empty ones and the short window splits (longest work first)
+  const int split = blockIdx.z, h = blockIdx.x, b = blockIdx.y;
   const int g = P.gqa;
   // per-warp results: an INT2 warp writes into its own (drained) page ring, a window warp
   // into a plain array; both start after the 1 KB of barriers and query data.
@@ -962,9 +964,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
 using namespace kvq;
 
 // Split counts from sizes only (no device query), so the workspace size is a pure
-// function of (cfg, max_ctx).  Aims at one wave of two CTAs per SM on 152 SMs: C CTAs per
-// (sequence, kv head), shared between INT2 splits and BF16-window splits in proportion to
-// their bytes (the window after a flush: S_sink + S_keep + S_flush tokens).
+// function of (cfg, max_ctx): one wave of two CTAs per SM on 152 SMs, shared between INT2
+// splits and BF16-window splits by bytes (the window after a flush: S_sink + S_keep +
+// S_flush tokens).
 // INT2 pages per sequence a call with contexts up to max_ctx can touch.
 static int kvq_attn_pages(const kvq_config* cfg, int32_t max_ctx) {
   const int p = max(0, (max_ctx - cfg->s_sink + kPage - 1) / kPage);
@@ -978,10 +980,19 @@ extern "C" void kvq_attn_splits(const kvq_config* cfg, int32_t max_ctx, int* n_i
   const long long tile_b = (long long)kPage * kHeadDim * 2 * 2;
   const long long wtiles = (cfg->s_sink + kPage - 1) / kPage + (cfg->s_keep + cfg->s_flush + kPage - 1) / kPage + 1;
   const double wbytes = (double)wtiles * tile_b, ibytes = (double)pages * pb;
-  int per_unit = (int)max(2LL, 304 / max(units, 1LL));
-  int nw = (int)(per_unit * wbytes / (wbytes + ibytes) + 0.5);
-  nw = max(1, min(nw, per_unit - 1));
-  int ni = per_unit - nw;
+  // p = CTAs per unit for one wave of two CTAs per SM.  When the windows are worth at least
+  // half a CTA they get their share of the p; otherwise the INT2 splits take all p slots and
+  // one short window split per unit comes on top (it fills a slot as the first CTAs retire).
+  const int p = (int)max(1LL, 2LL * kSms / max(units, 1LL));
+  int nw = (int)(p * wbytes / (wbytes + ibytes) + 0.5);
+  int ni;
+  if (p == 1 || nw == 0) {
+    ni = p;
+    nw = 1;
+  } else {
+    nw = min(nw, p - 1);
+    ni = p - nw;
+  }
   if (cfg->attn_splits > 0) ni = cfg->attn_splits;
   ni = max(1, min(ni, max(1, pages)));
   *n_int2 = ni;
@@ -1069,7 +1080,8 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
       attr_done[vi] |= 1ull << dev;
     }
   }
-  dim3 grid(P.n_split, cfg->n_kv_heads, cfg->batch);
+  if (cfg->batch > 65535 || P.n_split > 65535) return KVQ_ERR_UNSUPPORTED;   // grid y / z limits
+  dim3 grid(cfg->n_kv_heads, cfg->batch, P.n_split);
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, P) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

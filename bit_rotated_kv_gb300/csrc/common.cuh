@@ -114,6 +114,14 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int32_t* p, int v) {
   return old;
 }
 
+// Atomic add with release semantics only (orders this thread's earlier accesses before it;
+// later ones are not held back, so the result can be consumed much later).
+__device__ __forceinline__ int atomic_add_release_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.add.release.gpu.global.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Warm L2 with [src, src + bytes) (16-byte aligned, multiple of 16) or with the line holding
 // src: no data reaches the SM and nothing is ordered, so a kernel may issue these before its
 // producer kernel has finished (before pdl_wait); the reads that count come after the wait.

@@ -215,6 +215,16 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
       n = 0;
     }
   }
+  // Every warp has read s_quant once the CTA passes this barrier.  A single CTA publishes the
+  // new value at once (later kernels read it only after this grid completes); otherwise each
+  // CTA takes a ticket now -- a release atomic whose result is only needed at the end, so its
+  // latency hides behind the work -- and the last reader publishes.
+  __syncthreads();
+  int ticket = -1;
+  if (threadIdx.x == 0) {
+    if (gridDim.x == 1) P.s_quant[b] = sq + n;
+    else ticket = atomic_add_release_gpu(P.counters + b, 1);
+  }
   const int ng = kHeadDim / P.group;
   // work items: (token, kv head, K|V) in that order, a contiguous range per CTA, strided over
   // the CTA's warps.  Ranges and strides are even, so a warp always handles keys (even warps)
@@ -323,17 +333,12 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
     }
     if (bad && lane == 0) set_status(P.status, KVQ_ERR_NONFINITE);
   }
-  // every warp has read s_quant by now; the last CTA of this sequence publishes the new value
-  // and re-zeroes the ticket (a sequence handled by a single CTA needs no ticket)
-  __syncthreads();
-  if (threadIdx.x == 0 && gridDim.x == 1) {
+  // the last CTA of this sequence to have read s_quant publishes the new value and re-zeroes
+  // the ticket (its fence orders that store after every other CTA's read)
+  if (threadIdx.x == 0 && ticket == (int)gridDim.x - 1) {
+    __threadfence();
     P.s_quant[b] = sq + n;
-  } else if (threadIdx.x == 0) {
-    const int ticket = atomic_add_acq_rel_gpu(P.counters + b, 1);
-    if (ticket == (int)gridDim.x - 1) {
-      P.s_quant[b] = sq + n;
-      P.counters[b] = 0;
-    }
+    P.counters[b] = 0;
   }
 }
 

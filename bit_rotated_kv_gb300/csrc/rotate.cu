@@ -98,10 +98,11 @@ __device__ __forceinline__ int bf16_if_decided(float v, float e) {
 
 // One dense tile per CTA of 256 threads: up to RT rows that share matrix mh.  Thread 2i + half
 // keeps its 64 matrix entries T[mh][i][64 half .. 64 half + 63] in registers and forms, for
-// every row, the fp32 FMA chain v_k = RN(v_{k-1} + T_ik x_k) over its half.  Each step adds an
-// error of at most u |v_k| (u = 2^-24), so with the halves' sums A = sum_k |v_k| and the final
-// v = RN(v_A + v_B), |v - y| <= u (A_A + A_B + |v|) for y = sum_j T_ij x_j (plus at most 2^-142
-// from underflow; the fp32 evaluation of the bound is covered by a factor 1 + 2^-16).  bf16(v)
+// every row, four fp32 FMA chains v_k = RN(v_{k-1} + T_ik x_k) of 16 terms each, which three
+// additions inside the thread and one with the partner thread combine.  Every rounding r adds
+// an error of at most u |r| (u = 2^-24), so with A = the sum of |r| over all partial results
+// (chains, combining sums and the final v), |v - y| <= u A for y = sum_j T_ij x_j (plus at most
+// 2^-142 from underflow; the fp32 evaluation of A is covered by a factor 1 + 2^-16).  bf16(v)
 // is then the correctly rounded result unless a rounding midpoint lies within that distance;
 // those few outputs are recomputed exactly (double-float) by a warp each after the tile.
 // Loads are issued in the order that overlaps them: the destination's sequence index and
@@ -158,19 +159,26 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
     uint16_t* dst = dst_sh[r];
     if (dst == nullptr) continue;
     const float* x = xs[r] + 64 * half;
-    float v = 0.f, a = 0.f;
+    // four independent FMA chains of 16 terms (float4 j4 feeds chain j4 % 4), each with its
+    // running sum of |partial|; then two adds inside the thread and one with the partner
+    float vc[4] = {0.f, 0.f, 0.f, 0.f}, ac[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int j4 = 0; j4 < 16; ++j4) {
       const float4 xv = *reinterpret_cast<const float4*>(x + 4 * j4);
+      float& v = vc[j4 & 3];
+      float& a = ac[j4 & 3];
       v = fmaf(m[j4].x, xv.x, v); a += fabsf(v);
       v = fmaf(m[j4].y, xv.y, v); a += fabsf(v);
       v = fmaf(m[j4].z, xv.z, v); a += fabsf(v);
       v = fmaf(m[j4].w, xv.w, v); a += fabsf(v);
     }
+    const float s01 = vc[0] + vc[1], s23 = vc[2] + vc[3];
+    float v = s01 + s23;
+    float a = ((ac[0] + ac[1]) + (ac[2] + ac[3])) + ((fabsf(s01) + fabsf(s23)) + fabsf(v));
     v += __shfl_xor_sync(0xffffffffu, v, 1);
     a += __shfl_xor_sync(0xffffffffu, a, 1);
     if (half == 0) {
-      const float e = fmaf(a + fabsf(v), 0x1.0001p-24f, 0x1p-140f);
+      const float e = fmaf(a + fabsf(v), 0x1.0001p-24f, 0x1p-140f);   // A includes the final v
       const int b = bf16_if_decided(v, e);
       if (b >= 0) dst[i] = (uint16_t)b;
       else fallback[atomicAdd(&n_fallback, 1)] = (uint16_t)((r << 7) | i);

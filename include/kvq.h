@@ -231,6 +231,7 @@ KVQ_API int kv_quant_flush(const kvq_config* cfg, const kvq_cache* cache, int32_
  *            ticket counters at its head zero again (the rest is overwritten).
  * Softmax over sink | INT2 | recent tokens with online (max, sum) merging across
  * splits in one launch; all g = Hq/Hkv query heads of a kv head share one read.
+ * batch <= 65535 (KVQ_ERR_UNSUPPORTED otherwise: it is a grid dimension).
  * Source: [OSCAR] section 4 "Decoding Attention Kernel"; [OScaR] attention fused
  * kernel (in-register dequantisation, split attention); [WUSH] GQA. */
 KVQ_API int kv_attn_decode(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
