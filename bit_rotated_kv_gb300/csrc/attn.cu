@@ -990,7 +990,7 @@ extern "C" void kvq_attn_splits(const kvq_config* cfg, int32_t max_ctx, int* n_i
     ni = p;
     nw = 1;
   } else {
-    nw = min(nw, p - 1);
+    nw = (int)min((long long)min(nw, p - 1), wtiles);     // no more window splits than tiles
     ni = p - nw;
   }
   if (cfg->attn_splits > 0) ni = cfg->attn_splits;

@@ -324,7 +324,10 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
   long long dense_pairs = 0;
   for (int i = 0; i < 3; ++i)
     if (P.t[i].mode == ROT_DENSE) dense_pairs += (long long)P.t[i].rows * P.t[i].heads;
-  long long rt = (dense_pairs + 303) / 304;
+  // rows per tile: at most one tile per SM while that is enough (no SM runs two of a handful
+  // of tiles), else about two tiles per SM
+  const long long slots = dense_pairs <= 2 * kSms ? kSms : 2 * kSms;
+  long long rt = (dense_pairs + slots - 1) / slots;
   P.rt = (int)(rt < 1 ? 1 : (rt > kMaxRT ? kMaxRT : rt));
   for (int i = 0; i < 3; ++i) {
     const long long items = (long long)P.t[i].rows * P.t[i].heads;

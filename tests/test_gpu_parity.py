@@ -113,7 +113,7 @@ def test_edge(name):
     _check_units(run, [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)])
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])     # 64: partials beyond the one-level merge
 def test_split_count_invariance(splits):
     w = BASE.replace(ctx_lo=900, ctx_hi=900)
     ref = harness.GpuRun(w, attn_splits=1).snapshot()["out"]
