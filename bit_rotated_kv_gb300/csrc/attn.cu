@@ -37,7 +37,7 @@ namespace kvq {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 8;
+constexpr int kStages = 4;
 constexpr long long kWaitLimit = 1LL << 22;
 constexpr int kRow = 4 + kHeadDim;      // one (m, l, -, -, o[d]) record; o 16-byte aligned
 constexpr int kGroup = 8;               // splits merged together at the first merge level
