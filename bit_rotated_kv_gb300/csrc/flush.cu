@@ -120,34 +120,58 @@ __device__ __forceinline__ void order_stats(const float s[4], int n, int nl, uns
 // RN(q0 + (y - q0 d) r), the remainder exact by FMA -- as long as nothing underflows or
 // overflows, which holds for 2^-96 <= |y| <= 2^96 since 2^-24 <= d <= 65504.  Other y (and
 // y = 0, NaN or infinity) take the IEEE division.
-__device__ __forceinline__ float div_by_scale(float y, float d, float r) {
+__device__ __forceinline__ bool div_fast_ok(float y) {
   const float ay = fabsf(y);
-  if (ay >= 0x1p-96f && ay <= 0x1p96f) {
-    const float q0 = __fmul_rn(y, r);
-    const float rem = __fmaf_rn(-q0, d, y);
-    return __fmaf_rn(rem, r, q0);
-  }
-  return __fdiv_rn(y, d);
+  return ay >= 0x1p-96f && ay <= 0x1p96f;
 }
+__device__ __forceinline__ float div_fast(float y, float d, float r) {
+  const float q0 = __fmul_rn(y, r);
+  const float rem = __fmaf_rn(-q0, d, y);
+  return __fmaf_rn(rem, r, q0);
+}
+__device__ __forceinline__ float div_by_scale(float y, float d, float r) {
+  return div_fast_ok(y) ? div_fast(y, d, r) : __fdiv_rn(y, d);
+}
+// The four quotients of a lane, branch-free unless some lane of the warp holds a dividend
+// outside the fast range (then those quotients are redone by IEEE division).
+__device__ __forceinline__ void div4_by_scale(const float (&y)[4], float d, float (&q)[4]) {
+  const float r = __frcp_rn(d);
+  bool ok = true;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    q[m] = div_fast(y[m], d, r);
+    ok = ok && div_fast_ok(y[m]);
+  }
+  if (!__all_sync(0xffffffffu, ok)) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      if (!div_fast_ok(y[m])) q[m] = __fdiv_rn(y[m], d);
+  }
+}
+
+// Quantizer constants of one warp's rows (keys or values), held in registers.
+struct QuantConsts {
+  int nl, group, affine, n_hi, n_lo, i_hi, i_lo;
+  float f_hi, f_lo;
+  double alpha;
+};
 
 // Quantize one row held as 4 float32 values per lane; returns the lane's 4 codes and the
 // group's Delta16 / z16 in dz (valid on all lanes).
-__device__ __forceinline__ void quant_row(const FlushParams& P, int which, const float y[4], int lane,
+__device__ __forceinline__ void quant_row(const QuantConsts& Q, const float (&y)[4], int lane,
                                           uint32_t (&code)[4], __half2& dz, bool& bad) {
-  const int nl = P.group >> 2;
+  const int nl = Q.nl;
   const unsigned gmask = nl == 32 ? 0xffffffffu : (((1u << nl) - 1u) << (lane & ~(nl - 1)));
   __half d16, z16;
-  if (P.quantizer == KVQ_QUANT_AFFINE_KAPPA) {
+  if (Q.affine) {
     float s[4] = {y[0], y[1], y[2], y[3]};
     sort4(s[0], s[1], s[2], s[3]);
     float hc, hp, lc, lp;
-    order_stats<true>(s, P.n_hi[which], nl, gmask, lane, hc, hp);
-    order_stats<false>(s, P.n_lo[which], nl, gmask, lane, lc, lp);
-    const int g = P.group;
-    float hi = (P.i_hi[which] >= g - 1) ? hc
-                                        : __fadd_rn(hc, __fmul_rn(P.f_hi[which], __fsub_rn(hp, hc)));
-    float lo = (P.i_lo[which] >= g - 1) ? lc
-                                        : __fadd_rn(lp, __fmul_rn(P.f_lo[which], __fsub_rn(lc, lp)));
+    order_stats<true>(s, Q.n_hi, nl, gmask, lane, hc, hp);
+    order_stats<false>(s, Q.n_lo, nl, gmask, lane, lc, lp);
+    const int g = Q.group;
+    float hi = (Q.i_hi >= g - 1) ? hc : __fadd_rn(hc, __fmul_rn(Q.f_hi, __fsub_rn(hp, hc)));
+    float lo = (Q.i_lo >= g - 1) ? lc : __fadd_rn(lp, __fmul_rn(Q.f_lo, __fsub_rn(lc, lp)));
     float delta = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
     d16 = __float2half_rn(delta);
     if (__half2float(d16) == 0.0f) d16 = __float2half_rn(1.0f);
@@ -158,25 +182,25 @@ __device__ __forceinline__ void quant_row(const FlushParams& P, int which, const
 #pragma unroll
     for (int m = 0; m < 4; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[m], (double)y[m]));
     for (int o = nl >> 1; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
-    double rms = __dsqrt_rn(__ddiv_rn(ss, (double)P.group));
-    double delta = __ddiv_rn(__dmul_rn(__dmul_rn(2.0, P.alpha), rms), 3.0);
+    double rms = __dsqrt_rn(__ddiv_rn(ss, (double)Q.group));
+    double delta = __ddiv_rn(__dmul_rn(__dmul_rn(2.0, Q.alpha), rms), 3.0);
     d16 = double_to_half_rn(delta);
     if (__half2float(d16) == 0.0f) d16 = __float2half_rn(1.0f);
     z16 = __float2half_rn(1.5f);
   }
   float df = __half2float(d16), zf = __half2float(z16);
   if (!isfinite(df) || !isfinite(zf)) bad = true;
-  const float rf = __frcp_rn(df);
+  float qv[4];
+  div4_by_scale(y, df, qv);
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    float u = __fadd_rn(div_by_scale(y[m], df, rf), zf);
-    int c = __float2int_rn(u);
-    code[m] = (uint32_t)(c < 0 ? 0 : (c > 3 ? 3 : c));
+    const int c = __float2int_rn(__fadd_rn(qv[m], zf));
+    code[m] = (uint32_t)min(max(c, 0), 3);
   }
   dz = __halves2half2(d16, z16);
 }
 
-__global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
+__global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   // shared-memory copy of the parameters (see rotate_kernel)
   pdl_trigger();
   __shared__ FlushParams Ps;
@@ -237,12 +261,29 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
   const int which = warp & 1;
   const uint16_t* ring = which ? P.ring_v : P.ring_k;
   const int hkv = P.hkv, rcap = P.ring_cap, dh = nwarps >> 1;
+  // everything the row loop needs, in registers (the parameter block is shared memory, which
+  // the compiler would re-read after every store through a generic pointer)
+  QuantConsts Q;
+  Q.nl = P.group >> 2;
+  Q.group = P.group;
+  Q.affine = P.quantizer == KVQ_QUANT_AFFINE_KAPPA;
+  Q.n_hi = P.n_hi[which];
+  Q.n_lo = P.n_lo[which];
+  Q.i_hi = P.i_hi[which];
+  Q.i_lo = P.i_lo[which];
+  Q.f_hi = P.f_hi[which];
+  Q.f_lo = P.f_lo[which];
+  Q.alpha = P.alpha;
+  const bool key_norm = which == 0 && P.l2;
+  const int s_sink = P.s_sink, max_pages = P.max_pages, num_pages = P.num_pages, page_bytes = P.page_bytes;
+  const int32_t* ptab = P.page_table + (size_t)b * max_pages;
+  uint8_t* const pages = P.pages;
   int it = i0 + warp;
   int nx_h = 0, nx_tok = 0, nx_slot = 0, pid_n = -1;
   uint2 raw_n = make_uint2(0u, 0u);
   auto fetch = [&]() {
-    const int pidx = (nx_tok - P.s_sink) >> 4;
-    pid_n = (pidx < P.max_pages) ? P.page_table[(size_t)b * P.max_pages + pidx] : -1;
+    const int pidx = (nx_tok - s_sink) >> 4;
+    pid_n = (pidx < max_pages) ? ptab[pidx] : -1;
     raw_n = *reinterpret_cast<const uint2*>(
         ring + (((size_t)b * hkv + nx_h) * rcap + nx_slot) * kHeadDim + 4 * lane);
   };
@@ -263,19 +304,19 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
       if (++nx_slot == rcap) nx_slot = 0;
     }
     if (it + nwarps < i1) fetch();
-    const int tp = (tok - P.s_sink) & (kPage - 1);
-    if (pid < 0 || pid >= P.num_pages) {
+    const int tp = (tok - s_sink) & (kPage - 1);
+    if (pid < 0 || pid >= num_pages) {
       if (lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
       continue;
     }
-    uint8_t* chunk = P.pages + ((size_t)pid * hkv + h) * P.page_bytes;
+    uint8_t* chunk = pages + ((size_t)pid * hkv + h) * page_bytes;
     bool bad = false;
     float y[4];
     y[0] = __uint_as_float(raw.x << 16);
     y[1] = __uint_as_float(raw.x & 0xffff0000u);
     y[2] = __uint_as_float(raw.y << 16);
     y[3] = __uint_as_float(raw.y & 0xffff0000u);
-    if (which == 0 && P.l2) {
+    if (key_norm) {
       double ss = 0.0;
 #pragma unroll
       for (int m = 0; m < 4; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[m], (double)y[m]));
@@ -283,15 +324,19 @@ __global__ void __launch_bounds__(256) flush_kernel(const FlushParams Pk) {
       __half s16 = double_to_half_rn(__dsqrt_rn(ss));
       float sf = __half2float(s16);
       if (!isfinite(sf)) bad = true;
-      const float rs = __frcp_rn(sf);
-#pragma unroll
-      for (int m = 0; m < 4; ++m) y[m] = (sf == 0.0f) ? 0.0f : div_by_scale(y[m], sf, rs);
+      if (sf == 0.0f) {
+        y[0] = y[1] = y[2] = y[3] = 0.0f;
+      } else {
+        float yn[4];
+        div4_by_scale(y, sf, yn);
+        y[0] = yn[0]; y[1] = yn[1]; y[2] = yn[2]; y[3] = yn[3];
+      }
       if (lane == 0) reinterpret_cast<__half*>(chunk + norm_off(ng))[tp] = s16;
     }
     __half2 dz;
     uint32_t c[4];
-    quant_row(P, which, y, lane, c, dz, bad);
-    const int nl = P.group >> 2;
+    quant_row(Q, y, lane, c, dz, bad);
+    const int nl = Q.nl;
     if ((lane & (nl - 1)) == 0) {
       const int g = lane / nl;
       if (which == 0) {
@@ -450,7 +495,7 @@ extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, i
   int threads = 128, ipw = 1;
   if (total > 4LL * kSms * 16) {
     threads = 256;
-    const long long slots = (long long)kSms * 4 * (threads / 32);   // 4 resident CTAs per SM at 52 registers
+    const long long slots = (long long)kSms * 3 * (threads / 32);   // 3 resident CTAs per SM (<= 85 registers)
     ipw = (int)((total + slots - 1) / slots);
   }
   const long long ipc = (long long)ipw * (threads / 32);

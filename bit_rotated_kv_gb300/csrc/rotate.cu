@@ -36,7 +36,9 @@ struct RotTensor {
 
 struct RotParams {
   RotTensor t[3];
-  int rt;                // rows per dense tile (rows that share one matrix)
+  int rt;                // rows per chunk of a dense tile (rows that share one matrix)
+  int rpc;               // chunks per dense tile (the matrix is loaded once per tile)
+  int rpw;               // items per warp for exact copies
   int n_dense[3];        // dense tiles per tensor (0 when not dense)
   int n_warp[3];         // warp items per tensor (0 when dense)
   int dense_total, warp_total;
@@ -96,7 +98,8 @@ __device__ __forceinline__ int bf16_if_decided(float v, float e) {
   return (fabsf(v - m1) > e && fabsf(v - m2) > e) ? (int)b : -1;   // NaN compares false
 }
 
-// One dense tile per CTA of 256 threads: up to RT rows that share matrix mh.  Thread 2i + half
+// One dense tile per CTA of 256 threads: chunks of up to RT rows that share matrix mh, the
+// matrix loaded once per tile.  Thread 2i + half
 // keeps its 64 matrix entries T[mh][i][64 half .. 64 half + 63] in registers and forms, for
 // every row, four fp32 FMA chains v_k = RN(v_{k-1} + T_ik x_k) of 16 terms each, which three
 // additions inside the thread and one with the partner thread combine.  Every rounding r adds
@@ -108,105 +111,147 @@ __device__ __forceinline__ int bf16_if_decided(float v, float e) {
 // Loads are issued in the order that overlaps them: the destination's sequence index and
 // position, the matrix, the rows, and only then the dependent s_quant check.
 constexpr int kMaxRT = 16;
+constexpr int kMaxRPW = 8;
 __device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const RotTensor& T = P.t[tt];
   const int pairs = T.rows * T.head_div;                 // (row, head) pairs per matrix
-  const int tiles_per_mat = (pairs + P.rt - 1) / P.rt;
+  const int chunks_per_mat = (pairs + P.rt - 1) / P.rt;
+  const int tiles_per_mat = (chunks_per_mat + P.rpc - 1) / P.rpc;
   const int mh = tile / tiles_per_mat;
-  const int p0 = (tile % tiles_per_mat) * P.rt;
-  const int np = min(P.rt, pairs - p0);
+  const int c0 = (tile % tiles_per_mat) * P.rpc;         // first chunk of this tile
+  const int c1 = min(chunks_per_mat, c0 + P.rpc);
   __shared__ __align__(16) float xs[kMaxRT][kHeadDim];
   __shared__ uint16_t* dst_sh[kMaxRT];
   __shared__ uint16_t fallback[kMaxRT * kHeadDim];      // (row << 7) | output, undecided outputs
   __shared__ int n_fallback;
   const int tid = threadIdx.x;
-  int d_row = 0, d_head = 0, d_b = 0, d_p = 0;
-  if (tid < np) {
-    tile_row(T, mh, p0 + tid, d_row, d_head);
-    if (!T.is_query) {
-      d_b = P.seq_idx[d_row];
-      d_p = P.pos[d_row];
-    }
-  }
+  const int lane = tid & 31, warp = tid >> 5;
   const int i = tid >> 1, half = tid & 1;
+  const int xrow = tid >> 4, xpart = tid & 15;
+  // the chunk's destinations and rows: one 16-byte piece (8 bf16) of a row per thread
+  int d_row = 0, d_head = 0, d_b = 0, d_p = 0;
+  uint4 xr = make_uint4(0u, 0u, 0u, 0u);
+  auto load_chunk = [&](int c) {
+    const int p0 = c * P.rt, np = min(P.rt, pairs - p0);
+    if (tid < np) {
+      tile_row(T, mh, p0 + tid, d_row, d_head);
+      if (!T.is_query) {
+        d_b = P.seq_idx[d_row];
+        d_p = P.pos[d_row];
+      }
+    }
+    if (xrow < np) {
+      int row, head;
+      tile_row(T, mh, p0 + xrow, row, head);
+      xr = reinterpret_cast<const uint4*>(T.src + ((size_t)row * T.heads + head) * kHeadDim)[xpart];
+    }
+  };
+  load_chunk(c0);
+  // the matrix, once per tile: thread 2i + half keeps T[mh][i][64 half .. 64 half + 63]
   const float* mrow = T.mat + ((size_t)mh * kHeadDim + i) * kHeadDim;
   const float4* m4 = reinterpret_cast<const float4*>(mrow + 64 * half);
   float4 m[16];
 #pragma unroll
   for (int j4 = 0; j4 < 16; ++j4) m[j4] = m4[j4];
-  // rows: one 16-byte piece (8 bf16) per thread, 16 pieces per row
-  uint4 xr = make_uint4(0u, 0u, 0u, 0u);
-  const int xrow = tid >> 4, xpart = tid & 15;
-  if (xrow < np) {
-    int row, head;
-    tile_row(T, mh, p0 + xrow, row, head);
-    xr = reinterpret_cast<const uint4*>(T.src + ((size_t)row * T.heads + head) * kHeadDim)[xpart];
-  }
   // everything above reads only the caller's inputs, which the kernels of this library never
   // write: it overlaps the producer kernel; the cache state (s_quant, seq_len) comes after
   pdl_wait();
-  if (tid < np) dst_sh[tid] = rot_dst(P, T, d_row, d_head, d_b, d_p, true);
-  if (xrow < np) {
-    float4* xd = reinterpret_cast<float4*>(&xs[xrow][8 * xpart]);
-    xd[0] = make_float4(__uint_as_float(xr.x << 16), __uint_as_float(xr.x & 0xffff0000u),
-                        __uint_as_float(xr.y << 16), __uint_as_float(xr.y & 0xffff0000u));
-    xd[1] = make_float4(__uint_as_float(xr.z << 16), __uint_as_float(xr.z & 0xffff0000u),
-                        __uint_as_float(xr.w << 16), __uint_as_float(xr.w & 0xffff0000u));
-  }
-  if (tid == 0) n_fallback = 0;
-  __syncthreads();
-  for (int r = 0; r < np; ++r) {
-    uint16_t* dst = dst_sh[r];
-    if (dst == nullptr) continue;
-    const float* x = xs[r] + 64 * half;
-    // four independent FMA chains of 16 terms (float4 j4 feeds chain j4 % 4), each with its
-    // running sum of |partial|; then two adds inside the thread and one with the partner
-    float vc[4] = {0.f, 0.f, 0.f, 0.f}, ac[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = c0; c < c1; ++c) {
+    const int np = min(P.rt, pairs - c * P.rt);
+    if (tid < np) dst_sh[tid] = rot_dst(P, T, d_row, d_head, d_b, d_p, true);
+    if (xrow < np) {
+      float4* xd = reinterpret_cast<float4*>(&xs[xrow][8 * xpart]);
+      xd[0] = make_float4(__uint_as_float(xr.x << 16), __uint_as_float(xr.x & 0xffff0000u),
+                          __uint_as_float(xr.y << 16), __uint_as_float(xr.y & 0xffff0000u));
+      xd[1] = make_float4(__uint_as_float(xr.z << 16), __uint_as_float(xr.z & 0xffff0000u),
+                          __uint_as_float(xr.w << 16), __uint_as_float(xr.w & 0xffff0000u));
+    }
+    if (tid == 0) n_fallback = 0;
+    __syncthreads();
+    if (c + 1 < c1) load_chunk(c + 1);                  // the next chunk's loads fly meanwhile
+    for (int r = 0; r < np; ++r) {
+      uint16_t* dst = dst_sh[r];
+      if (dst == nullptr) continue;
+      const float* x = xs[r] + 64 * half;
+      // four independent FMA chains of 16 terms (float4 j4 feeds chain j4 % 4), each with its
+      // running sum of |partial|; then two adds inside the thread and one with the partner
+      float vc[4] = {0.f, 0.f, 0.f, 0.f}, ac[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int j4 = 0; j4 < 16; ++j4) {
-      const float4 xv = *reinterpret_cast<const float4*>(x + 4 * j4);
-      float& v = vc[j4 & 3];
-      float& a = ac[j4 & 3];
-      v = fmaf(m[j4].x, xv.x, v); a += fabsf(v);
-      v = fmaf(m[j4].y, xv.y, v); a += fabsf(v);
-      v = fmaf(m[j4].z, xv.z, v); a += fabsf(v);
-      v = fmaf(m[j4].w, xv.w, v); a += fabsf(v);
+      for (int j4 = 0; j4 < 16; ++j4) {
+        const float4 xv = *reinterpret_cast<const float4*>(x + 4 * j4);
+        float& v = vc[j4 & 3];
+        float& a = ac[j4 & 3];
+        v = fmaf(m[j4].x, xv.x, v); a += fabsf(v);
+        v = fmaf(m[j4].y, xv.y, v); a += fabsf(v);
+        v = fmaf(m[j4].z, xv.z, v); a += fabsf(v);
+        v = fmaf(m[j4].w, xv.w, v); a += fabsf(v);
+      }
+      const float s01 = vc[0] + vc[1], s23 = vc[2] + vc[3];
+      float v = s01 + s23;
+      float a = ((ac[0] + ac[1]) + (ac[2] + ac[3])) + ((fabsf(s01) + fabsf(s23)) + fabsf(v));
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      a += __shfl_xor_sync(0xffffffffu, a, 1);
+      if (half == 0) {
+        const float e = fmaf(a + fabsf(v), 0x1.0001p-24f, 0x1p-140f);   // A includes the final v
+        const int b = bf16_if_decided(v, e);
+        if (b >= 0) dst[i] = (uint16_t)b;
+        else fallback[atomicAdd(&n_fallback, 1)] = (uint16_t)((r << 7) | i);
+      }
     }
-    const float s01 = vc[0] + vc[1], s23 = vc[2] + vc[3];
-    float v = s01 + s23;
-    float a = ((ac[0] + ac[1]) + (ac[2] + ac[3])) + ((fabsf(s01) + fabsf(s23)) + fabsf(v));
-    v += __shfl_xor_sync(0xffffffffu, v, 1);
-    a += __shfl_xor_sync(0xffffffffu, a, 1);
-    if (half == 0) {
-      const float e = fmaf(a + fabsf(v), 0x1.0001p-24f, 0x1p-140f);   // A includes the final v
-      const int b = bf16_if_decided(v, e);
-      if (b >= 0) dst[i] = (uint16_t)b;
-      else fallback[atomicAdd(&n_fallback, 1)] = (uint16_t)((r << 7) | i);
-    }
-  }
-  __syncthreads();
-  // exact recomputation of the undecided outputs: one warp per output, 4 terms per lane
-  const int lane = tid & 31, warp = tid >> 5;
-  for (int f = warp; f < n_fallback; f += (int)(blockDim.x >> 5)) {
-    const int r = fallback[f] >> 7, o = fallback[f] & 127;
-    const float4 t4 = reinterpret_cast<const float4*>(T.mat + ((size_t)mh * kHeadDim + o) * kHeadDim)[lane];
-    const float4 x4 = reinterpret_cast<const float4*>(xs[r])[lane];
-    float hi = 0.f, lo = 0.f;
-    ff_mac(hi, lo, t4.x, x4.x);
-    ff_mac(hi, lo, t4.y, x4.y);
-    ff_mac(hi, lo, t4.z, x4.z);
-    ff_mac(hi, lo, t4.w, x4.w);
+    __syncthreads();
+    // exact recomputation of the undecided outputs: one warp per output, 4 terms per lane
+    for (int f = warp; f < n_fallback; f += (int)(blockDim.x >> 5)) {
+      const int r = fallback[f] >> 7, o = fallback[f] & 127;
+      const float4 t4 = reinterpret_cast<const float4*>(T.mat + ((size_t)mh * kHeadDim + o) * kHeadDim)[lane];
+      const float4 x4 = reinterpret_cast<const float4*>(xs[r])[lane];
+      float hi = 0.f, lo = 0.f;
+      ff_mac(hi, lo, t4.x, x4.x);
+      ff_mac(hi, lo, t4.y, x4.y);
+      ff_mac(hi, lo, t4.z, x4.z);
+      ff_mac(hi, lo, t4.w, x4.w);
 #pragma unroll
-    for (int s2 = 16; s2 > 0; s2 >>= 1) {
-      const float oh = __shfl_xor_sync(0xffffffffu, hi, s2);
-      const float ol = __shfl_xor_sync(0xffffffffu, lo, s2);
-      ff_add(hi, lo, oh, ol, hi, lo);
+      for (int s2 = 16; s2 > 0; s2 >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, hi, s2);
+        const float ol = __shfl_xor_sync(0xffffffffu, lo, s2);
+        ff_add(hi, lo, oh, ol, hi, lo);
+      }
+      if (lane == 0) dst_sh[r][o] = ff_to_bf16(hi, lo);
     }
-    if (lane == 0) dst_sh[r][o] = ff_to_bf16(hi, lo);
+    __syncthreads();                                    // xs, dst_sh and the list are reused
   }
 }
 
-// One warp per (row, head): normalised Walsh-Hadamard transform or exact copy.
+// Exact copies (identity transform): one warp per P.rpw consecutive (row, head) items, all of
+// their loads in flight before the first store.
+__device__ void warp_copies(const RotParams& P, int tt, int witem, int lane) {
+  const RotTensor& T = P.t[tt];
+  const int item0 = witem * P.rpw;
+  const int n = min(P.rpw, T.rows * T.heads - item0);
+  int bb[kMaxRPW], pp[kMaxRPW];
+  uint2 raw[kMaxRPW];
+#pragma unroll
+  for (int k = 0; k < kMaxRPW; ++k) {
+    bb[k] = pp[k] = 0;
+    raw[k] = make_uint2(0u, 0u);
+    if (k < n) {
+      const int item = item0 + k, row = item / T.heads, h = item - row * T.heads;
+      bb[k] = P.seq_idx[row];
+      pp[k] = P.pos[row];
+      raw[k] = reinterpret_cast<const uint2*>(T.src + ((size_t)row * T.heads + h) * kHeadDim)[lane];
+    }
+  }
+  pdl_wait();                           // (the caller's inputs above: see dense_tile)
+#pragma unroll
+  for (int k = 0; k < kMaxRPW; ++k) {
+    if (k < n) {
+      const int item = item0 + k, row = item / T.heads, h = item - row * T.heads;
+      uint16_t* dst = rot_dst(P, T, row, h, bb[k], pp[k], lane == 0);
+      if (dst != nullptr) reinterpret_cast<uint2*>(dst)[lane] = raw[k];
+    }
+  }
+}
+
+// One warp per (row, head): normalised Walsh-Hadamard transform.
 __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   const RotTensor& T = P.t[tt];
   int row = item / T.heads, h = item % T.heads;
@@ -220,10 +265,6 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   pdl_wait();                           // (the caller's inputs above: see dense_tile)
   uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
   if (dst == nullptr) return;
-  if (T.mode == ROT_COPY) {
-    *reinterpret_cast<uint2*>(dst + 4 * lane) = raw;
-    return;
-  }
   float hi[4], lo[4];
   hi[0] = __uint_as_float(raw.x << 16);
   hi[1] = __uint_as_float(raw.x & 0xffff0000u);
@@ -295,7 +336,8 @@ __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
   }
   int tt, item;
   find_item(P.n_warp, w, tt, item);
-  warp_item(P, tt, item, threadIdx.x & 31);
+  if (P.t[tt].mode == ROT_COPY) warp_copies(P, tt, item, threadIdx.x & 31);
+  else warp_item(P, tt, item, threadIdx.x & 31);
 }
 
 }  // namespace kvq
@@ -329,14 +371,32 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
   const long long slots = dense_pairs <= 2 * kSms ? kSms : 2 * kSms;
   long long rt = (dense_pairs + slots - 1) / slots;
   P.rt = (int)(rt < 1 ? 1 : (rt > kMaxRT ? kMaxRT : rt));
+  // chunks per tile: one for decode-sized calls; for prefill-sized ones enough that the grid
+  // is about four waves of two tiles per SM, so each 64 KB matrix is read once per many rows
+  long long chunks = 0;
+  for (int i = 0; i < 3; ++i)
+    if (P.t[i].mode == ROT_DENSE)
+      chunks += (long long)(P.t[i].heads / P.t[i].head_div) *
+                (((long long)P.t[i].rows * P.t[i].head_div + P.rt - 1) / P.rt);
+  const long long target = 8LL * kSms;
+  long long rpc = chunks > target ? (chunks + target - 1) / target : 1;
+  P.rpc = (int)(rpc > (1 << 20) ? (1 << 20) : rpc);
+  // copies per warp: one while the copies fit two waves of 16 warps per SM, up to kMaxRPW
+  long long copies = 0;
+  for (int i = 0; i < 3; ++i)
+    if (P.t[i].mode == ROT_COPY) copies += (long long)P.t[i].rows * P.t[i].heads;
+  const long long cslots = 2LL * kSms * 16;
+  P.rpw = (int)(copies > cslots ? min((copies + cslots - 1) / cslots, (long long)kMaxRPW) : 1);
   for (int i = 0; i < 3; ++i) {
     const long long items = (long long)P.t[i].rows * P.t[i].heads;
     const int n_mats = P.t[i].heads / P.t[i].head_div;
     const long long pairs = (long long)P.t[i].rows * P.t[i].head_div;
-    const long long tiles = (long long)n_mats * ((pairs + P.rt - 1) / P.rt);
+    const long long tiles = (long long)n_mats * ((((pairs + P.rt - 1) / P.rt) + P.rpc - 1) / P.rpc);
     if (tiles > 0x3fffffffLL || items > 0x3fffffffLL) return KVQ_ERR_UNSUPPORTED;
     P.n_dense[i] = P.t[i].mode == ROT_DENSE ? (int)tiles : 0;
-    P.n_warp[i] = P.t[i].mode == ROT_DENSE ? 0 : (int)items;
+    P.n_warp[i] = P.t[i].mode == ROT_DENSE ? 0
+                  : P.t[i].mode == ROT_COPY  ? (int)((items + P.rpw - 1) / P.rpw)
+                                             : (int)items;
   }
   P.dense_total = P.n_dense[0] + P.n_dense[1] + P.n_dense[2];
   P.warp_total = P.n_warp[0] + P.n_warp[1] + P.n_warp[2];
