@@ -190,3 +190,22 @@ def test_empty_calls_are_noops():
     kvq.kv_quant_flush(cfg, cache, 0, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("w", [
+    BASE.replace(n_new=40, ctx_lo=600, ctx_hi=600),
+    BASE.replace(n_q_heads=16, n_kv_heads=2, batch=2, ctx_lo=300, ctx_hi=700, n_new=24, group_size=64,
+                 kappa_k=0.995, kappa_v=0.995),
+], ids=["gqa4_40_steps", "gqa8_g64_b2_24_steps"])
+def test_pipelined_decode_steps_without_sync(w):
+    """n_new single-token decode steps (rotate, flush, decode) launched back to back with no
+    host synchronization, so each kernel overlaps its predecessor's tail; the final cache and
+    the last step's attention must equal the oracle's state after the n_new tokens."""
+    run = harness.GpuRun(w, do_step=False)
+    r = run.runner
+    steps = [r.step_inputs(run.k_all, run.v_all, run.lengths + t, 1) for t in range(w.n_new)]
+    torch.cuda.synchronize()
+    for k_rows, v_rows, sidx, pos in steps:        # only the library's kernels from here on
+        r.step(run.q, k_rows, v_rows, sidx, pos, n_new=1)
+    torch.cuda.synchronize()
+    _check_units(run, [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)])
