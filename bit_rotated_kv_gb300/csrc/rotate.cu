@@ -112,6 +112,7 @@ __device__ __forceinline__ int bf16_if_decided(float v, float e) {
 // position, the matrix, the rows, and only then the dependent s_quant check.
 constexpr int kMaxRT = 16;
 constexpr int kMaxRPW = 8;
+template <bool kMulti>
 __device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const RotTensor& T = P.t[tt];
   const int pairs = T.rows * T.head_div;                 // (row, head) pairs per matrix
@@ -119,7 +120,7 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const int tiles_per_mat = (chunks_per_mat + P.rpc - 1) / P.rpc;
   const int mh = tile / tiles_per_mat;
   const int c0 = (tile % tiles_per_mat) * P.rpc;         // first chunk of this tile
-  const int c1 = min(chunks_per_mat, c0 + P.rpc);
+  const int c1 = kMulti ? min(chunks_per_mat, c0 + P.rpc) : c0 + 1;
   __shared__ __align__(16) float xs[kMaxRT][kHeadDim];
   __shared__ uint16_t* dst_sh[kMaxRT];
   __shared__ uint16_t fallback[kMaxRT * kHeadDim];      // (row << 7) | output, undecided outputs
@@ -168,7 +169,7 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
     }
     if (tid == 0) n_fallback = 0;
     __syncthreads();
-    if (c + 1 < c1) load_chunk(c + 1);                  // the next chunk's loads fly meanwhile
+    if (kMulti && c + 1 < c1) load_chunk(c + 1);        // the next chunk's loads fly meanwhile
     for (int r = 0; r < np; ++r) {
       uint16_t* dst = dst_sh[r];
       if (dst == nullptr) continue;
@@ -313,6 +314,10 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   *reinterpret_cast<uint2*>(dst + 4 * lane) = outv;
 }
 
+// kMulti: dense tiles span several row chunks (prefill-sized calls); decode-sized calls use
+// the single-chunk instantiation, whose smaller register footprint leaves room on the SMs for
+// the next kernels of the step to start early.
+template <bool kMulti>
 __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
   // Work on a shared-memory copy of the parameters: device functions take references and
   // index arrays of the struct at run time, which must never address the parameter space.
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
   if (blk < P.dense_total) {
     int tt, item;
     find_item(P.n_dense, blk, tt, item);
-    dense_tile(P, tt, item);
+    dense_tile<kMulti>(P, tt, item);
     return;
   }
   int w = (blk - P.dense_total) * 8 + (threadIdx.x >> 5);
@@ -412,6 +417,7 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
   long long blocks = (long long)P.dense_total + (P.warp_total + 7) / 8;
   if (blocks == 0) return KVQ_OK;
   if (blocks > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
-  return launch_pdl(rotate_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, P) == cudaSuccess ? KVQ_OK
+  return launch_pdl(P.rpc > 1 ? rotate_kernel<true> : rotate_kernel<false>, dim3((unsigned)blocks), dim3(256), 0,
+                    stream, P) == cudaSuccess ? KVQ_OK
                                                                                        : KVQ_ERR_CUDA;
 }
