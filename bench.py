@@ -264,16 +264,27 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
     # ---- end to end through the C ABI with host buffers: H2D of the step's inputs from
     # pinned memory, the three calls, D2H of the attention output, every step
-    h_k, h_v = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    h_s, h_p, h_q = sidx.cpu().pin_memory(), pos.cpu().pin_memory(), q.cpu().pin_memory()
+    # the step's inputs packed into one pinned host buffer (256-byte aligned segments), so the
+    # upload is a single copy
+    parts = [x.contiguous() for x in (k_new, v_new, sidx, pos, q)]
+    offs, nb = [], 0
+    for x in parts:
+        offs.append(nb)
+        nb += (x.numel() * x.element_size() + 255) // 256 * 256
+    h_buf = torch.empty(nb, dtype=torch.uint8).pin_memory()
+    d_buf = torch.empty(nb, dtype=torch.uint8, device=dev)
+    views = []
+    for x, o in zip(parts, offs):
+        n = x.numel() * x.element_size()
+        h_buf[o:o + n].copy_(x.cpu().contiguous().view(-1).view(torch.uint8))
+        views.append(d_buf[o:o + n].view(x.dtype).view(x.shape))
+    d_k, d_v, d_s, d_p, d_q = views
     h_out = torch.empty(r.out.shape, dtype=r.out.dtype).pin_memory()
-    d_k, d_v, d_s, d_p, d_q = (torch.empty_like(x, device=dev) for x in (h_k, h_v, h_s, h_p, h_q))
-    h2d = sum(x.numel() * x.element_size() for x in (h_k, h_v, h_s, h_p, h_q))
+    h2d = nb
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        d_k.copy_(h_k, non_blocking=True); d_v.copy_(h_v, non_blocking=True)
-        d_s.copy_(h_s, non_blocking=True); d_p.copy_(h_p, non_blocking=True); d_q.copy_(h_q, non_blocking=True)
+        d_buf.copy_(h_buf, non_blocking=True)
         r.append(d_k, d_v, d_s, d_p, d_q, r.q_out)
         r.flush(w.n_new + w.s_flush)
         r.decode(r.q_out, r.out)
