@@ -307,6 +307,7 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
     float e = __fmaf_rn(hi[m], ch, -p);
     e = __fadd_rn(e, __fadd_rn(__fmul_rn(hi[m], cl), __fmul_rn(lo[m], ch)));
     o[m] = ff_to_bf16(p, e);
+    if (o[m] == 0x8000u) o[m] = 0;                       // an exact zero is +0
   }
   uint2 outv;
   outv.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);

@@ -144,3 +144,64 @@ def test_generator_transforms_inverse_transpose():
     for h in range(2):
         e = tk[h].astype(np.float64).T @ tkit[h].astype(np.float64) - np.eye(128)
         assert np.max(np.abs(e)) < 1e-5          # float32-rounded T^{-T} of the float32 T
+
+
+def _nearest_bf16_decimal(y) -> float:
+    """Nearest bfloat16 to a high-precision Decimal y (no ties occur for irrational values),
+    by enumerating the bit patterns around it."""
+    import decimal
+    t = int(np.float32(float(y)).view(np.uint32) >> 16)
+    best = None
+    for c in (t - 2, t - 1, t, t + 1, t + 2):
+        if not 0 <= c <= 0xFFFF:
+            continue
+        v = float((np.uint32(c) << np.uint32(16)).view(np.float32))
+        if not math.isfinite(v):
+            continue
+        dist = abs(decimal.Decimal(v) - y)
+        if best is None or dist < best[0]:
+            best = (dist, v)
+    return best[1]
+
+
+def test_hadamard_rows_exact_cancellation_and_rounding():
+    """Rows whose Walsh-Hadamard sums cancel exactly (a constant row; small-integer rows) give
+    +0 there -- float64 summation noise must not survive as a tiny bfloat16 -- and every other
+    output is the nearest bfloat16 of S / sqrt(128), checked with 60-digit decimals."""
+    import decimal
+    decimal.getcontext().prec = 60
+    rng = np.random.default_rng(11)
+    rows = [np.full(128, 1.25)]
+    rows += [rng.choice([-2.0, -1.0, 1.0, 2.0], 128) for _ in range(3)]
+    rows += [rng.standard_normal(128) * 2.0 ** rng.integers(-30, 10) for _ in range(2)]
+    x_bits = synth.f32_to_bf16_bits(np.array(rows, np.float32))
+    got = transform.rotate_rows(None, x_bits, "hadamard")
+    x = fp.bf16_to_f32(x_bits).astype(np.float64)
+    sign = scipy.linalg.hadamard(128)
+    root = decimal.Decimal(128).sqrt()
+    zeros = 0
+    for r in range(len(rows)):
+        for i in range(128):
+            S = sum(decimal.Decimal(float(x[r, j])) * int(sign[i, j]) for j in range(128))
+            if S == 0:
+                zeros += 1
+                assert fp.f32_to_bf16_bits(got[r:r + 1, i:i + 1])[0, 0] == 0, (r, i)
+            else:
+                assert float(got[r, i]) == _nearest_bf16_decimal(S / root), (r, i)
+    assert zeros > 127          # the constant row alone contributes 127
+
+
+def test_dense_rows_exact_cancellation():
+    """A dense row that cancels exactly (T_i = (x_1, -x_0, 0, ...)) gives +0, also when the row
+    shares the batch with large rows (float64 blocking must not leak noise into it)."""
+    rng = np.random.default_rng(12)
+    x_bits = synth.f32_to_bf16_bits(rng.standard_normal((5, 128)).astype(np.float32) * 100)
+    x = fp.bf16_to_f32(x_bits)
+    t = rng.standard_normal((128, 128)).astype(np.float32)
+    t[7] = 0.0
+    t[7, 0], t[7, 1] = x[2, 1], -x[2, 0]
+    got = transform.rotate_rows(t, x_bits)
+    assert fp.f32_to_bf16_bits(got[2:3, 7:8])[0, 0] == 0
+    for i in (0, 7, 100):
+        exact = sum(Fraction(float(t[i, j])) * Fraction(float(x[2, j])) for j in range(128))
+        assert float(got[2, i]) == _nearest_by_enumeration(exact, "bf16")
