@@ -25,16 +25,16 @@ def random_workload(seed: int) -> synth.Workload:
     ctx_hi = int(rng.integers(1, 900))
     return synth.Workload(
         name=f"random-{seed}", seed=100 + seed, batch=int(rng.integers(1, 4)), n_q_heads=hkv * g, n_kv_heads=hkv,
-        ctx_lo=int(rng.integers(0, ctx_hi + 1)), ctx_hi=ctx_hi, n_new=int(rng.choice([1, 3, 17, 40])),
+        ctx_lo=int(rng.integers(0, ctx_hi + 1)), ctx_hi=ctx_hi, n_new=int(rng.choice([1, 3, 17, 40, 100])),
         group_size=int(rng.choice([32, 64, 128])), kappa_k=float(rng.choice([1.0, 0.99, 0.95, 0.9])),
         kappa_v=float(rng.choice([1.0, 0.99, 0.95])), quantizer=quantizer, key_l2norm=l2,
         s_sink=s_sink, s_keep=s_keep, s_flush=s_flush,
         transform=str(rng.choice(["orthogonal", "hadamard", "invertible", "identity"])),
         value_transform=str(rng.choice(["orthogonal", "identity"])),
-        key_dist=str(rng.choice(["outlier", "lognormal_norm", "degenerate"])))
+        key_dist=str(rng.choice(["outlier", "lognormal_norm", "degenerate", "wide_exponent"])))
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_configuration(seed):
     w = random_workload(seed)
     run = harness.GpuRun(w)
