@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
         l.kvq_version.restype = ctypes.c_int
         l.kvq_selftest_scale_division.argtypes = [vp, vp]
         l.kvq_selftest_scale_division.restype = ctypes.c_int
+        l.kvq_selftest_tc_integer_sums.argtypes = [vp, vp]
+        l.kvq_selftest_tc_integer_sums.restype = ctypes.c_int
         _lib = l
     return _lib
 
@@ -254,6 +256,14 @@ def kvq_selftest_scale_division(mismatches, stream=None) -> None:
     number of differing results to `mismatches` (a zeroed int64 device tensor of one element)."""
     rc = lib().kvq_selftest_scale_division(_ptr(mismatches), _stream(stream))
     _check(rc, "kvq_selftest_scale_division")
+
+
+def kvq_selftest_tc_integer_sums(mismatches, stream=None) -> None:
+    """Device self-check that the tensor cores add the rotation's integer digit products exactly;
+    adds the number of differing sums to `mismatches` (a zeroed int64 device tensor of one
+    element)."""
+    rc = lib().kvq_selftest_tc_integer_sums(_ptr(mismatches), _stream(stream))
+    _check(rc, "kvq_selftest_tc_integer_sums")
 
 
 def workspace(cfg: KVConfig, max_ctx: int, device="cuda") -> torch.Tensor:

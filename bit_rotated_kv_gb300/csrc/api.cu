@@ -51,6 +51,11 @@ KVQ_API int kvq_selftest_scale_division(unsigned long long* d_mismatches, void* 
   return kvq_launch_div_selftest(d_mismatches, (cudaStream_t)stream);
 }
 
+KVQ_API int kvq_selftest_tc_integer_sums(unsigned long long* d_mismatches, void* stream) {
+  if (!d_mismatches) return KVQ_ERR_INVALID_ARG;
+  return kvq_launch_tc_selftest(d_mismatches, (cudaStream_t)stream);
+}
+
 KVQ_API const char* kvq_status_string(int code) {
   switch (code) {
     case KVQ_OK: return "ok";

@@ -16,6 +16,7 @@ int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_
 int kvq_launch_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, float* out,
                             float sm_scale, int32_t max_ctx, int32_t* d_status, cudaStream_t stream);
 int kvq_launch_div_selftest(unsigned long long* d_mismatches, cudaStream_t stream);
+int kvq_launch_tc_selftest(unsigned long long* d_mismatches, cudaStream_t stream);
 size_t kvq_attn_counter_bytes(const kvq_config* cfg, int32_t max_ctx);
 size_t kvq_attn_ws_bytes(const kvq_config* cfg, int32_t max_ctx);
 void kvq_attn_splits(const kvq_config* cfg, int32_t max_ctx, int* n_int2, int* n_win);

@@ -14,89 +14,10 @@
 // sums).  The matrices stay L2-resident across decode steps.
 // The Hadamard transform is a warp-wide butterfly (two in-thread stages, five shuffle
 // stages) in double-float, then one scaling by 1/sqrt(d).
-#include "common.cuh"
-#include "launch.h"
+#include "rotate.cuh"
 
 namespace kvq {
 
-enum RotMode { ROT_DENSE = 0, ROT_WHT = 1, ROT_COPY = 2 };
-
-struct RotTensor {
-  const uint16_t* src;   // [rows][heads][d]
-  int rows, heads;
-  int mode;              // RotMode
-  const float* mat;      // [mat_heads][d][d] for ROT_DENSE
-  int head_div;          // matrix index = head / head_div
-  int is_query;          // 1: write to q_out; 0: write into the cache
-  uint16_t* dst_q;       // q_out
-  uint16_t* sink;        // cache destination (keys or values)
-  uint16_t* ring;
-  int update_len;        // raise seq_len (keys only)
-};
-
-struct RotParams {
-  RotTensor t[3];
-  int rt;                // rows per chunk of a dense tile (rows that share one matrix)
-  int rpc;               // chunks per dense tile (the matrix is loaded once per tile)
-  int rpw;               // items per warp for exact copies
-  int n_dense[3];        // dense tiles per tensor (0 when not dense)
-  int n_warp[3];         // warp items per tensor (0 when dense)
-  int dense_total, warp_total;
-  const int32_t* seq_idx;
-  const int32_t* pos;
-  int32_t* seq_len;
-  const int32_t* s_quant;
-  int s_sink, ring_cap, batch, hkv;
-  int32_t* status;
-};
-
-// Destination of row `row`, head `h` of tensor tt (b = seq_idx[row], p = pos[row] for cache
-// rows, loaded by the caller); nullptr when the row is skipped.
-__device__ __forceinline__ uint16_t* rot_dst(const RotParams& P, const RotTensor& T, int row, int h, int b,
-                                             int p, bool leader) {
-  if (T.is_query) return T.dst_q + ((size_t)row * T.heads + h) * kHeadDim;
-  if (b < 0 || b >= P.batch || p < 0) {
-    if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
-    return nullptr;
-  }
-  uint16_t* dst;
-  if (p < P.s_sink) {
-    dst = T.sink + (((size_t)b * P.hkv + h) * P.s_sink + p) * kHeadDim;
-  } else {
-    int sq = P.s_quant[b];
-    if (p < sq || p >= sq + P.ring_cap) {
-      if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
-      return nullptr;
-    }
-    dst = T.ring + (((size_t)b * P.hkv + h) * P.ring_cap + (p % P.ring_cap)) * kHeadDim;
-  }
-  if (leader && T.update_len && h == 0) atomicMax(P.seq_len + b, p + 1);
-  return dst;
-}
-
-__device__ __forceinline__ void find_item(const int* counts, int idx, int& tt, int& item) {
-  tt = 0;
-  while (tt < 2 && idx >= counts[tt]) { idx -= counts[tt]; ++tt; }
-  item = idx;
-}
-
-// (row, head) of the p-th pair that uses matrix mh: heads [mh * head_div, (mh + 1) * head_div)
-// share it, so pairs run over rows x those heads.
-__device__ __forceinline__ void tile_row(const RotTensor& T, int mh, int p, int& row, int& head) {
-  row = p / T.head_div;
-  head = mh * T.head_div + p % T.head_div;
-}
-
-// bf16 bits of the exact value y, decided from an fp32 value v with |v - y| <= e: the result
-// when no bf16 rounding midpoint lies within e of v, else -1 (y must be computed exactly).
-__device__ __forceinline__ int bf16_if_decided(float v, float e) {
-  const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
-  const float bv = __uint_as_float(b << 16);
-  const float lo = __uint_as_float(((b - 1u) & 0xffffu) << 16);   // adjacent bf16 values
-  const float hi = __uint_as_float(((b + 1u) & 0xffffu) << 16);
-  const float m1 = 0.5f * (bv + lo), m2 = 0.5f * (bv + hi);        // exact midpoints
-  return (fabsf(v - m1) > e && fabsf(v - m2) > e) ? (int)b : -1;   // NaN compares false
-}
 
 // One dense tile per CTA of 256 threads: chunks of up to RT rows that share matrix mh, the
 // matrix loaded once per tile.  Thread 2i + half
@@ -367,45 +288,6 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
   // values
   P.t[2] = RotTensor{v, n_kv_rows, cfg->n_kv_heads, tr->t_v ? ROT_DENSE : ROT_COPY, tr->t_v, 1, 0,
                      nullptr, cache->sink_v, cache->ring_v, 0};
-  // rows per dense tile: one tile per row while that still fills two CTAs per SM, more rows
-  // per tile (fewer matrix reads) for prefill-sized calls
-  long long dense_pairs = 0;
-  for (int i = 0; i < 3; ++i)
-    if (P.t[i].mode == ROT_DENSE) dense_pairs += (long long)P.t[i].rows * P.t[i].heads;
-  // rows per tile: at most one tile per SM while that is enough (no SM runs two of a handful
-  // of tiles), else about two tiles per SM
-  const long long slots = dense_pairs <= 2 * kSms ? kSms : 2 * kSms;
-  long long rt = (dense_pairs + slots - 1) / slots;
-  P.rt = (int)(rt < 1 ? 1 : (rt > kMaxRT ? kMaxRT : rt));
-  // chunks per tile: one for decode-sized calls; for prefill-sized ones enough that the grid
-  // is about four waves of two tiles per SM, so each 64 KB matrix is read once per many rows
-  long long chunks = 0;
-  for (int i = 0; i < 3; ++i)
-    if (P.t[i].mode == ROT_DENSE)
-      chunks += (long long)(P.t[i].heads / P.t[i].head_div) *
-                (((long long)P.t[i].rows * P.t[i].head_div + P.rt - 1) / P.rt);
-  const long long target = 8LL * kSms;
-  long long rpc = chunks > target ? (chunks + target - 1) / target : 1;
-  P.rpc = (int)(rpc > (1 << 20) ? (1 << 20) : rpc);
-  // copies per warp: one while the copies fit two waves of 16 warps per SM, up to kMaxRPW
-  long long copies = 0;
-  for (int i = 0; i < 3; ++i)
-    if (P.t[i].mode == ROT_COPY) copies += (long long)P.t[i].rows * P.t[i].heads;
-  const long long cslots = 2LL * kSms * 16;
-  P.rpw = (int)(copies > cslots ? min((copies + cslots - 1) / cslots, (long long)kMaxRPW) : 1);
-  for (int i = 0; i < 3; ++i) {
-    const long long items = (long long)P.t[i].rows * P.t[i].heads;
-    const int n_mats = P.t[i].heads / P.t[i].head_div;
-    const long long pairs = (long long)P.t[i].rows * P.t[i].head_div;
-    const long long tiles = (long long)n_mats * ((((pairs + P.rt - 1) / P.rt) + P.rpc - 1) / P.rpc);
-    if (tiles > 0x3fffffffLL || items > 0x3fffffffLL) return KVQ_ERR_UNSUPPORTED;
-    P.n_dense[i] = P.t[i].mode == ROT_DENSE ? (int)tiles : 0;
-    P.n_warp[i] = P.t[i].mode == ROT_DENSE ? 0
-                  : P.t[i].mode == ROT_COPY  ? (int)((items + P.rpw - 1) / P.rpw)
-                                             : (int)items;
-  }
-  P.dense_total = P.n_dense[0] + P.n_dense[1] + P.n_dense[2];
-  P.warp_total = P.n_warp[0] + P.n_warp[1] + P.n_warp[2];
   P.seq_idx = seq_idx;
   P.pos = pos;
   P.seq_len = cache->seq_len;
@@ -415,10 +297,64 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
   P.batch = cfg->batch;
   P.hkv = cfg->n_kv_heads;
   P.status = d_status;
+  long long dense_pairs = 0, copies = 0;
+  for (int i = 0; i < 3; ++i) {
+    if (P.t[i].mode == ROT_DENSE) dense_pairs += (long long)P.t[i].rows * P.t[i].heads;
+    if (P.t[i].mode == ROT_COPY) copies += (long long)P.t[i].rows * P.t[i].heads;
+  }
+  // copies per warp: one while the copies fit two waves of 16 warps per SM, up to kMaxRPW
+  const long long cslots = 2LL * kSms * 16;
+  P.rpw = (int)(copies > cslots ? min((copies + cslots - 1) / cslots, (long long)kMaxRPW) : 1);
+  for (int i = 0; i < 3; ++i) {
+    const long long items = (long long)P.t[i].rows * P.t[i].heads;
+    if (items > 0x3fffffffLL) return KVQ_ERR_UNSUPPORTED;
+    P.n_warp[i] = P.t[i].mode == ROT_DENSE ? 0
+                  : P.t[i].mode == ROT_COPY  ? (int)((items + P.rpw - 1) / P.rpw)
+                                             : (int)items;
+  }
+  const long long warp_total = (long long)P.n_warp[0] + P.n_warp[1] + P.n_warp[2];
+  if (warp_total > 0x3fffffffLL) return KVQ_ERR_UNSUPPORTED;
+  P.warp_total = (int)warp_total;
+  if (dense_pairs >= kTcMinPairs) {
+    // prefill-sized: the warp items (copies, Hadamard rows) on their own, then every dense
+    // tensor on the tensor cores
+    if (P.warp_total > 0) {
+      RotParams W = P;
+      W.dense_total = 0;
+      W.n_dense[0] = W.n_dense[1] = W.n_dense[2] = 0;
+      W.rt = W.rpc = 1;
+      if (launch_pdl(rotate_kernel<false>, dim3((unsigned)((P.warp_total + 7) / 8)), dim3(256), 0, stream, W) !=
+          cudaSuccess)
+        return KVQ_ERR_CUDA;
+    }
+    return launch_rotate_tc(P, stream);
+  }
+  // rows per tile: at most one tile per SM while that is enough (no SM runs two of a handful
+  // of tiles), else about two tiles per SM
+  const long long slots = dense_pairs <= 2 * kSms ? kSms : 2 * kSms;
+  long long rt = (dense_pairs + slots - 1) / slots;
+  P.rt = (int)(rt < 1 ? 1 : (rt > kMaxRT ? kMaxRT : rt));
+  // chunks per tile: one for decode-sized calls; for larger ones enough that the grid is
+  // about four waves of two tiles per SM, so each 64 KB matrix is read once per many rows
+  long long chunks = 0;
+  for (int i = 0; i < 3; ++i)
+    if (P.t[i].mode == ROT_DENSE)
+      chunks += (long long)(P.t[i].heads / P.t[i].head_div) *
+                (((long long)P.t[i].rows * P.t[i].head_div + P.rt - 1) / P.rt);
+  const long long target = 8LL * kSms;
+  long long rpc = chunks > target ? (chunks + target - 1) / target : 1;
+  P.rpc = (int)(rpc > (1 << 20) ? (1 << 20) : rpc);
+  for (int i = 0; i < 3; ++i) {
+    const int n_mats = P.t[i].heads / P.t[i].head_div;
+    const long long pairs = (long long)P.t[i].rows * P.t[i].head_div;
+    const long long tiles = (long long)n_mats * ((((pairs + P.rt - 1) / P.rt) + P.rpc - 1) / P.rpc);
+    if (tiles > 0x3fffffffLL) return KVQ_ERR_UNSUPPORTED;
+    P.n_dense[i] = P.t[i].mode == ROT_DENSE ? (int)tiles : 0;
+  }
+  P.dense_total = P.n_dense[0] + P.n_dense[1] + P.n_dense[2];
   long long blocks = (long long)P.dense_total + (P.warp_total + 7) / 8;
   if (blocks == 0) return KVQ_OK;
   if (blocks > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
   return launch_pdl(P.rpc > 1 ? rotate_kernel<true> : rotate_kernel<false>, dim3((unsigned)blocks), dim3(256), 0,
-                    stream, P) == cudaSuccess ? KVQ_OK
-                                                                                       : KVQ_ERR_CUDA;
+                    stream, P) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

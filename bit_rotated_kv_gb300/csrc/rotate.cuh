@@ -1,0 +1,117 @@
+// Shared declarations of the kv_rotate_qk kernels: the per-call parameters, the destination of
+// a transformed row, and the rounding decision from a bounded approximation.
+#pragma once
+#include "common.cuh"
+#include "launch.h"
+
+namespace kvq {
+
+enum RotMode { ROT_DENSE = 0, ROT_WHT = 1, ROT_COPY = 2 };
+
+struct RotTensor {
+  const uint16_t* src;   // [rows][heads][d]
+  int rows, heads;
+  int mode;              // RotMode
+  const float* mat;      // [mat_heads][d][d] for ROT_DENSE
+  int head_div;          // matrix index = head / head_div
+  int is_query;          // 1: write to q_out; 0: write into the cache
+  uint16_t* dst_q;       // q_out
+  uint16_t* sink;        // cache destination (keys or values)
+  uint16_t* ring;
+  int update_len;        // raise seq_len (keys only)
+};
+
+struct RotParams {
+  RotTensor t[3];
+  int rt;                // rows per chunk of a dense tile (rows that share one matrix)
+  int rpc;               // chunks per dense tile (the matrix is loaded once per tile)
+  int rpw;               // items per warp for exact copies
+  int n_dense[3];        // dense tiles per tensor (0 when not dense)
+  int n_warp[3];         // warp items per tensor (0 when dense)
+  int dense_total, warp_total;
+  const int32_t* seq_idx;
+  const int32_t* pos;
+  int32_t* seq_len;
+  const int32_t* s_quant;
+  int s_sink, ring_cap, batch, hkv;
+  int32_t* status;
+};
+
+// Destination of row `row`, head `h` of tensor tt (b = seq_idx[row], p = pos[row] for cache
+// rows, loaded by the caller); nullptr when the row is skipped.
+__device__ __forceinline__ uint16_t* rot_dst(const RotParams& P, const RotTensor& T, int row, int h, int b,
+                                             int p, bool leader) {
+  if (T.is_query) return T.dst_q + ((size_t)row * T.heads + h) * kHeadDim;
+  if (b < 0 || b >= P.batch || p < 0) {
+    if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+    return nullptr;
+  }
+  uint16_t* dst;
+  if (p < P.s_sink) {
+    dst = T.sink + (((size_t)b * P.hkv + h) * P.s_sink + p) * kHeadDim;
+  } else {
+    int sq = P.s_quant[b];
+    if (p < sq || p >= sq + P.ring_cap) {
+      if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+      return nullptr;
+    }
+    dst = T.ring + (((size_t)b * P.hkv + h) * P.ring_cap + (p % P.ring_cap)) * kHeadDim;
+  }
+  if (leader && T.update_len && h == 0) atomicMax(P.seq_len + b, p + 1);
+  return dst;
+}
+
+__device__ __forceinline__ void find_item(const int* counts, int idx, int& tt, int& item) {
+  tt = 0;
+  while (tt < 2 && idx >= counts[tt]) { idx -= counts[tt]; ++tt; }
+  item = idx;
+}
+
+// (row, head) of the p-th pair that uses matrix mh: heads [mh * head_div, (mh + 1) * head_div)
+// share it, so pairs run over rows x those heads.
+__device__ __forceinline__ void tile_row(const RotTensor& T, int mh, int p, int& row, int& head) {
+  row = p / T.head_div;
+  head = mh * T.head_div + p % T.head_div;
+}
+
+// bf16 bits of the exact value y, decided from an fp32 value v with |v - y| <= e: the result
+// when no bf16 rounding midpoint lies within e of v, else -1 (y must be computed exactly).
+__device__ __forceinline__ int bf16_if_decided(float v, float e) {
+  const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v));
+  const float bv = __uint_as_float(b << 16);
+  const float lo = __uint_as_float(((b - 1u) & 0xffffu) << 16);   // adjacent bf16 values
+  const float hi = __uint_as_float(((b + 1u) & 0xffffu) << 16);
+  const float m1 = 0.5f * (bv + lo), m2 = 0.5f * (bv + hi);        // exact midpoints
+  return (fabsf(v - m1) > e && fabsf(v - m2) > e) ? (int)b : -1;   // NaN compares false
+}
+
+// Exact recomputation of output o of a bf16 row x (128 values, 8-byte aligned, shared or
+// global memory) against T row o (float32, global): double-float products and sums over one
+// warp; lane 0 stores the correctly rounded bf16 result to dst[o].
+__device__ __forceinline__ void exact_output_warp(const float* trow, const uint16_t* xrow, uint16_t* dst, int o,
+                                                  int lane) {
+  const float4 t4 = reinterpret_cast<const float4*>(trow)[lane];
+  const uint2 xr = reinterpret_cast<const uint2*>(xrow)[lane];
+  float hi = 0.f, lo = 0.f;
+  ff_mac(hi, lo, t4.x, __uint_as_float(xr.x << 16));
+  ff_mac(hi, lo, t4.y, __uint_as_float(xr.x & 0xffff0000u));
+  ff_mac(hi, lo, t4.z, __uint_as_float(xr.y << 16));
+  ff_mac(hi, lo, t4.w, __uint_as_float(xr.y & 0xffff0000u));
+#pragma unroll
+  for (int s2 = 16; s2 > 0; s2 >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, s2);
+    const float ol = __shfl_xor_sync(0xffffffffu, lo, s2);
+    ff_add(hi, lo, oh, ol, hi, lo);
+  }
+  if (lane == 0) dst[o] = ff_to_bf16(hi, lo);
+}
+
+// Dense (row, head) pairs from which a call runs its dense tensors on the tensor cores
+// (rotate_tc.cu): about one 128-row block per SM.
+constexpr long long kTcMinPairs = 128LL * kSms;
+
+// Launch of the dense tensors of P on the tensor cores (P.n_dense and the tile sizes are set
+// here; the warp items must already have been launched).
+int launch_rotate_tc(RotParams P, cudaStream_t stream);
+
+}  // namespace kvq

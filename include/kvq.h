@@ -273,6 +273,17 @@ KVQ_API const char* kvq_status_string(int code);
  * a self-test of this implementation.  Returns KVQ_ERR_INVALID_ARG for a NULL pointer. */
 KVQ_API int kvq_selftest_scale_division(unsigned long long* d_mismatches, void* stream);
 
+/* kvq_selftest_tc_integer_sums: for prefill-sized calls kv_rotate_qk runs its dense rows on
+ * the tensor cores with both operands written as integer digits in [-128, 128] (exact
+ * bf16 values), so every accumulated sum is an integer below 2^23; the outputs are exact
+ * as long as the tensor cores add such integers exactly, which the hardware documentation
+ * does not state.  This launches a check of that on the device: hashed and extreme digit
+ * matrices through the rotation's own sequence of MMAs, every accumulator compared with
+ * the integer sum formed on the CUDA cores; the number of differences is ADDED to
+ * *d_mismatches (a device uint64 the caller zeroes).  Not part of the method on the pages:
+ * a self-test of this implementation.  Returns KVQ_ERR_INVALID_ARG for a NULL pointer. */
+KVQ_API int kvq_selftest_tc_integer_sums(unsigned long long* d_mismatches, void* stream);
+
 /* Library ABI version (major * 100 + minor). */
 KVQ_API int kvq_version(void);
 

@@ -109,6 +109,7 @@ def test_rotate_validation(kvq):
 
 def test_selftest_rejects_null(kvq):
     assert kvq.lib().kvq_selftest_scale_division(None, None) == -1
+    assert kvq.lib().kvq_selftest_tc_integer_sums(None, None) == -1
 
 
 def test_status_strings(kvq):
