@@ -267,6 +267,26 @@ __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
   else warp_item(P, tt, item, threadIdx.x & 31);
 }
 
+
+// Warp items only (exact copies, Hadamard rows): the launch that accompanies the tensor-core
+// kernel.  Without the dense path's register footprint it runs at full occupancy.
+__global__ void __launch_bounds__(256) rotate_items_kernel(const RotParams Pk) {
+  pdl_trigger();
+  __shared__ RotParams Ps;
+  if (threadIdx.x == 0) Ps = Pk;
+  __syncthreads();
+  const RotParams& P = Ps;
+  const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (w >= P.warp_total) {
+    pdl_wait();
+    return;
+  }
+  int tt, item;
+  find_item(P.n_warp, w, tt, item);
+  if (P.t[tt].mode == ROT_COPY) warp_copies(P, tt, item, threadIdx.x & 31);
+  else warp_item(P, tt, item, threadIdx.x & 31);
+}
+
 }  // namespace kvq
 
 using namespace kvq;
@@ -323,7 +343,7 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
       W.dense_total = 0;
       W.n_dense[0] = W.n_dense[1] = W.n_dense[2] = 0;
       W.rt = W.rpc = 1;
-      if (launch_pdl(rotate_kernel<false>, dim3((unsigned)((P.warp_total + 7) / 8)), dim3(256), 0, stream, W) !=
+      if (launch_pdl(rotate_items_kernel, dim3((unsigned)((P.warp_total + 7) / 8)), dim3(256), 0, stream, W) !=
           cudaSuccess)
         return KVQ_ERR_CUDA;
     }

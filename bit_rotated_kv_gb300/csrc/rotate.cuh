@@ -38,9 +38,10 @@ struct RotParams {
 };
 
 // Destination of row `row`, head `h` of tensor tt (b = seq_idx[row], p = pos[row] for cache
-// rows, loaded by the caller); nullptr when the row is skipped.
+// rows, loaded by the caller; sq_loaded = s_quant[b] when the caller has loaded it, else -1);
+// nullptr when the row is skipped.
 __device__ __forceinline__ uint16_t* rot_dst(const RotParams& P, const RotTensor& T, int row, int h, int b,
-                                             int p, bool leader) {
+                                             int p, bool leader, int sq_loaded = -1) {
   if (T.is_query) return T.dst_q + ((size_t)row * T.heads + h) * kHeadDim;
   if (b < 0 || b >= P.batch || p < 0) {
     if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
@@ -50,7 +51,7 @@ __device__ __forceinline__ uint16_t* rot_dst(const RotParams& P, const RotTensor
   if (p < P.s_sink) {
     dst = T.sink + (((size_t)b * P.hkv + h) * P.s_sink + p) * kHeadDim;
   } else {
-    int sq = P.s_quant[b];
+    const int sq = sq_loaded >= 0 ? sq_loaded : P.s_quant[b];   // s_quant[b], if already loaded
     if (p < sq || p >= sq + P.ring_cap) {
       if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
       return nullptr;

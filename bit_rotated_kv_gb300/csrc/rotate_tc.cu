@@ -46,7 +46,7 @@ constexpr int kXSlice = kUmRows * kHeadDim * 2;      // one x digit matrix: 16 K
 constexpr int kXBuf = 3 * kXSlice;                   // three digit matrices per chunk buffer
 constexpr int kList = 256;                           // queued undecided outputs per warp
 
-// per-row metadata of a chunk (three buffers: chunk n, n + 1 being sliced, n + 2)
+// per-row metadata of a chunk (four buffers: warps run up to three chunks apart)
 struct UmRow {
   uint16_t* dst;         // destination row (nullptr: nothing to write)
   const uint16_t* src;   // the source row (for exact recomputation)
@@ -58,12 +58,19 @@ struct UmRow {
 static_assert(sizeof(UmRow) == 32, "UmRow layout");
 constexpr int kRowZero = 1, kRowBad = 2, kRowLossy = 4;
 
+constexpr int kWorkers = 16;                         // warps that slice rows and decide outputs
+constexpr int kThreads = 32 * (kWorkers + 1);        // + one warp that issues the MMAs
+constexpr int kRowsPerWarp = kUmRows / kWorkers;     // rows a worker warp slices per chunk
+constexpr int kParts = kWorkers / 4;                 // worker warps per TMEM lane quadrant
+constexpr int kEpiRows = kUmRows / kParts;           // rows (accumulator columns) per thread
+constexpr int kTSpan = kHeadDim / kParts;            // entries of a T row per thread
+
 constexpr int kMetaOff = 2 * kXBuf;
-constexpr int kListOff = kMetaOff + 3 * kUmRows * (int)sizeof(UmRow);
-constexpr int kExchOff = kListOff + 8 * kList * 2;
-constexpr int kUmUsed = kExchOff + 3 * 1024;   // exponent exchange [2][128] int, sums [2][128] u64
+constexpr int kListOff = kMetaOff + 4 * kUmRows * (int)sizeof(UmRow);
+constexpr int kExchOff = kListOff + kWorkers * kList * 2;
+constexpr int kUmUsed = kExchOff + 2 * kParts * 128 * 4;   // exponent and |T| sum exchange
 // more than half of an SM's shared memory: never two CTAs on one SM (each holds all of TMEM)
-constexpr int kUmSmem = 118 * 1024;
+constexpr int kUmSmem = 120 * 1024;
 static_assert(kUmUsed + 1024 <= kUmSmem, "shared memory layout");
 
 constexpr uint32_t kTmemCols = 512;
@@ -134,12 +141,26 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
       : "r"(taddr));
 }
 #undef UM_O8
+#define UM_O8(b)                                                                                            \
+  "=r"(v[b]), "=r"(v[b + 1]), "=r"(v[b + 2]), "=r"(v[b + 3]), "=r"(v[b + 4]), "=r"(v[b + 5]), "=r"(v[b + 6]), \
+      "=r"(v[b + 7])
+// 16 consecutive TMEM columns of this warp's 32 lanes -> registers (not yet waited for)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : UM_O8(0), UM_O8(8)
+      : "r"(taddr));
+}
+#undef UM_O8
 // wait for this thread's TMEM loads; the registers pass through so no use moves above it
 #define UM_IO8(b)                                                                                           \
   "+r"(v[b]), "+r"(v[b + 1]), "+r"(v[b + 2]), "+r"(v[b + 3]), "+r"(v[b + 4]), "+r"(v[b + 5]), "+r"(v[b + 6]), \
       "+r"(v[b + 7])
 __device__ __forceinline__ void tmem_wait_ld32(uint32_t* v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : UM_IO8(0), UM_IO8(8), UM_IO8(16), UM_IO8(24)::"memory");
+}
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t* v) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : UM_IO8(0), UM_IO8(8)::"memory");
 }
 #undef UM_IO8
 
@@ -180,72 +201,91 @@ __device__ __forceinline__ void issue_chunk(uint32_t tb, uint32_t xbuf) {
   }
 }
 
-// T row i, K half `half` (64 entries, global) -> the four digit matrices in TMEM columns
-// 64 b + 32 half + ..., this warp's lanes.  e_i is the row's exponent field (both halves);
-// returns sum_j M_j of this half (M_j = |T_ij| / U_i in units of 2^-24, truncated).
-__device__ __forceinline__ unsigned long long slice_t_half(const float* trow, int e_i, uint32_t taddr) {
-  unsigned long long msum = 0;
+// v * 2^k, exact whenever the result is a normal float (k in [-126, 254])
+__device__ __forceinline__ float scale_pow2(float v, int k) {
+  if (k > 127) {
+    v *= 0x1p64f;
+    k -= 64;
+  }
+  return v * __int_as_float((k + 127) << 23);
+}
+
+// bf16 bits of two integer-valued floats of at most 8 significant bits (exact), low = a
+__device__ __forceinline__ uint32_t pack_digits(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// Balanced base-256 digits of X (|X| < 128): X = d0 + d1/2^8 + d2/2^16 (+ d3/2^24) + rest,
+// each digit an integer in [-128, 128] (round to nearest, so the rest is at most half a unit
+// of the last digit).  Every step is exact in fp32.
+__device__ __forceinline__ float next_digit(float& r) {
+  const float d = rintf(r);
+  r = (r - d) * 256.0f;
+  return d;
+}
+
+// T row i, entries kTSpan part .. (global) -> the four digit matrices in TMEM columns
+// 64 b + kTSpan / 2 part + ..., this warp's lanes.  Returns sum_j |T_ij| / U_i over them.
+__device__ __forceinline__ float slice_t_part(const float* trow, int e_i, uint32_t taddr) {
+  const int k = 133 - e_i;
+  float asum = 0.f;
 #pragma unroll 1
-  for (int blk = 0; blk < 4; ++blk) {
+  for (int blk = 0; blk < kTSpan / 16; ++blk) {
     uint32_t out[4][8];
 #pragma unroll
     for (int j4 = 0; j4 < 4; ++j4) {
       const float4 t4 = reinterpret_cast<const float4*>(trow)[4 * blk + j4];
+      float d[2][2][4];                                 // [pair element][column][digit]
       const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
 #pragma unroll
       for (int m2 = 0; m2 < 4; ++m2) {
-        const uint32_t u = __float_as_uint(tv[m2]);
-        const int E = (int)((u >> 23) & 0xffu);
-        const uint32_t m = E ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
-        const int sh = e_i - max(E, 1);
-        uint32_t M = sh < 31 ? (m << 7) >> sh : 0u;
-        msum += M;
-        int d[4];
-        d[3] = take_digit(M);
-        d[2] = take_digit(M);
-        d[1] = take_digit(M);
-        d[0] = (int)M;
-        const bool neg = (u >> 31) != 0u;
-        const int col = 2 * j4 + (m2 >> 1), hi = m2 & 1;
+        float r = scale_pow2(tv[m2], k);
+        asum += fabsf(r);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const uint32_t bits = digit_bf16(neg ? -d[b] : d[b]);
-          out[b][col] = hi ? (out[b][col] | (bits << 16)) : bits;
-        }
+        for (int b = 0; b < 4; ++b) d[m2 & 1][m2 >> 1][b] = next_digit(r);
       }
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) out[b][2 * j4 + c2] = pack_digits(d[0][c2][b], d[1][c2][b]);
     }
 #pragma unroll
     for (int b = 0; b < 4; ++b) tmem_st8(taddr + 64u * (uint32_t)b + 8u * (uint32_t)blk, out[b]);
   }
-  return msum;
+  return asum;
 }
 
-// One warp's 8 rows of a chunk, loaded ahead of slicing.
+// One worker warp's rows of a chunk, loaded ahead of slicing.
 struct XPre {
-  uint2 x[8];             // this lane's 4 bf16 (k = 4 lane .. 4 lane + 3) of rows 8 w + j
-  int row, head, b, p;    // lanes 0..7: indices of row 8 w + lane (b, p for cache rows)
-  int valid;              // lanes 0..7: the row exists
+  uint2 x[kRowsPerWarp];  // this lane's 4 bf16 (k = 4 lane .. 4 lane + 3) of rows R w + j
+  int row, head, b, p;    // lanes 0..R-1: indices of row R w + lane (b, p for cache rows)
+  int sq;                 // lanes 0..R-1: s_quant[b] (cache rows, loaded after the dependency wait)
+  int valid;              // lanes 0..R-1: the row exists
 };
 
+// after_wait: s_quant may be read (it is written by the previous kernel of a step)
 __device__ __forceinline__ void x_prefetch(const RotParams& P, const RotTensor& T, int mh, int chunk, int pairs,
-                                           int warp, int lane, XPre& pre) {
+                                           int warp, int lane, bool after_wait, XPre& pre) {
   const int p0 = chunk * kUmRows, np = min(kUmRows, pairs - p0);
-  const int r = 8 * warp + (lane & 7);
-  pre.valid = (lane < 8 && r < np) ? 1 : 0;
+  const int r = kRowsPerWarp * warp + (lane % kRowsPerWarp);
+  pre.valid = (lane < kRowsPerWarp && r < np) ? 1 : 0;
   int row = 0, head = 0;
   if (r < np) tile_row(T, mh, p0 + r, row, head);
   pre.row = row;
   pre.head = head;
   pre.b = pre.p = 0;
+  pre.sq = -1;
   if (pre.valid && !T.is_query) {
     pre.b = __ldg(P.seq_idx + row);
     pre.p = __ldg(P.pos + row);
+    if (after_wait && pre.b >= 0 && pre.b < P.batch) pre.sq = P.s_quant[pre.b];
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < kRowsPerWarp; ++j) {
     const int rj = __shfl_sync(0xffffffffu, row, j), hj = __shfl_sync(0xffffffffu, head, j);
     pre.x[j] = make_uint2(0u, 0u);
-    if (8 * warp + j < np)
+    if (kRowsPerWarp * warp + j < np)
       pre.x[j] = __ldg(reinterpret_cast<const uint2*>(T.src + ((size_t)rj * T.heads + hj) * kHeadDim) + lane);
   }
 }
@@ -258,66 +298,45 @@ __device__ __forceinline__ void x_slice(const RotParams& P, const RotTensor& T, 
   const uint16_t* src = nullptr;
   if (pre.valid) {
     src = T.src + ((size_t)pre.row * T.heads + pre.head) * kHeadDim;
-    dst = rot_dst(P, T, pre.row, pre.head, pre.b, pre.p, true);
+    dst = rot_dst(P, T, pre.row, pre.head, pre.b, pre.p, true, pre.sq);
   }
-#pragma unroll 2
-  for (int j = 0; j < 8; ++j) {
-    const int r = 8 * warp + j;
-    const uint32_t h[4] = {pre.x[j].x & 0xffffu, pre.x[j].x >> 16, pre.x[j].y & 0xffffu, pre.x[j].y >> 16};
-    int ef = 1;
-    bool bad_l = false, nz_l = false;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int E = (int)((h[k] >> 7) & 0xffu);
-      ef = max(ef, max(E, 1));
-      bad_l |= E == 255;
-      nz_l |= (h[k] & 0x7fffu) != 0u;
-    }
-    const int fr = __reduce_max_sync(0xffffffffu, ef);
-    const bool bad = __any_sync(0xffffffffu, bad_l), nz = __any_sync(0xffffffffu, nz_l);
-    uint32_t lo[3] = {0u, 0u, 0u}, hi[3] = {0u, 0u, 0u};
-    uint32_t nsum = 0;
+  for (int j = 0; j < kRowsPerWarp; ++j) {
+    const float xf[4] = {__uint_as_float(pre.x[j].x << 16), __uint_as_float(pre.x[j].x & 0xffff0000u),
+                         __uint_as_float(pre.x[j].y << 16), __uint_as_float(pre.x[j].y & 0xffff0000u)};
+    const uint32_t am = max(max(__float_as_uint(fabsf(xf[0])), __float_as_uint(fabsf(xf[1]))),
+                            max(__float_as_uint(fabsf(xf[2])), __float_as_uint(fabsf(xf[3]))));
+    const uint32_t amax = __reduce_max_sync(0xffffffffu, am);     // non-negative floats order as integers
+    const int fr = max(1, (int)(amax >> 23));                        // (a NaN is caught by `bad`)
+    const bool bad = amax >= 0x7f800000u, zero = amax == 0u;
+    const int k = 133 - fr;
+    float d[3][4];
     bool lost_l = false;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int E = (int)((h[k] >> 7) & 0xffu);
-      const uint32_t m = E ? ((h[k] & 0x7fu) | 0x80u) : (h[k] & 0x7fu);
-      const int sh = fr - max(E, 1);
-      const uint32_t full = m << 15;
-      uint32_t N = sh < 32 ? full >> sh : 0u;
-      const bool lost = sh < 32 ? ((N << sh) != full) : (full != 0u);
-      lost_l |= lost;
-      nsum += N + (lost ? 1u : 0u);
-      int d[3];
-      d[2] = take_digit(N);
-      d[1] = take_digit(N);
-      d[0] = (int)N;
-      const bool neg = (h[k] >> 15) != 0u;
+    for (int m2 = 0; m2 < 4; ++m2) {
+      float r = scale_pow2(xf[m2], k);
+      lost_l |= (r == 0.f) && (xf[m2] != 0.f);
 #pragma unroll
-      for (int a = 0; a < 3; ++a) {
-        const uint32_t bits = digit_bf16(neg ? -d[a] : d[a]);
-        if (k < 2) lo[a] |= bits << (16 * k);
-        else hi[a] |= bits << (16 * (k - 2));
-      }
+      for (int a = 0; a < 3; ++a) d[a][m2] = next_digit(r);
+      lost_l |= r != 0.f;
     }
     const bool lossy = __any_sync(0xffffffffu, lost_l);
-    const uint32_t sx = __reduce_add_sync(0xffffffffu, nsum);
-    const int off = xs_offset(r, 4 * lane);
+    const int offj = xs_offset(kRowsPerWarp * warp + j, 4 * lane);
 #pragma unroll
-    for (int a = 0; a < 3; ++a) *reinterpret_cast<uint2*>(xb + a * kXSlice + off) = make_uint2(lo[a], hi[a]);
+    for (int a = 0; a < 3; ++a)
+      *reinterpret_cast<uint2*>(xb + a * kXSlice + offj) =
+          make_uint2(pack_digits(d[a][0], d[a][1]), pack_digits(d[a][2], d[a][3]));
     uint16_t* dj = (uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)dst, j);
     const uint16_t* sj = (const uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)src, j);
     if (lane == 0) {
       UmRow m;
       m.dst = dj;
       m.src = sj;
-      // dropped digit products and the fp32 combination (2^-10, 2^-17) and T's truncation,
-      // 2^-24 per unit of sum |x| (sx / 2^16 bounds sum |x| in units)
-      m.c = 0x1.01p-10f + 0x1p-17f + (float)sx * 0x1.01p-40f;
+      m.c = 0.f;
       m.fr = fr;
-      m.flags = (nz ? 0 : kRowZero) | (bad ? kRowBad : 0) | (lossy ? kRowLossy : 0);
+      m.flags = (zero ? kRowZero : 0) | (bad ? kRowBad : 0) | (lossy ? kRowLossy : 0);
       m.pad = 0;
-      meta[r] = m;
+      meta[kRowsPerWarp * warp + j] = m;
     }
   }
 }
@@ -334,23 +353,55 @@ __device__ __noinline__ int exact_list(const uint16_t* list, int count, const Um
   return 0;
 }
 
-// One CTA per tile: P.rpc chunks of 64 (row, head) pairs that share one matrix.
-__global__ void __launch_bounds__(256, 1) rotate_tc_kernel(const RotParams Pk) {
+// Bounded wait that also gives up when another warp has given up.
+__device__ __noinline__ bool um_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  for (long long it = 0; it < kSpinLimit; ++it) {
+    if (um_mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+  }
+  *abort_flag = 1;
+  return false;
+}
+// The same, decided by lane 0 for the whole warp (so the warp stays converged).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
+  int ok = 0;
+  if (lane == 0) ok = um_wait(bar, parity, abort_flag) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+__device__ __forceinline__ void um_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(um_saddr(bar)) : "memory");
+}
+
+// Constant part of the bound, units of U_i V_r: T's digits kept to 2^-25 (2^-25 sum |x| <=
+// 2^-11), the digit products dropped ((1,3), (2,2): 2^-11 each; (2,3): 2^-19) and the fp32
+// combination of the levels beyond 3u|v| (2^-17).
+constexpr float kBoundConst = 0x1.9p-10f;
+
+// One CTA per tile: P.rpc chunks of 64 (row, head) pairs that share one matrix.  Warps
+// 0 .. kWorkers - 1 slice rows and decide outputs; the last warp issues the MMAs.
+__global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams Pk) {
   pdl_trigger();
   __shared__ RotParams Ps;
   __shared__ uint32_t tbase_sh;
-  __shared__ __align__(8) uint64_t mbar[2];
-  __shared__ int tile_bad, abort_sh;
+  __shared__ __align__(8) uint64_t bar_x[2], bar_acc, bar_mma[2];
+  __shared__ int tile_bad;
+  __shared__ volatile int abort_sh;
   extern __shared__ uint8_t um_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(um_smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int q = warp & 3, half = warp >> 2, i = 32 * q + lane;
+  const bool worker = warp < kWorkers;
+  const int q = warp & 3, part = (warp >> 2) % kParts, i = 32 * q + lane;
   if (tid == 0) {
     Ps = Pk;
     tile_bad = 0;
     abort_sh = 0;
-    um_mbar_init(&mbar[0]);
-    um_mbar_init(&mbar[1]);
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(um_saddr(&bar_x[0])), "r"(kWorkers) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(um_saddr(&bar_x[1])), "r"(kWorkers) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(um_saddr(&bar_acc)), "r"(kWorkers) : "memory");
+    um_mbar_init(&bar_mma[0]);
+    um_mbar_init(&bar_mma[1]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -375,19 +426,21 @@ __global__ void __launch_bounds__(256, 1) rotate_tc_kernel(const RotParams Pk) {
   const int c0 = (tile % tiles_per_mat) * P.rpc, nch = min(cpm, c0 + P.rpc) - c0;
   const float* tmat = T.mat + (size_t)mh * kHeadDim * kHeadDim;
   UmRow* meta = reinterpret_cast<UmRow*>(sm + kMetaOff);
-  uint16_t* list = reinterpret_cast<uint16_t*>(sm + kListOff) + warp * kList;
-  int* ex_e = reinterpret_cast<int*>(sm + kExchOff);                        // [2][128]
-  unsigned long long* ex_m = reinterpret_cast<unsigned long long*>(sm + kExchOff + 1024);   // [2][128]
+  uint16_t* list = reinterpret_cast<uint16_t*>(sm + kListOff) + (warp % kWorkers) * kList;
+  int* ex_e = reinterpret_cast<int*>(sm + kExchOff);                           // [kParts][128]
+  float* ex_s = reinterpret_cast<float*>(sm + kExchOff + kParts * 128 * 4);    // [kParts][128]
+  auto xbuf = [&](int n) { return sm + (n & 1) * kXBuf; };
 
   // ---- the matrix (a caller input: before the dependency wait) ----
   XPre pre;
-  x_prefetch(P, T, mh, c0, pairs, warp, lane, pre);
-  const float* trow = tmat + (size_t)i * kHeadDim + 64 * half;
-  int e_i, tnz;
-  {
+  int e_i = 1, tnz = 0;
+  float st16 = 0.f;
+  const float* trow = tmat + (size_t)i * kHeadDim + kTSpan * part;
+  if (worker) {
+    x_prefetch(P, T, mh, c0, pairs, warp, lane, false, pre);
     int e = 1, nz = 0, bad = 0;
 #pragma unroll 4
-    for (int j4 = 0; j4 < 16; ++j4) {
+    for (int j4 = 0; j4 < kTSpan / 4; ++j4) {
       const float4 t4 = reinterpret_cast<const float4*>(trow)[j4];
       const uint32_t u[4] = {__float_as_uint(t4.x), __float_as_uint(t4.y), __float_as_uint(t4.z), __float_as_uint(t4.w)};
 #pragma unroll
@@ -398,100 +451,125 @@ __global__ void __launch_bounds__(256, 1) rotate_tc_kernel(const RotParams Pk) {
         nz |= (u[m2] & 0x7fffffffu) != 0u;
       }
     }
-    ex_e[half * 128 + i] = e | (nz << 16);
+    ex_e[part * 128 + i] = e | (nz << 16);
     if (bad) tile_bad = 1;
-    __syncthreads();
-    const int a0 = ex_e[i], a1 = ex_e[128 + i];
-    e_i = max(a0 & 0xffff, a1 & 0xffff);
-    tnz = (a0 | a1) >> 16;
   }
-  ex_m[half * 128 + i] = slice_t_half(trow, e_i, tb + tlane + 32u * (uint32_t)half);
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
   __syncthreads();
-  // 2^-16 sum_j |T_ij| / U_i (rounded up): X's truncation bound for lossy rows
-  const float st16 = (float)(ex_m[i] + ex_m[128 + i] + 128ull) * 0x1.01p-40f;
+  if (worker) {
+#pragma unroll
+    for (int pp = 0; pp < kParts; ++pp) {
+      const int a = ex_e[pp * 128 + i];
+      e_i = max(e_i, a & 0xffff);
+      tnz |= a >> 16;
+    }
+    ex_s[part * 128 + i] =
+        slice_t_part(trow, e_i, tb + tlane + (uint32_t)(kTSpan / 2) * (uint32_t)part);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // X's truncation (lossy rows): 2^-16 sum_j |T_ij| / U_i, rounded up
+  if (worker) {
+    float ssum = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < kParts; ++pp) ssum += ex_s[pp * 128 + i];
+    st16 = ssum * 0x1.01p-16f;
+  }
   const bool force = tile_bad != 0;
 
   pdl_wait();
-  // ---- pipeline: slice chunk n + 2 while the tensor cores run chunk n + 1 ----
-  auto xbuf = [&](int n) { return sm + (n & 1) * kXBuf; };
-  x_slice(P, T, pre, xbuf(0), meta, warp, lane);
-  if (nch > 1) x_prefetch(P, T, mh, c0 + 1, pairs, warp, lane, pre);
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  tc_fence_before();
-  __syncthreads();
-  if (tid == 0) {
-    tc_fence_after();
-    issue_chunk(tb, um_saddr(xbuf(0)));
-    umma_commit(&mbar[0]);
-  }
-  if (nch > 1) {
-    x_slice(P, T, pre, xbuf(1), meta + kUmRows, warp, lane);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (nch > 2) x_prefetch(P, T, mh, c0 + 2, pairs, warp, lane, pre);
-  }
-  int count = 0, stuck = -1;
-  for (int n = 0; n < nch; ++n) {
-    const int timed_out = um_mbar_wait(&mbar[n & 1], (uint32_t)((n >> 1) & 1)) ? 0 : 1;
-    stuck = n;
-    tc_fence_after();
-    uint32_t acc[4][32];
-#pragma unroll
-    for (int L = 0; L < 4; ++L) tmem_ld32(tb + tlane + kAccCol + 64u * (uint32_t)L + 32u * (uint32_t)half, acc[L]);
-#pragma unroll
-    for (int L = 0; L < 4; ++L) tmem_wait_ld32(acc[L]);
-    tc_fence_before();
-    // accumulators free; chunk n + 1's digits written; every thread takes the same exit
-    if (__syncthreads_or(timed_out)) {
-      abort_sh = 1;
-      break;
-    }
-    if (tid == 0 && n + 1 < nch) {
-      tc_fence_after();
-      issue_chunk(tb, um_saddr(xbuf(n + 1)));
-      umma_commit(&mbar[(n + 1) & 1]);
-    }
-    // ---- rounding decisions of chunk n: this thread's output i, rows 32 half + c ----
-    const UmRow* mrow = meta + (n % 3) * kUmRows;
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const int r = 32 * half + c;
-      uint16_t* dst = mrow[r].dst;
-      const float cr = mrow[r].c;
-      const int fr = mrow[r].fr, flags = mrow[r].flags;
-      const float L0 = __uint_as_float(acc[0][c]), L1 = __uint_as_float(acc[1][c]);
-      const float L2 = __uint_as_float(acc[2][c]), L3 = __uint_as_float(acc[3][c]);
-      const float v = fmaf(L3, 0x1p-24f, fmaf(L2, 0x1p-16f, fmaf(L1, 0x1p-8f, L0)));
-      // |y / (U_i V_r) - v| <= 3u|v| + the row's terms (+ X's truncation for lossy rows)
-      const float bnd = fmaf(fabsf(v), 0x1.81p-23f, (flags & kRowLossy) ? cr + st16 : cr);
-      int b = bf16_if_decided(v, bnd);
-      if (b >= 0) {
-        const int Eu = (b >> 7) & 0xff, S = e_i + fr - 266, Ey = Eu + S;
-        b = (Eu != 0 && Ey >= 1 && Ey <= 254) ? b + (S << 7) : -1;
+  if (!worker) {
+    // ---- MMA warp: chunk n once its digits are written and chunk n - 1's sums were read ----
+    if (lane == 0) {
+      int last = -1;
+      for (int n = 0; n < nch; ++n) {
+        if (!um_wait(&bar_x[n & 1], (uint32_t)((n >> 1) & 1), &abort_sh)) break;
+        if (n > 0 && !um_wait(&bar_acc, (uint32_t)((n - 1) & 1), &abort_sh)) break;
+        tc_fence_after();
+        issue_chunk(tb, um_saddr(xbuf(n)));
+        umma_commit(&bar_mma[n & 1]);
+        last = n;
       }
-      if ((flags & kRowZero) || !tnz) b = 0;             // an exact zero is +0
-      if (force || (flags & kRowBad)) b = -1;
-      if (dst != nullptr && b >= 0) dst[i] = (uint16_t)b;
-      const bool und = dst != nullptr && b < 0;
-      const unsigned mk = __ballot_sync(0xffffffffu, und);
-      if (und) list[count + __popc(mk & ((1u << lane) - 1u))] = (uint16_t)((r << 7) | i);
-      count += __popc(mk);
-      if (count > kList - 32) count = exact_list(list, count, mrow, tmat, lane);
+      if (abort_sh && last >= 0) {
+        set_status(P.status, KVQ_ERR_TIMEOUT);
+        uint32_t fl = 0;      // the last committed chunk must finish before TMEM is released
+        for (long long it = 0; it < kSpinLimit && !um_mbar_try(&bar_mma[last & 1], (uint32_t)((last >> 1) & 1)); ++it)
+          fl++;
+      }
     }
-    count = exact_list(list, count, mrow, tmat, lane);
-    // ---- digits of chunk n + 2 into chunk n's buffer (its MMAs have completed) ----
-    if (n + 2 < nch) {
-      x_slice(P, T, pre, xbuf(n), meta + ((n + 2) % 3) * kUmRows, warp, lane);
+  } else {
+    // ---- worker warps ----
+    auto publish = [&](int n) {             // chunk n's digits (buffer n & 1) -> the MMA warp
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      if (n + 3 < nch) x_prefetch(P, T, mh, c0 + n + 3, pairs, warp, lane, pre);
+      __syncwarp();
+      if (lane == 0) um_arrive(&bar_x[n & 1]);
+    };
+    x_slice(P, T, pre, xbuf(0), meta, warp, lane);
+    publish(0);
+    if (nch > 1) {
+      x_prefetch(P, T, mh, c0 + 1, pairs, warp, lane, true, pre);
+      x_slice(P, T, pre, xbuf(1), meta + kUmRows, warp, lane);
+      publish(1);
+      if (nch > 2) x_prefetch(P, T, mh, c0 + 2, pairs, warp, lane, true, pre);
     }
-  }
-  if (abort_sh) {
-    // chunk `stuck` is the only one committed and not seen complete: give it one more bounded
-    // wait before TMEM is released
-    if (tid == 0) {
-      set_status(P.status, KVQ_ERR_TIMEOUT);
-      (void)um_mbar_wait(&mbar[stuck & 1], (uint32_t)((stuck >> 1) & 1));
+    int count = 0;
+    for (int n = 0; n < nch; ++n) {
+      if (!warp_wait(&bar_mma[n & 1], (uint32_t)((n >> 1) & 1), &abort_sh, lane)) break;
+      tc_fence_after();
+      uint32_t acc[4][kEpiRows];
+#pragma unroll
+      for (int L = 0; L < 4; ++L)
+        tmem_ld16(tb + tlane + kAccCol + 64u * (uint32_t)L + (uint32_t)(kEpiRows * part), acc[L]);
+#pragma unroll
+      for (int L = 0; L < 4; ++L) tmem_wait_ld16(acc[L]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) um_arrive(&bar_acc);
+      // ---- rounding decisions of chunk n: output i, rows kEpiRows part + c ----
+      // All rows first, without control flow (independent chains the scheduler interleaves);
+      // undecided outputs are queued afterwards, only when the warp has any.
+      const UmRow* mrow = meta + (n & 3) * kUmRows;
+      uint32_t und_bits = 0;
+#pragma unroll
+      for (int c = 0; c < kEpiRows; ++c) {
+        const int r = kEpiRows * part + c;
+        uint16_t* dst = mrow[r].dst;
+        const int fr = mrow[r].fr, flags = mrow[r].flags;
+        const float v = fmaf(__uint_as_float(acc[3][c]), 0x1p-24f,
+                             fmaf(__uint_as_float(acc[2][c]), 0x1p-16f,
+                                  fmaf(__uint_as_float(acc[1][c]), 0x1p-8f, __uint_as_float(acc[0][c]))));
+        const float bnd = fmaf(fabsf(v), 0x1.81p-23f, (flags & kRowLossy) ? kBoundConst + st16 : kBoundConst);
+        // the midpoint above v's bf16 truncation; with bound < |v| / 1024 no other midpoint is
+        // as close (the decision is the same after the exact scaling by 2^S below)
+        const float mid = __uint_as_float((__float_as_uint(v) & 0xffff0000u) | 0x8000u);
+        const bool decided = fabsf(v - mid) > bnd && bnd * 1024.0f < fabsf(v);
+        const int bu = (int)__bfloat16_as_ushort(__float2bfloat16_rn(v));
+        // y = v 2^S, S = e_i + f_r - 266: shift the exponent field; the result must stay normal
+        const int ey = ((bu >> 7) & 0xff) + e_i + fr;
+        int b = (decided && (unsigned)(ey - 267) < 254u) ? bu + (ey - 266 - ((bu >> 7) & 0xff)) * 128 : -1;
+        b = ((flags & kRowZero) || !tnz) ? 0 : b;           // an exact zero is +0
+        b = (force || (flags & kRowBad)) ? -1 : b;
+        if (dst != nullptr && b >= 0) dst[i] = (uint16_t)b;
+        und_bits |= (dst != nullptr && b < 0) ? (1u << c) : 0u;
+      }
+      if (__any_sync(0xffffffffu, und_bits != 0u)) {
+#pragma unroll 1
+        for (int c = 0; c < kEpiRows; ++c) {
+          const bool und = (und_bits >> c) & 1u;
+          const unsigned mk = __ballot_sync(0xffffffffu, und);
+          if (und) list[count + __popc(mk & ((1u << lane) - 1u))] = (uint16_t)(((kEpiRows * part + c) << 7) | i);
+          count += __popc(mk);
+          if (count > kList - 32) count = exact_list(list, count, mrow, tmat, lane);
+        }
+      }
+      count = exact_list(list, count, mrow, tmat, lane);
+      // ---- digits of chunk n + 2 into chunk n's buffer (its MMAs have completed) ----
+      if (n + 2 < nch) {
+        x_slice(P, T, pre, xbuf(n), meta + ((n + 2) & 3) * kUmRows, warp, lane);
+        publish(n + 2);
+        if (n + 3 < nch) x_prefetch(P, T, mh, c0 + n + 3, pairs, warp, lane, true, pre);
+      }
     }
   }
   tc_fence_before();
@@ -658,7 +736,7 @@ int launch_rotate_tc(RotParams P, cudaStream_t stream) {
       attr_done |= 1ull << dev;
     }
   }
-  return launch_pdl(rotate_tc_kernel, dim3((unsigned)dense_total), dim3(256), (size_t)kUmSmem, stream, P) ==
+  return launch_pdl(rotate_tc_kernel, dim3((unsigned)dense_total), dim3(kThreads), (size_t)kUmSmem, stream, P) ==
                  cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
