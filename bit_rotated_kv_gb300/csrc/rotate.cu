@@ -144,31 +144,41 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
 }
 
 // Exact copies (identity transform): one warp per P.rpw consecutive (row, head) items, all of
-// their loads in flight before the first store.
+// their loads in flight before the first store.  Lane k < rpw resolves item k's indices and
+// destination (one division per warp, no per-lane repetition); the rows are then moved 8
+// bytes per lane with the destination taken from lane k.
 __device__ void warp_copies(const RotParams& P, int tt, int witem, int lane) {
   const RotTensor& T = P.t[tt];
   const int item0 = witem * P.rpw;
   const int n = min(P.rpw, T.rows * T.heads - item0);
-  int bb[kMaxRPW], pp[kMaxRPW];
+  const int row0 = item0 / T.heads, h0 = item0 - row0 * T.heads;
+  // item k = (row0 + (h0 + k) / heads, (h0 + k) % heads), k < rpw <= kMaxRPW <= heads or not
+  int krow = row0, kh = h0 + (lane < n ? lane : 0);
+  while (kh >= T.heads) {
+    kh -= T.heads;
+    ++krow;
+  }
+  int kb = 0, kp = 0;
+  if (lane < n && !T.is_query) {
+    kb = P.seq_idx[krow];
+    kp = P.pos[krow];
+  }
   uint2 raw[kMaxRPW];
 #pragma unroll
   for (int k = 0; k < kMaxRPW; ++k) {
-    bb[k] = pp[k] = 0;
     raw[k] = make_uint2(0u, 0u);
     if (k < n) {
-      const int item = item0 + k, row = item / T.heads, h = item - row * T.heads;
-      bb[k] = P.seq_idx[row];
-      pp[k] = P.pos[row];
-      raw[k] = reinterpret_cast<const uint2*>(T.src + ((size_t)row * T.heads + h) * kHeadDim)[lane];
+      const int rk = __shfl_sync(0xffffffffu, krow, k), hk = __shfl_sync(0xffffffffu, kh, k);
+      raw[k] = reinterpret_cast<const uint2*>(T.src + ((size_t)rk * T.heads + hk) * kHeadDim)[lane];
     }
   }
   pdl_wait();                           // (the caller's inputs above: see dense_tile)
+  uint16_t* dst = lane < n ? rot_dst(P, T, krow, kh, kb, kp, true) : nullptr;
 #pragma unroll
   for (int k = 0; k < kMaxRPW; ++k) {
     if (k < n) {
-      const int item = item0 + k, row = item / T.heads, h = item - row * T.heads;
-      uint16_t* dst = rot_dst(P, T, row, h, bb[k], pp[k], lane == 0);
-      if (dst != nullptr) reinterpret_cast<uint2*>(dst)[lane] = raw[k];
+      uint16_t* d = (uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)dst, k);
+      if (d != nullptr) reinterpret_cast<uint2*>(d)[lane] = raw[k];
     }
   }
 }
