@@ -190,6 +190,10 @@ KVQ_API size_t kvq_page_bytes(const kvq_config* cfg);
  *            KVQ_ERR_BOUNDS in *d_status.  seq_len[b] is raised to pos + 1.
  * q, k, v and the matrices must be 16-byte aligned, q_out 8-byte aligned
  * (KVQ_ERR_INVALID_ARG otherwise).
+ * Execution: one kernel for decode-sized calls.  From 19,456 dense (row, head) pairs on
+ * (about one 128-row block per SM) the dense rows run on the tensor cores and the copies /
+ * Hadamard rows in a second kernel launched first; the outputs are bit-identical either way
+ * (see kvq_selftest_tc_integer_sums for the one hardware property that path relies on).
  * Source: [WUSH] inference algorithm (transform each new key and query, append at
  * full precision); [OScaR] algorithm, key and query processing (online FHT of K and Q). */
 KVQ_API int kv_rotate_qk(const kvq_config* cfg, const kvq_transform* tr,
