@@ -387,6 +387,323 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   }
 }
 
+// ---- prefill-sized flushes: two rows per warp -----------------------------------------------
+// Half-warp hr = lane / 16 takes one row; lane hl = lane % 16 of it owns channels 8 hl ..
+// 8 hl + 7, so a group of G channels spans G / 8 lanes.  Every per-row step that the whole
+// warp executes once per row (order-statistic merges, the scale arithmetic, the code packing,
+// the stores) is shared by two rows.  The arithmetic is the one-row kernel's, step for step.
+
+__device__ __forceinline__ void cswap(float& a, float& b) {
+  const float t = fminf(a, b);
+  b = fmaxf(a, b);
+  a = t;
+}
+// ascending; an optimal 19-comparator network for 8 inputs
+__device__ __forceinline__ void sort8(float (&s)[8]) {
+  cswap(s[0], s[1]); cswap(s[2], s[3]); cswap(s[4], s[5]); cswap(s[6], s[7]);
+  cswap(s[0], s[2]); cswap(s[1], s[3]); cswap(s[4], s[6]); cswap(s[5], s[7]);
+  cswap(s[1], s[2]); cswap(s[5], s[6]); cswap(s[0], s[4]); cswap(s[3], s[7]);
+  cswap(s[1], s[5]); cswap(s[2], s[6]);
+  cswap(s[1], s[4]); cswap(s[3], s[6]);
+  cswap(s[2], s[4]); cswap(s[3], s[5]);
+  cswap(s[3], s[4]);
+}
+
+// as group_topk, from each lane's 8 sorted values
+template <int K, bool TOP>
+__device__ __forceinline__ void group_topk8(const float (&s)[8], int nl, float (&r)[K]) {
+#pragma unroll
+  for (int i = 0; i < K; ++i) r[i] = TOP ? s[7 - i] : s[i];
+  for (int o = nl >> 1; o > 0; o >>= 1) {
+    float w[K], m[K];
+#pragma unroll
+    for (int i = 0; i < K; ++i) w[i] = __shfl_xor_sync(0xffffffffu, r[i], o);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      float best = TOP ? fmaxf(r[k], w[k]) : fminf(r[k], w[k]);
+#pragma unroll
+      for (int i = 1; i <= k; ++i) {
+        const float t = TOP ? fminf(r[i - 1], w[k - i]) : fmaxf(r[i - 1], w[k - i]);
+        best = TOP ? fmaxf(best, t) : fminf(best, t);
+      }
+      m[k] = best;
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) r[k] = m[k];
+  }
+}
+
+// as extract, from each lane's 8 sorted values
+template <bool TOP>
+__device__ __forceinline__ void extract8(const float (&s)[8], int n, int nl, unsigned gmask, int lane,
+                                         float& cur, float& prev) {
+  int ptr = TOP ? 7 : 0;
+  float cand = TOP ? s[7] : s[0];
+  cur = prev = cand;
+  for (int it = 0; it < n; ++it) {
+    float m = cand;
+    for (int o = nl >> 1; o > 0; o >>= 1) {
+      const float other = __shfl_xor_sync(0xffffffffu, m, o);
+      m = TOP ? fmaxf(m, other) : fminf(m, other);
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, cand == m) & gmask;
+    if (lane == __ffs(bal) - 1) {
+      ptr += TOP ? -1 : 1;
+      float next = TOP ? -INFINITY : INFINITY;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (ptr == q) next = s[q];
+      cand = next;
+    }
+    prev = cur;
+    cur = m;
+  }
+}
+
+template <bool TOP>
+__device__ __forceinline__ void order_stats8(const float (&s)[8], int n, int nl, unsigned gmask, int lane,
+                                             float& cur, float& prev) {
+  switch (n) {
+    case 1: { float r[1]; group_topk8<1, TOP>(s, nl, r); cur = prev = r[0]; break; }
+    case 2: { float r[2]; group_topk8<2, TOP>(s, nl, r); cur = r[1]; prev = r[0]; break; }
+    case 3: { float r[3]; group_topk8<3, TOP>(s, nl, r); cur = r[2]; prev = r[1]; break; }
+    case 4: { float r[4]; group_topk8<4, TOP>(s, nl, r); cur = r[3]; prev = r[2]; break; }
+    default: extract8<TOP>(s, n, nl, gmask, lane, cur, prev); break;
+  }
+}
+
+// quant_row for a half-warp row: 8 values per lane, Q.nl = G / 8 lanes per group
+__device__ __forceinline__ void quant_row8(const QuantConsts& Q, const float (&y)[8], int lane,
+                                           uint32_t (&code)[8], __half2& dz, bool& bad) {
+  const int nl = Q.nl;
+  const unsigned gmask = ((1u << nl) - 1u) << ((lane & 16) + ((lane & 15) & ~(nl - 1)));
+  __half d16, z16;
+  if (Q.affine) {
+    float s[8] = {y[0], y[1], y[2], y[3], y[4], y[5], y[6], y[7]};
+    sort8(s);
+    float hc, hp, lc, lp;
+    order_stats8<true>(s, Q.n_hi, nl, gmask, lane, hc, hp);
+    order_stats8<false>(s, Q.n_lo, nl, gmask, lane, lc, lp);
+    const int g = Q.group;
+    float hi = (Q.i_hi >= g - 1) ? hc : __fadd_rn(hc, __fmul_rn(Q.f_hi, __fsub_rn(hp, hc)));
+    float lo = (Q.i_lo >= g - 1) ? lc : __fadd_rn(lp, __fmul_rn(Q.f_lo, __fsub_rn(lc, lp)));
+    float delta = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
+    d16 = __float2half_rn(delta);
+    if (__half2float(d16) == 0.0f) d16 = __float2half_rn(1.0f);
+    float z = -__fdiv_rn(lo, __half2float(d16));
+    z16 = __float2half_rn(z);
+  } else {
+    double ss = 0.0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[m], (double)y[m]));
+    for (int o = nl >> 1; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    double rms = __dsqrt_rn(__ddiv_rn(ss, (double)Q.group));
+    double delta = __ddiv_rn(__dmul_rn(__dmul_rn(2.0, Q.alpha), rms), 3.0);
+    d16 = double_to_half_rn(delta);
+    if (__half2float(d16) == 0.0f) d16 = __float2half_rn(1.0f);
+    z16 = __float2half_rn(1.5f);
+  }
+  float df = __half2float(d16), zf = __half2float(z16);
+  if (!isfinite(df) || !isfinite(zf)) bad = true;
+  float qv[8];
+  div4_by_scale(*reinterpret_cast<const float(*)[4]>(&y[0]), df, *reinterpret_cast<float(*)[4]>(&qv[0]));
+  div4_by_scale(*reinterpret_cast<const float(*)[4]>(&y[4]), df, *reinterpret_cast<float(*)[4]>(&qv[4]));
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int c = __float2int_rn(__fadd_rn(qv[m], zf));
+    code[m] = (uint32_t)min(max(c, 0), 3);
+  }
+  dz = __halves2half2(d16, z16);
+}
+
+__global__ void __launch_bounds__(256, 3) flush_kernel2(const FlushParams Pk) {
+  pdl_trigger();
+  __shared__ FlushParams Ps;
+  if (threadIdx.x == 0) Ps = Pk;
+  __syncthreads();
+  const FlushParams& P = Ps;
+  const int b = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hr = lane >> 4, hl = lane & 15;
+  const int nwarps = blockDim.x >> 5;
+  {
+    // warm L2 with this half's first ring row (a prefetch only; see flush_kernel)
+    const int sq_g = P.s_quant[b];
+    const int r0 = (blockIdx.x * P.items_per_cta + warp + hr * nwarps) >> 1;
+    const int t = r0 / P.hkv, hh = r0 - t * P.hkv;
+    const int tok = sq_g + t;
+    if (hl < 2 && tok >= P.s_sink) {
+      const uint16_t* ring = (warp & 1) ? P.ring_v : P.ring_k;
+      prefetch_l2_line(ring + (((size_t)b * P.hkv + hh) * P.ring_cap + tok % P.ring_cap) * kHeadDim + 64 * hl);
+    }
+  }
+  pdl_wait();
+  const int L = P.seq_len[b], sq = P.s_quant[b];
+  int n;
+  {
+    const int avail = L - sq - P.s_keep;
+    n = avail >= P.s_flush ? (avail / P.s_flush) * P.s_flush : 0;
+    const int cap = (P.max_tokens / P.s_flush) * P.s_flush;
+    n = n < cap ? n : cap;
+    if (sq < P.s_sink || L < 0) {
+      if (lane == 0 && warp == 0) set_status(P.status, KVQ_ERR_BOUNDS);
+      n = 0;
+    }
+  }
+  __syncthreads();
+  int ticket = -1;
+  if (threadIdx.x == 0) {
+    if (gridDim.x == 1) P.s_quant[b] = sq + n;
+    else ticket = atomic_add_release_gpu(P.counters + b, 1);
+  }
+  const int ng = kHeadDim / P.group;
+  // items (token, kv head, K|V) as in flush_kernel; warp w takes items i0 + w + k nwarps
+  // (all of kind w & 1), half hr the ones with k = hr mod 2
+  const int n_items = n * P.hkv * 2;
+  const int i0 = blockIdx.x * P.items_per_cta;
+  const int i1 = min(n_items, i0 + P.items_per_cta);
+  const int which = warp & 1;
+  const uint16_t* ring = which ? P.ring_v : P.ring_k;
+  const int hkv = P.hkv, rcap = P.ring_cap;
+  QuantConsts Q;
+  Q.nl = P.group >> 3;
+  Q.group = P.group;
+  Q.affine = P.quantizer == KVQ_QUANT_AFFINE_KAPPA;
+  Q.n_hi = P.n_hi[which];
+  Q.n_lo = P.n_lo[which];
+  Q.i_hi = P.i_hi[which];
+  Q.i_lo = P.i_lo[which];
+  Q.f_hi = P.f_hi[which];
+  Q.f_lo = P.f_lo[which];
+  Q.alpha = P.alpha;
+  const bool key_norm = which == 0 && P.l2;
+  const int s_sink = P.s_sink, max_pages = P.max_pages, num_pages = P.num_pages, page_bytes = P.page_bytes;
+  const int32_t* ptab = P.page_table + (size_t)b * max_pages;
+  uint8_t* const pages = P.pages;
+  // this half's row position, advanced by nwarps (token, head) steps per iteration
+  int item = i0 + warp + hr * nwarps;
+  int nx_h = 0, nx_tok = 0, nx_slot = 0, pid_n = -1;
+  uint4 raw_n = make_uint4(0u, 0u, 0u, 0u);
+  auto fetch = [&]() {
+    const int pidx = (nx_tok - s_sink) >> 4;
+    pid_n = (pidx < max_pages) ? ptab[pidx] : -1;
+    raw_n = *reinterpret_cast<const uint4*>(
+        ring + (((size_t)b * hkv + nx_h) * rcap + nx_slot) * kHeadDim + 8 * hl);
+  };
+  {
+    const int r0 = item >> 1, t = r0 / hkv;
+    nx_h = r0 - t * hkv;
+    nx_tok = sq + t;
+    nx_slot = nx_tok % rcap;
+    if (item < i1) fetch();
+  }
+  for (int base = i0 + warp; base < i1; base += 2 * nwarps, item += 2 * nwarps) {
+    const bool live = item < i1;
+    const int tok = nx_tok, h = nx_h, pid = pid_n;
+    const uint4 raw = raw_n;
+    nx_h += nwarps;
+    while (nx_h >= hkv) {
+      nx_h -= hkv;
+      ++nx_tok;
+      if (++nx_slot == rcap) nx_slot = 0;
+    }
+    if (item + 2 * nwarps < i1) fetch();
+    const int tp = (tok - s_sink) & (kPage - 1);
+    const bool pid_ok = pid >= 0 && pid < num_pages;
+    if (live && !pid_ok && hl == 0) set_status(P.status, KVQ_ERR_BOUNDS);
+    const bool valid = live && pid_ok;
+    uint8_t* chunk = pages + ((size_t)(valid ? pid : 0) * hkv + h) * page_bytes;
+    bool bad = false;
+    float y[8];
+    y[0] = __uint_as_float(raw.x << 16);
+    y[1] = __uint_as_float(raw.x & 0xffff0000u);
+    y[2] = __uint_as_float(raw.y << 16);
+    y[3] = __uint_as_float(raw.y & 0xffff0000u);
+    y[4] = __uint_as_float(raw.z << 16);
+    y[5] = __uint_as_float(raw.z & 0xffff0000u);
+    y[6] = __uint_as_float(raw.w << 16);
+    y[7] = __uint_as_float(raw.w & 0xffff0000u);
+    if (!valid) {
+#pragma unroll
+      for (int m = 0; m < 8; ++m) y[m] = 0.0f;
+    }
+    if (key_norm) {
+      double ss = 0.0;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[m], (double)y[m]));
+      for (int o = 8; o > 0; o >>= 1) ss = __dadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+      __half s16 = double_to_half_rn(__dsqrt_rn(ss));
+      float sf = __half2float(s16);
+      if (!isfinite(sf)) bad = true;
+      // both halves divide (the division's warp vote needs the whole warp); a zero norm gives
+      // a zero row
+      const float sdiv = sf == 0.0f ? 1.0f : sf;
+      float yn[8];
+      div4_by_scale(*reinterpret_cast<const float(*)[4]>(&y[0]), sdiv, *reinterpret_cast<float(*)[4]>(&yn[0]));
+      div4_by_scale(*reinterpret_cast<const float(*)[4]>(&y[4]), sdiv, *reinterpret_cast<float(*)[4]>(&yn[4]));
+#pragma unroll
+      for (int m = 0; m < 8; ++m) y[m] = sf == 0.0f ? 0.0f : yn[m];
+      if (valid && hl == 0) reinterpret_cast<__half*>(chunk + norm_off(ng))[tp] = s16;
+    }
+    __half2 dz;
+    uint32_t c[8];
+    quant_row8(Q, y, lane, c, dz, bad);
+    const int nl = Q.nl;
+    if (valid && (hl & (nl - 1)) == 0) {
+      const int g = hl / nl;
+      if (which == 0) {
+        *reinterpret_cast<__half2*>(chunk + k_scale_off() + (tp * ng + g) * 4) = dz;
+      } else {
+        *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g)) = __low2half(dz);
+        *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g)) = __high2half(dz);
+      }
+    }
+    // Pack as flush_kernel does: channels 8 hl + 4 j + m are those of the one-row kernel's lane
+    // 2 hl + j, whose words land at bits 2 (hl >> 1) and 16 + 2 (hl >> 1); OR over the lanes of
+    // equal hl % 2.  Lane hl < 2 then holds the words of class 2 hl + j.
+    const int sh = 2 * (hl >> 1);
+    uint32_t u[2][2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      u[j][0] = (c[4 * j] << sh) | (c[4 * j + 1] << (16 + sh));
+      u[j][1] = (c[4 * j + 2] << sh) | (c[4 * j + 3] << (16 + sh));
+    }
+#pragma unroll
+    for (int o = 2; o < 16; o <<= 1)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        u[j][0] |= __shfl_xor_sync(0xffffffffu, u[j][0], o);
+        u[j][1] |= __shfl_xor_sync(0xffffffffu, u[j][1], o);
+      }
+    if (valid && hl < 2) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int hi = hl, lo = j;
+        if (which == 0) {
+          uint32_t* kw = reinterpret_cast<uint32_t*>(chunk);
+          const int kb = (4 * (tp & 7) + 2 * lo) * 4 + 2 * hi + (tp >> 3);
+          kw[kb] = u[j][0];
+          kw[kb + 4] = u[j][1];
+        } else {
+          uint16_t* vw = reinterpret_cast<uint16_t*>(chunk + kCodeBytes);
+          const int off = 2 * (((tp & 7) >> 1) * 4 + 2 * (tp >> 3) + hi) + (tp & 1);
+          const int rr = 4 * lo;
+          vw[2 * (4 * rr) * 4 + off] = (uint16_t)(u[j][0] & 0xffffu);
+          vw[2 * (4 * (rr + 1)) * 4 + off] = (uint16_t)(u[j][0] >> 16);
+          vw[2 * (4 * (rr + 2)) * 4 + off] = (uint16_t)(u[j][1] & 0xffffu);
+          vw[2 * (4 * (rr + 3)) * 4 + off] = (uint16_t)(u[j][1] >> 16);
+        }
+      }
+    }
+    if (bad && valid && hl == 0) set_status(P.status, KVQ_ERR_NONFINITE);
+  }
+  if (threadIdx.x == 0 && ticket == (int)gridDim.x - 1) {
+    __threadfence();
+    P.s_quant[b] = sq + n;
+    P.counters[b] = 0;
+  }
+}
+
 // ---- self-check of the scale division ------------------------------------------------------
 // div_by_scale against IEEE division for every finite bf16 y and every positive finite
 // float16 d (the whole domain of the unscaled quantizer: 65,280 x 31,743 pairs), plus 2^29
@@ -503,5 +820,8 @@ extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, i
   P.items_per_cta = (int)ipc;
   const int ctas = (int)((items + ipc - 1) / ipc);
   dim3 grid(ctas, cfg->batch);
-  return launch_pdl(flush_kernel, grid, dim3(threads), 0, stream, P) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  // prefill-sized flushes take two rows per warp (the per-row warp work is shared)
+  return launch_pdl(threads == 256 ? flush_kernel2 : flush_kernel, grid, dim3(threads), 0, stream, P) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
 }
