@@ -9,8 +9,9 @@
 // rounding are not documented, so no output may depend on them.  Each operand is written as
 // fixed-point digits on a grid common to the whole dot product:
 //   * T row i (float32, 24-bit significands) in units U_i = 2^(e_i - 133), e_i the largest
-//     exponent field of the row: |T_ij| / U_i < 128, kept to 2^-24 units as four balanced
-//     base-256 digits t_0 + t_1/2^8 + t_2/2^16 + t_3/2^24, each an integer in [-128, 128];
+//     exponent field of the row: |T_ij| / U_i < 128, kept to 2^-25 units as four balanced
+//     base-256 digits t_0 + t_1/2^8 + t_2/2^16 + t_3/2^24, each an integer in [-128, 128]
+//     (round-to-nearest extraction in fp32, every step exact);
 //   * x row r (bf16, 8-bit significands) in units V_r = 2^(f_r - 133), likewise three digits
 //     kept to 2^-16 units (exact unless an element lies 16 or more binades below the row's
 //     largest).
@@ -21,19 +22,21 @@
 // products with a + b <= 3 go to four fp32 accumulators by level L = a + b:
 //   y = U_i V_r sum_L 2^(-8 L) D_L + (dropped digits and truncation, bounded below),
 // and the CUDA cores combine the four levels, bound the remainder, and decide the correctly
-// rounded bf16 whenever no rounding midpoint lies within that bound; the rest (about 0.01%
-// of outputs on the pages' workloads) are recomputed exactly in double-float.
+// rounded bf16 whenever no rounding midpoint lies within that bound; the rest (none of 4.2 M
+// outputs on the pages' key rows and matrices; non-finite and subnormal results always) are
+// recomputed exactly in double-float.
 //
-// Layout (one CTA of 8 warps per SM, it holds all 512 TMEM columns):
+// Layout (one CTA of 17 warps per SM, it holds all 512 TMEM columns):
 //   TMEM columns   0..255  the four T digit matrices, A operand (lane = output i, K packed
 //                          two bf16 per column), written once per tile;
 //   TMEM columns 256..511  the four level accumulators D_L for a chunk of 64 rows
 //                          (lane = output i, column = row);
 //   shared memory          the three x digit matrices of a chunk (B operand, K-major,
 //                          128-byte swizzle), double-buffered; per-row metadata.
-// One thread issues the 72 MMAs of a chunk (M = 128, N = 64, K = 16 each) while the other
-// warps slice the next chunk's rows; the accumulators are read into registers at once, so the
-// next chunk's MMAs overlap this chunk's rounding decisions and stores.
+// Warp 16 issues the 72 MMAs of a chunk (M = 128, N = 64, K = 16 each) as soon as the
+// chunk's digits are written and the previous chunk's sums were read; warps 0-15 read the
+// accumulators into registers at once (so the next chunk's MMAs overlap this chunk's rounding
+// decisions and stores), then slice the rows of the chunk after next.
 #include "rotate.cuh"
 
 #include <mutex>
@@ -50,7 +53,7 @@ constexpr int kList = 256;                           // queued undecided outputs
 struct UmRow {
   uint16_t* dst;         // destination row (nullptr: nothing to write)
   const uint16_t* src;   // the source row (for exact recomputation)
-  float c;               // bound terms of the row, units of U_i V_r
+  float c;               // (unused)
   int fr;                // exponent field f_r of the row's units
   int flags;             // kRowZero | kRowBad | kRowLossy
   int pad;
