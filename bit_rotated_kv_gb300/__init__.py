@@ -37,7 +37,8 @@ KVQ_TRANSFORM_DENSE = 0
 KVQ_TRANSFORM_HADAMARD = 1
 
 EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_attn_decode", "kv_attn_decode_noalloc", "kv_attn_workspace_bytes",
-            "kvq_page_head_bytes", "kvq_page_bytes", "kvq_status_string", "kvq_version")
+            "kvq_page_head_bytes", "kvq_page_bytes", "kvq_status_string", "kvq_version",
+            "kvq_selftest_scale_division", "kvq_selftest_tc_integer_sums")
 
 
 class CConfig(ctypes.Structure):
