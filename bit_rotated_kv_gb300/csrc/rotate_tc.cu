@@ -53,10 +53,9 @@ constexpr int kList = 256;                           // queued undecided outputs
 struct UmRow {
   uint16_t* dst;         // destination row (nullptr: nothing to write)
   const uint16_t* src;   // the source row (for exact recomputation)
-  float c;               // (unused)
   int fr;                // exponent field f_r of the row's units
   int flags;             // kRowZero | kRowBad | kRowLossy
-  int pad;
+  int pad[2];
 };
 static_assert(sizeof(UmRow) == 32, "UmRow layout");
 constexpr int kRowZero = 1, kRowBad = 2, kRowLossy = 4;
@@ -85,6 +84,24 @@ constexpr long long kSpinLimit = 1LL << 22;      // try_wait rounds before a wai
 
 // ---- tcgen05 / mbarrier primitives ---------------------------------------------------------
 __device__ __forceinline__ uint32_t um_saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+// explicit shared-memory accesses (the buffers are reached through a re-aligned pointer, which
+// the compiler would otherwise treat as generic)
+__device__ __forceinline__ void sts_v2(uint32_t a, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void sts_u64(uint32_t a, unsigned long long x) {
+  asm volatile("st.shared.u64 [%0], %1;" ::"r"(a), "l"(x) : "memory");
+}
+__device__ __forceinline__ unsigned long long lds_u64(uint32_t a) {
+  unsigned long long x;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(x) : "r"(a) : "memory");
+  return x;
+}
+__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+  uint2 x;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x.x), "=r"(x.y) : "r"(a) : "memory");
+  return x;
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -327,19 +344,15 @@ __device__ __forceinline__ void x_slice(const RotParams& P, const RotTensor& T, 
     const int offj = xs_offset(kRowsPerWarp * warp + j, 4 * lane);
 #pragma unroll
     for (int a = 0; a < 3; ++a)
-      *reinterpret_cast<uint2*>(xb + a * kXSlice + offj) =
-          make_uint2(pack_digits(d[a][0], d[a][1]), pack_digits(d[a][2], d[a][3]));
+      sts_v2(um_saddr(xb) + (uint32_t)(a * kXSlice + offj), pack_digits(d[a][0], d[a][1]),
+             pack_digits(d[a][2], d[a][3]));
     uint16_t* dj = (uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)dst, j);
     const uint16_t* sj = (const uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)src, j);
     if (lane == 0) {
-      UmRow m;
-      m.dst = dj;
-      m.src = sj;
-      m.c = 0.f;
-      m.fr = fr;
-      m.flags = (zero ? kRowZero : 0) | (bad ? kRowBad : 0) | (lossy ? kRowLossy : 0);
-      m.pad = 0;
-      meta[kRowsPerWarp * warp + j] = m;
+      const uint32_t ma = um_saddr(meta + kRowsPerWarp * warp + j);
+      sts_u64(ma, (unsigned long long)dj);
+      sts_u64(ma + 8, (unsigned long long)sj);
+      sts_v2(ma + 16, (uint32_t)fr, (uint32_t)((zero ? kRowZero : 0) | (bad ? kRowBad : 0) | (lossy ? kRowLossy : 0)));
     }
   }
 }
@@ -533,12 +546,15 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
       // All rows first, without control flow (independent chains the scheduler interleaves);
       // undecided outputs are queued afterwards, only when the warp has any.
       const UmRow* mrow = meta + (n & 3) * kUmRows;
+      const uint32_t mrow_s = um_saddr(mrow);
       uint32_t und_bits = 0;
 #pragma unroll
       for (int c = 0; c < kEpiRows; ++c) {
         const int r = kEpiRows * part + c;
-        uint16_t* dst = mrow[r].dst;
-        const int fr = mrow[r].fr, flags = mrow[r].flags;
+        const uint32_t ma = mrow_s + (uint32_t)r * (uint32_t)sizeof(UmRow);
+        uint16_t* dst = (uint16_t*)lds_u64(ma);
+        const uint2 ff = lds_v2(ma + 16);
+        const int fr = (int)ff.x, flags = (int)ff.y;
         const float v = fmaf(__uint_as_float(acc[3][c]), 0x1p-24f,
                              fmaf(__uint_as_float(acc[2][c]), 0x1p-16f,
                                   fmaf(__uint_as_float(acc[1][c]), 0x1p-8f, __uint_as_float(acc[0][c]))));
@@ -553,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
         int b = (decided && (unsigned)(ey - 267) < 254u) ? bu + (ey - 266 - ((bu >> 7) & 0xff)) * 128 : -1;
         b = ((flags & kRowZero) || !tnz) ? 0 : b;           // an exact zero is +0
         b = (force || (flags & kRowBad)) ? -1 : b;
-        if (dst != nullptr && b >= 0) dst[i] = (uint16_t)b;
+        if (dst != nullptr && b >= 0) __stcg(reinterpret_cast<unsigned short*>(dst + i), (unsigned short)b);
         und_bits |= (dst != nullptr && b < 0) ? (1u << c) : 0u;
       }
       if (__any_sync(0xffffffffu, und_bits != 0u)) {
