@@ -324,13 +324,12 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
       __half s16 = double_to_half_rn(__dsqrt_rn(ss));
       float sf = __half2float(s16);
       if (!isfinite(sf)) bad = true;
-      if (sf == 0.0f) {
-        y[0] = y[1] = y[2] = y[3] = 0.0f;
-      } else {
-        float yn[4];
-        div4_by_scale(y, sf, yn);
-        y[0] = yn[0]; y[1] = yn[1]; y[2] = yn[2]; y[3] = yn[3];
-      }
+      // the division's warp vote stays outside any branch; a zero norm gives a zero row
+      const float sdiv = sf == 0.0f ? 1.0f : sf;
+      float yn[4];
+      div4_by_scale(y, sdiv, yn);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) y[m] = sf == 0.0f ? 0.0f : yn[m];
       if (lane == 0) reinterpret_cast<__half*>(chunk + norm_off(ng))[tp] = s16;
     }
     __half2 dz;
