@@ -340,7 +340,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
 
 def workload(args) -> synth.Workload:
     """The configuration, optionally shrunk (--batch) for a profiler capture of the same kernel."""
-    w = synth.CONFIGS[args.config]
+    w = synth.WORKLOADS[args.config]
     if args.batch:
         w = w.replace(batch=args.batch)
     return w
@@ -364,7 +364,7 @@ def oracle_step_sample(config: int, budget_s: float) -> dict:
     the workload until about budget_s of CPU time has been spent; returns GB/s equivalent."""
     from oracle import attention, cache, quant, transform
     from oracle.fp import bf16_to_f32, f32_to_bf16_bits
-    w = synth.CONFIGS[config]
+    w = synth.WORKLOADS[config]
     tk, tkit, tv = synth.transforms(w)
     lengths = synth.context_lengths(w)
     ctx = lengths
@@ -492,7 +492,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank == 0:
             cb = cpu_baseline(args.config, args.cpu_budget)
-            w = synth.CONFIGS[args.config]
+            w = synth.WORKLOADS[args.config]
             res = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": world,
                    "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
                    "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",

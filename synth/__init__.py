@@ -107,25 +107,26 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# Configurations (shapes and distributions follow the hot-path scope table).
-CONFIGS: dict[int, Workload] = {
-    1: Workload(name="tiny-gqa4-ctx512", seed=0, batch=1, n_q_heads=4, n_kv_heads=1,
-                ctx_lo=504, ctx_hi=504, n_new=8, group_size=128, kappa_k=0.99, kappa_v=0.99,
-                s_sink=16, s_keep=128, s_flush=8, key_dist="fixed_outlier", outlier_scale=20.0,
-                fixed_outlier_channels=(3, 77)),
-    2: Workload(name="qwen3-8b-ctx32k-b1", seed=2, batch=1, n_q_heads=32, n_kv_heads=8,
-                ctx_lo=32760, ctx_hi=32760, n_new=8, group_size=128, kappa_k=0.99, kappa_v=0.99),
-    3: Workload(name="qwen3-4b-b64-ctx4k-8k", seed=3, batch=64, n_q_heads=32, n_kv_heads=8,
-                ctx_lo=4096, ctx_hi=8192, n_new=1, group_size=64, kappa_k=0.995, kappa_v=0.995),
-    4: Workload(name="qwen3-32b-ctx128k-b4-oscar", seed=4, batch=4, n_q_heads=64, n_kv_heads=8,
-                ctx_lo=131072, ctx_hi=131072, n_new=1, group_size=32, kappa_k=1.0, kappa_v=1.0,
-                key_l2norm=True, s_sink=0, s_keep=0, s_flush=128, transform="hadamard",
-                value_transform="identity", key_dist="lognormal_norm"),
-    5: Workload(name="wush-qwen3-8b-b16-chunk2048-on-16k", seed=5, batch=16, n_q_heads=32,
-                n_kv_heads=8, ctx_lo=16384, ctx_hi=16384, n_new=2048, group_size=128,
-                kappa_k=0.99, kappa_v=0.99, transform="invertible", value_transform="identity",
-                chunk_queries=True),
-}
+# The pages' workloads (shapes and distributions follow the hot-path scope table), by name;
+# WORKLOADS numbers them for the bench's --config option.
+TINY_GQA4 = Workload(name="tiny-gqa4-ctx512", seed=0, batch=1, n_q_heads=4, n_kv_heads=1,
+                     ctx_lo=504, ctx_hi=504, n_new=8, group_size=128, kappa_k=0.99, kappa_v=0.99,
+                     s_sink=16, s_keep=128, s_flush=8, key_dist="fixed_outlier", outlier_scale=20.0,
+                     fixed_outlier_channels=(3, 77))
+QWEN3_8B_32K = Workload(name="qwen3-8b-ctx32k-b1", seed=2, batch=1, n_q_heads=32, n_kv_heads=8,
+                        ctx_lo=32760, ctx_hi=32760, n_new=8, group_size=128, kappa_k=0.99, kappa_v=0.99)
+QWEN3_4B_B64 = Workload(name="qwen3-4b-b64-ctx4k-8k", seed=3, batch=64, n_q_heads=32, n_kv_heads=8,
+                        ctx_lo=4096, ctx_hi=8192, n_new=1, group_size=64, kappa_k=0.995, kappa_v=0.995)
+QWEN3_32B_128K = Workload(name="qwen3-32b-ctx128k-b4-oscar", seed=4, batch=4, n_q_heads=64, n_kv_heads=8,
+                          ctx_lo=131072, ctx_hi=131072, n_new=1, group_size=32, kappa_k=1.0, kappa_v=1.0,
+                          key_l2norm=True, s_sink=0, s_keep=0, s_flush=128, transform="hadamard",
+                          value_transform="identity", key_dist="lognormal_norm")
+WUSH_CHUNK_B16 = Workload(name="wush-qwen3-8b-b16-chunk2048-on-16k", seed=5, batch=16, n_q_heads=32,
+                          n_kv_heads=8, ctx_lo=16384, ctx_hi=16384, n_new=2048, group_size=128,
+                          kappa_k=0.99, kappa_v=0.99, transform="invertible", value_transform="identity",
+                          chunk_queries=True)
+WORKLOADS: dict[int, Workload] = {1: TINY_GQA4, 2: QWEN3_8B_32K, 3: QWEN3_4B_B64, 4: QWEN3_32B_128K,
+                                  5: WUSH_CHUNK_B16}
 
 
 # ---- transforms handed over by offline calibration -----------------------------

@@ -46,37 +46,37 @@ def _check_units(run, units):
 
 
 def test_config1_full():
-    w = synth.CONFIGS[1]
+    w = synth.TINY_GQA4
     run = harness.GpuRun(w)
     _check_units(run, [(0, 0)])
 
 
 def test_config2_full():
-    w = synth.CONFIGS[2]
+    w = synth.QWEN3_8B_32K
     run = harness.GpuRun(w)
     _check_units(run, [(0, h) for h in range(w.n_kv_heads)])
 
 
 def test_config3_sampled():
-    w = synth.CONFIGS[3]
+    w = synth.QWEN3_4B_B64
     run = harness.GpuRun(w)
     _check_units(run, harness.units_sample(w, 10, seed=3))
 
 
 def test_config4_sampled():
-    w = synth.CONFIGS[4]
+    w = synth.QWEN3_32B_128K
     run = harness.GpuRun(w)
     _check_units(run, harness.units_sample(w, 5, seed=4))
 
 
 def test_config5_sampled():
-    w = synth.CONFIGS[5]
+    w = synth.WUSH_CHUNK_B16
     run = harness.GpuRun(w, ring_extra=2048)
     _check_units(run, harness.units_sample(w, 5, seed=5))
 
 
 # ---- edge cases on small shapes -----------------------------------------------------
-BASE = synth.CONFIGS[1]
+BASE = synth.TINY_GQA4
 EDGES = {
     "sink_only": BASE.replace(ctx_lo=5, ctx_hi=5, n_new=3),
     "windows_only": BASE.replace(ctx_lo=100, ctx_hi=100),
@@ -128,7 +128,7 @@ def test_split_count_invariance(splits):
 
 def test_chunk_query_rotation():
     """Prefill-sized query chunk (WUSH-style invertible T): q' rows bit-exact."""
-    w = synth.CONFIGS[5].replace(batch=2, ctx_lo=300, ctx_hi=300, n_new=64)
+    w = synth.WUSH_CHUNK_B16.replace(batch=2, ctx_lo=300, ctx_hi=300, n_new=64)
     import bit_rotated_kv_gb300 as kvq
     dev = torch.device("cuda")
     tr, host = harness.device_transform(w, dev)

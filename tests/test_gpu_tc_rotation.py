@@ -33,7 +33,7 @@ def _rotate_queries(x_bits: np.ndarray, tkit: np.ndarray, n_kv_heads: int) -> np
     """x_bits [n, Hq, d] uint16 -> q' bits from kv_rotate_qk with T_K^{-T} = tkit [Hkv, d, d]."""
     import bit_rotated_kv_gb300 as kvq
     n, hq, d = x_bits.shape
-    w = synth.CONFIGS[1].replace(n_q_heads=hq, n_kv_heads=n_kv_heads, batch=1)
+    w = synth.TINY_GQA4.replace(n_q_heads=hq, n_kv_heads=n_kv_heads, batch=1)
     dev = torch.device("cuda")
     cfg, _ = harness.kv_config(w, [512])
     t = torch.from_numpy(np.ascontiguousarray(tkit, np.float32)).to(dev)
@@ -75,14 +75,14 @@ def _gauss_rows(rng, shape, wide=False):
 @pytest.mark.parametrize("hq,hkv,n", [(32, 8, 650), (8, 8, 2437), (16, 2, 1300), (64, 8, 305)],
                          ids=["gqa4", "gqa1", "gqa8", "gqa8_h64"])
 def test_invertible_queries_bit_exact(hq, hkv, n):
-    w = synth.CONFIGS[5].replace(n_q_heads=hq, n_kv_heads=hkv)
+    w = synth.WUSH_CHUNK_B16.replace(n_q_heads=hq, n_kv_heads=hkv)
     _, tkit, _ = synth.transforms(w)
     rng = np.random.default_rng(hq * 1000 + n)
     _check(_gauss_rows(rng, (n, hq, 128)), tkit, hkv)
 
 
 def test_orthogonal_queries_wide_exponents():
-    w = synth.CONFIGS[2]
+    w = synth.QWEN3_8B_32K
     tk, _, _ = synth.transforms(w)
     rng = np.random.default_rng(7)
     _check(_gauss_rows(rng, (700, 32, 128), wide=True), np.ascontiguousarray(tk), 8)
@@ -92,7 +92,7 @@ def test_subnormal_matrix_entries():
     """Subnormal float32 entries lie far below their row's largest: truncated at 2^-24 of the
     row's units, inside the bound -- still bit-exact.  One row is scaled by 2^-100 (its units
     follow its own exponent)."""
-    w = synth.CONFIGS[5]
+    w = synth.WUSH_CHUNK_B16
     _, tkit, _ = synth.transforms(w)
     tkit = tkit.copy()
     tkit[3, 5, 7] = np.float32(1e-39)
@@ -103,7 +103,7 @@ def test_subnormal_matrix_entries():
 
 
 def test_zero_rows_and_zero_matrix_rows():
-    w = synth.CONFIGS[5]
+    w = synth.WUSH_CHUNK_B16
     _, tkit, _ = synth.transforms(w)
     tkit = tkit.copy()
     tkit[2, 17, :] = 0.0

@@ -33,16 +33,16 @@ def test_flush_schedule_closed_form(s_sink, s_keep, s_flush):
 
 def test_survey_cache_states():
     # config 1: INT2 [16, 384) = 23 pages, BF16 16 + 128
-    w = synth.CONFIGS[1]
+    w = synth.TINY_GQA4
     assert pipeline.s_quant_schedule(w, 504) == (376, 384)
     # config 2: s_quant = 32768 - 264 before, one span of 8 flushed by the step
-    w = synth.CONFIGS[2]
+    w = synth.QWEN3_8B_32K
     assert pipeline.s_quant_schedule(w, 32760) == (32504, 32512)
     # config 5: INT2 [64, 16128) before, +2048 after
-    w = synth.CONFIGS[5]
+    w = synth.WUSH_CHUNK_B16
     assert pipeline.s_quant_schedule(w, 16384) == (16128, 18176)
     # config 4: everything INT2, one new BF16 token
-    w = synth.CONFIGS[4]
+    w = synth.QWEN3_32B_128K
     assert pipeline.s_quant_schedule(w, 131072) == (131072, 131072)
 
 
@@ -81,7 +81,7 @@ def test_attention_special_cases():
 
 
 def test_gqa_one_reduces_to_mha():
-    w = synth.CONFIGS[1].replace(n_q_heads=1, n_kv_heads=1, ctx_lo=40, ctx_hi=40, s_sink=4, s_keep=8)
+    w = synth.TINY_GQA4.replace(n_q_heads=1, n_kv_heads=1, ctx_lo=40, ctx_hi=40, s_sink=4, s_keep=8)
     tk, tkit, tv = synth.transforms(w)
     ui = synth.unit_inputs(w, 0, 0)
     r = pipeline.run_unit(w, ui, tk, tkit, tv)
@@ -93,7 +93,7 @@ def test_gqa_one_reduces_to_mha():
 
 def test_all_bf16_when_context_fits_windows():
     # context <= S_sink + S_keep: nothing is quantized, attention is plain BF16 attention
-    w = synth.CONFIGS[1].replace(ctx_lo=100, ctx_hi=100)
+    w = synth.TINY_GQA4.replace(ctx_lo=100, ctx_hi=100)
     tk, tkit, tv = synth.transforms(w)
     ui = synth.unit_inputs(w, 0, 0)
     r = pipeline.run_unit(w, ui, tk, tkit, tv)
@@ -108,7 +108,7 @@ def test_config1_end_to_end_shapes_and_accuracy():
     """Config 1 through the oracle.  The accuracy of INT2 attention against
     unquantized attention is reported, not pinned (the pages' accuracy claims
     need trained models)."""
-    w = synth.CONFIGS[1]
+    w = synth.TINY_GQA4
     tk, tkit, tv = synth.transforms(w)
     ui = synth.unit_inputs(w, 0, 0)
     r = pipeline.run_unit(w, ui, tk, tkit, tv)

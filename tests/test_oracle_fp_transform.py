@@ -139,7 +139,7 @@ def test_rotate_identity_is_exact():
 
 
 def test_generator_transforms_inverse_transpose():
-    w = synth.CONFIGS[5]
+    w = synth.WUSH_CHUNK_B16
     tk, tkit, tv = synth.transforms(w)
     for h in range(2):
         e = tk[h].astype(np.float64).T @ tkit[h].astype(np.float64) - np.eye(128)

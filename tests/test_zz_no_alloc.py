@@ -24,8 +24,8 @@ def _rel(out: torch.Tensor, ref: torch.Tensor) -> float:
 
 
 @pytest.mark.parametrize("w", [
-    synth.CONFIGS[1],
-    synth.CONFIGS[1].replace(n_q_heads=16, n_kv_heads=2, batch=2, ctx_lo=300, ctx_hi=640, group_size=64),
+    synth.TINY_GQA4,
+    synth.TINY_GQA4.replace(n_q_heads=16, n_kv_heads=2, batch=2, ctx_lo=300, ctx_hi=640, group_size=64),
 ], ids=["config1", "gqa8_b2_g64"])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(w):
     import bit_rotated_kv_gb300 as kvq
