@@ -508,10 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
         last = n;
       }
       if (abort_sh && last >= 0) {
-        set_status(P.status, KVQ_ERR_TIMEOUT);
-        uint32_t fl = 0;      // the last committed chunk must finish before TMEM is released
-        for (long long it = 0; it < kSpinLimit && !um_mbar_try(&bar_mma[last & 1], (uint32_t)((last >> 1) & 1)); ++it)
-          fl++;
+        // the last committed chunk must finish before TMEM is released (bounded)
+        for (long long it = 0; it < kSpinLimit; ++it)
+          if (um_mbar_try(&bar_mma[last & 1], (uint32_t)((last >> 1) & 1))) break;
       }
     }
   } else {
@@ -594,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (tid == 0 && abort_sh) set_status(P.status, KVQ_ERR_TIMEOUT);   // whichever warp gave up
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tb), "r"(kTmemCols) : "memory");
 }
