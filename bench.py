@@ -331,7 +331,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "e2e": {"value": round(world * nbytes["total"] / (t_e2e * 1e-3) / 1e9, 2), "unit": UNIT,
                 "ms_per_step": round(t_e2e, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "kernel_ms": kernel_ms,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": args.steps * step_launches(w, int(q.shape[0]), int(k_new.shape[0]), run.cfg.ring_cap),
         "clocks": sampler.summary(),
         "device_status": status,
     }
@@ -355,6 +355,30 @@ def synth_sq(w, ctx: int) -> int:
     while L - s >= w.s_keep + w.s_flush:
         s += w.s_flush
     return s
+
+
+# ---- launches per step ---------------------------------------------------------------------
+# kv_rotate_qk's dispatch (include/kvq.h): from this many dense (row, head) pairs on, the dense
+# rows run on the tensor cores and the exact copies / Hadamard rows in a second launch
+TC_MIN_PAIRS = 128 * 152
+
+
+def rotate_launches(w, n_q_rows: int, n_kv_rows: int) -> int:
+    """Kernel launches of one kv_rotate_qk call (the library's dispatch rule)."""
+    had = w.transform == "hadamard"
+    q_pairs, kv_pairs = n_q_rows * w.n_q_heads, n_kv_rows * w.n_kv_heads
+    dense = (0 if had else q_pairs + kv_pairs) + (kv_pairs if w.value_transform != "identity" else 0)
+    items = (q_pairs + kv_pairs if had else 0) + (kv_pairs if w.value_transform == "identity" else 0)
+    if dense < TC_MIN_PAIRS:
+        return 1 if dense + items > 0 else 0
+    return 2 if items > 0 else 1
+
+
+def step_launches(w, n_q_rows: int, n_kv_rows: int, ring_cap: int) -> int:
+    """Kernel launches of one bench step: rotate, flush (when it may quantize anything), decode."""
+    max_tokens = min(w.n_new + w.s_flush, ring_cap - w.s_keep)
+    flush = 1 if (max_tokens // w.s_flush) * w.s_flush > 0 else 0
+    return rotate_launches(w, n_q_rows, n_kv_rows) + flush + 1
 
 
 # ---- CPU baseline: the oracle as it stands on a bounded sample -----------------------------
