@@ -7,7 +7,13 @@ is built once (untimed); before every timed step the cache's seq_len / s_quant a
 to the pre-step state and L2 is flushed by a 512 MB memset (both untimed), so every step
 does identical work from HBM.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C | --configs C1,C2,..]
+                  [--impl reference]
+
+The headline is the 128K-context workload (qwen3-32b-ctx128k-b4-oscar); the 32K, batched
+and chunk-append workloads are measured in the same run and reported as "sub_configs"
+(each with its roofline, end-to-end figure and oracle baseline; the chunk workload also
+times its K/V chunk rotate+quantize and its chunk query rotation on their own).
 
 Prints one JSON line (rank 0).  Multi-GPU runs are independent replicas, one per rank
 (weak scaling): the decode units (sequence, kv head) need no exchange.
@@ -36,7 +42,8 @@ import synth  # noqa: E402
 
 METRIC = "INT2 paged decode attention: effective HBM GB/s (% of ~8 TB/s), tokens/s"
 UNIT = "GB/s"
-DEFAULT_CONFIG = 2
+DEFAULT_CONFIG = 4                 # the largest single-GPU workload (128K context)
+SUB_CONFIGS = "2,3,5"              # measured in the same run, reported as sub-records
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -174,14 +181,28 @@ class ClockSampler:
 
 
 # ---- the GPU arm ----------------------------------------------------------------------------
-def run_ours(args, rank: int, world: int, local_rank: int):
+def _timed_avg(fn, steps: int, stream, reset=None):
+    """Average ms of fn() over `steps` runs, CUDA events on `stream` around each run."""
     import torch
-    import bit_rotated_kv_gb300 as kvq
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        if reset is not None:
+            reset()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
+def measure_config(args, w: synth.Workload, rank: int, world: int, local_rank: int, headline: bool):
+    """One workload: the step timed as a user runs it, per-kernel times, end to end through the
+    C ABI from pinned host buffers, and (chunk workloads) the chunk rotate+quantize and the
+    chunk query rotation timed on their own."""
+    import torch
     from tests import harness
 
     dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    w = workload(args)
     # the realistic ring capacity (S_keep + S_flush + n_new): window splits are sized by it
     run = harness.GpuRun(w, device=dev, do_step=False, ring_extra=0, attn_splits=args.splits)
     r = run.runner
@@ -216,7 +237,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         step()
     torch.cuda.synchronize()
     if int(r.status.item()) != 0:
-        raise RuntimeError(f"device status {int(r.status.item())}")
+        raise RuntimeError(f"{w.name}: device status {int(r.status.item())}")
 
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -235,7 +256,7 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     ev_s, ev_e = mk(), mk()
     barrier(world)
     torch.cuda.synchronize()
-    with nvtx_range("timed_steps"):          # lets a profiler select exactly these launches
+    with nvtx_range("timed_steps" if headline else "timed_steps_" + w.name):
         for i in range(args.steps):
             reset()
             ev_s[i].record(stream)
@@ -263,9 +284,9 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     status = int(r.status.item())
 
     # ---- end to end through the C ABI with host buffers: H2D of the step's inputs from
-    # pinned memory, the three calls, D2H of the attention output, every step
-    # the step's inputs packed into one pinned host buffer (256-byte aligned segments), so the
-    # upload is a single copy
+    # pinned memory, the three calls, D2H of the attention output, every step.  The step's
+    # inputs are packed into one pinned host buffer (256-byte aligned segments), so the
+    # upload is a single copy.
     parts = [x.contiguous() for x in (k_new, v_new, sidx, pos, q)]
     offs, nb = [], 0
     for x in parts:
@@ -310,14 +331,12 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     achieved = nbytes["decode"] / (t_dec * 1e-3) / 1e9
     value = world * nbytes["total"] / (t_step_max * 1e-3) / 1e9
     res = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(t_step_max, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int2 codes x f16 tensor-core MMA, f32 accumulate",
-        "data": "synthetic (seeded; shapes of the pages' Qwen3 workloads, random transforms)",
+        "value": round(value, 2), "ms_per_step": round(t_step_max, 5),
         "config": {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
                    "head_dim": w.head_dim, "context": int(ctx.max()) + w.n_new, "n_new_tokens": w.n_new,
                    "group_size": w.group_size, "kappa": [w.kappa_k, w.kappa_v],
                    "windows_sink_keep_flush": [w.s_sink, w.s_keep, w.s_flush], "transform": w.transform,
+                   "key_l2norm": bool(w.key_l2norm),
                    "l2": "flushed between timed steps (512 MB memset, untimed)",
                    "bytes_per_step": nbytes, "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * w.batch / (t_step_max * 1e-3), 1),
@@ -335,12 +354,109 @@ def run_ours(args, rank: int, world: int, local_rank: int):
         "clocks": sampler.summary(),
         "device_status": status,
     }
+    if w.chunk_queries:
+        res["chunk"] = measure_chunk(args, w, run, k_new, v_new, sidx, pos, reset, stream, peak)
+    del run, r, flush_buf, d_buf
+    torch.cuda.empty_cache()
     return res
 
 
-def workload(args) -> synth.Workload:
+def chunk_bytes(w: synth.Workload) -> dict:
+    """Algorithmic bytes of a chunk append: the K/V rotate + quantize (the fused minimum: each
+    appended row read once, the quantized tokens written as INT2 and the rest as BF16 ring
+    rows, the ring rows pushed out of the window read once), and the chunk query rotation."""
+    d, hkv, B, n = w.head_dim, w.n_kv_heads, w.batch, w.n_new
+    ng = d // w.group_size
+    int2 = d // 4 + 4 * ng + (2 if w.key_l2norm else 0)      # one K or V row
+    ctx = int(w.ctx_lo)
+    sq0 = synth_sq(w.replace(n_new=0), ctx)
+    sq1 = synth_sq(w, ctx)
+    n_q = sq1 - sq0                                          # tokens quantized by the step
+    from_ring = max(0, min(n_q, ctx - sq0))                  # of them, rows already in the ring
+    from_new = n_q - from_ring
+    stay = n - from_new                                      # appended rows that stay BF16
+    per_tensor = (n * d * 2 + from_ring * d * 2 + n_q * int2 + stay * d * 2)
+    mats = hkv * d * d * 4 * (1 if w.transform != "hadamard" else 0)
+    kv = B * hkv * 2 * per_tensor + mats
+    qrows = B * n * w.n_q_heads
+    q = 2 * qrows * d * 2 + mats
+    return {"kv_rotate_quantize": int(kv), "query_rotation": int(q), "query_rows": int(qrows),
+            "kv_rows": int(B * n * hkv), "quantized_tokens_per_seq": int(n_q)}
+
+
+def measure_chunk(args, w, run, k_new, v_new, sidx, pos, reset, stream, peak):
+    """Chunk append of a prefill-sized step, timed on its own: (a) the new keys / values
+    rotated on the tensor cores and quantized by the flush (two calls), (b) the chunk's
+    queries (n_new x Hq rows per sequence) compensated with T_K^{-T}."""
+    import torch
+    r = run.runner
+    cb = chunk_bytes(w)
+
+    def kv():
+        r.append(k_new, v_new, sidx, pos)
+        r.flush(w.n_new + w.s_flush)
+    for _ in range(args.warmup):
+        reset()
+        kv()
+    t_kv = _timed_avg(kv, args.steps, stream, reset)
+    # the chunk queries, [B * n_new, Hq, d] (sequence-major, then token)
+    g = w.gqa
+    qc = np.zeros((w.batch, w.n_new, w.n_q_heads, w.head_dim), np.uint16)
+    for b in range(w.batch):
+        for h in range(w.n_kv_heads):
+            qc[b, :, h * g:(h + 1) * g] = synth.chunk_query_rows(w, b, h)
+    qd = torch.from_numpy(qc.reshape(-1, w.n_q_heads, w.head_dim).view(np.int16)).to(r.device).view(torch.bfloat16)
+    del qc
+    qo = torch.empty_like(qd)
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=r.device)
+    qrun = lambda: r.append(None, None, None, None, qd, qo)
+    for _ in range(args.warmup):
+        qrun()
+    t_q = _timed_avg(qrun, args.steps, stream, lambda: flush_buf.zero_())
+    if int(r.status.item()) != 0:
+        raise RuntimeError(f"{w.name}: device status {int(r.status.item())} after the chunk timings")
+    flops_q = 2.0 * w.head_dim * w.head_dim * cb["query_rows"]
+    flops_kv = 2.0 * w.head_dim * w.head_dim * cb["kv_rows"] * (1 if w.transform != "hadamard" else 0)
+    out = {
+        "kv_rotate_quantize": {"calls": "kv_rotate_qk (keys, values) + kv_quant_flush", "ms": round(t_kv, 5),
+                               "bytes": cb["kv_rotate_quantize"],
+                               "achieved_gbs": round(cb["kv_rotate_quantize"] / (t_kv * 1e-3) / 1e9, 2),
+                               "frac_of_peak": round(cb["kv_rotate_quantize"] / (t_kv * 1e-3) / 1e9 / peak, 4),
+                               "key_tflops": round(flops_kv / (t_kv * 1e-3) / 1e12, 2),
+                               "bytes_basis": "fused minimum (each new row read once, INT2 / BF16 written once)",
+                               "quantized_tokens_per_seq": cb["quantized_tokens_per_seq"]},
+        "query_rotation": {"calls": "kv_rotate_qk (queries only)", "rows": cb["query_rows"], "ms": round(t_q, 5),
+                           "bytes": cb["query_rotation"],
+                           "achieved_gbs": round(cb["query_rotation"] / (t_q * 1e-3) / 1e9, 2),
+                           "frac_of_peak": round(cb["query_rotation"] / (t_q * 1e-3) / 1e9 / peak, 4),
+                           "tflops": round(flops_q / (t_q * 1e-3) / 1e12, 2)},
+    }
+    del qd, qo, flush_buf
+    return out
+
+
+def run_ours(args, rank: int, world: int, local_rank: int):
+    import torch
+    torch.cuda.set_device(torch.device("cuda", local_rank))
+    configs = [int(c) for c in str(args.configs).split(",") if c.strip()] if args.configs else [args.config]
+    head = measure_config(args, workload(args, configs[0]), rank, world, local_rank, True)
+    res = {"metric": METRIC, "value": head.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "int2 codes x f16 tensor-core MMA, f32 accumulate",
+           "data": "synthetic (seeded; shapes of the pages' Qwen3 workloads, random transforms)"}
+    res.update(head)
+    subs = {}
+    for c in configs[1:]:
+        sub = measure_config(args, workload(args, c), rank, world, local_rank, False)
+        subs[sub["config"]["workload"]] = sub
+    if subs:
+        res["sub_configs"] = subs
+    return res
+
+
+def workload(args, config: int | None = None) -> synth.Workload:
     """The configuration, optionally shrunk (--batch) for a profiler capture of the same kernel."""
-    w = synth.WORKLOADS[args.config]
+    w = synth.WORKLOADS[args.config if config is None else config]
     if args.batch:
         w = w.replace(batch=args.batch)
     return w
@@ -400,7 +516,10 @@ def oracle_step_sample(config: int, budget_s: float) -> dict:
     done = 0
     spent = 0.0
     i = 0
-    while spent < budget_s and i < 100000:
+    # the untimed cache build of each sampled unit costs several times its timed step, so the
+    # sample also stops after 3 x budget_s of wall time
+    wall_end = time.time() + 3.0 * budget_s
+    while spent < budget_s and i < 100000 and (done == 0 or time.time() < wall_end):
         b, h = units[i % len(units)]
         i += 1
         ui = synth.unit_inputs(w, b, h, lengths)
@@ -502,7 +621,11 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, help="headline workload (synth.WORKLOADS)")
+    ap.add_argument("--configs", default=None,
+                    help="comma list: headline first, the rest as sub-records (default: headline + "
+                         f"{SUB_CONFIGS} when --config is the default, else the headline alone)")
+    ap.add_argument("--sub-cpu-budget", type=float, default=5.0, help="oracle seconds per sub-record")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -512,6 +635,10 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
+    if args.configs is None:
+        args.configs = (f"{args.config}," + SUB_CONFIGS) if (args.config == DEFAULT_CONFIG and not args.batch) \
+            else str(args.config)
+    args.config = int(args.configs.split(",")[0])
     rank, world, local = init_dist()
     if args.impl == "reference":
         if rank == 0:
@@ -528,6 +655,9 @@ def main(argv=None):
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             res["cpu_baseline"] = cpu_baseline(args.config, args.cpu_budget)
+            for name, sub in res.get("sub_configs", {}).items():
+                cid = next(k for k, v in synth.WORKLOADS.items() if v.name == name)
+                sub["cpu_baseline"] = cpu_baseline(cid, args.sub_cpu_budget)
         print(json.dumps(res), flush=True)
 
 

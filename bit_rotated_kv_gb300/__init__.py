@@ -135,11 +135,21 @@ class KVConfig:
     kappa_v: float = 0.99
     quest_alpha: float = 1.4935705
 
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        if name != "_cc":                    # any change rebuilds the C struct on next use
+            object.__setattr__(self, "_cc", None)
+
     def c(self) -> CConfig:
-        return CConfig(self.head_dim, self.n_q_heads, self.n_kv_heads, self.page_size, self.group_size,
-                       self.quantizer, int(bool(self.key_l2norm)), self.s_sink, self.s_keep, self.s_flush,
-                       self.ring_cap, self.batch, self.max_pages_per_seq, self.num_pages, self.attn_splits,
-                       0, float(self.kappa_k), float(self.kappa_v), float(self.quest_alpha))
+        """The C struct (built once, rebuilt only after a field changes)."""
+        cc = self.__dict__.get("_cc")
+        if cc is None:
+            cc = CConfig(self.head_dim, self.n_q_heads, self.n_kv_heads, self.page_size, self.group_size,
+                         self.quantizer, int(bool(self.key_l2norm)), self.s_sink, self.s_keep, self.s_flush,
+                         self.ring_cap, self.batch, self.max_pages_per_seq, self.num_pages, self.attn_splits,
+                         0, float(self.kappa_k), float(self.kappa_v), float(self.quest_alpha))
+            object.__setattr__(self, "_cc", cc)
+        return cc
 
     @property
     def gqa(self) -> int:
@@ -192,12 +202,21 @@ class KVCache:
         self.ring_k = torch.zeros((B, H, cfg.ring_cap, d), dtype=torch.bfloat16, device=dev)
         self.ring_v = torch.zeros((B, H, cfg.ring_cap, d), dtype=torch.bfloat16, device=dev)
         self.counters = torch.zeros(B, dtype=torch.int32, device=dev)
-        self._c = None
+
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        if name != "_cc":                    # a replaced buffer rebuilds the C struct on next use
+            object.__setattr__(self, "_cc", None)
 
     def c(self) -> CCache:
-        return CCache(_ptr(self.pages), _ptr(self.page_table), _ptr(self.seq_len), _ptr(self.s_quant),
-                      _ptr(self.sink_k), _ptr(self.sink_v), _ptr(self.ring_k), _ptr(self.ring_v),
-                      _ptr(self.counters))
+        """The C struct of device pointers (built once, rebuilt only after a buffer is replaced)."""
+        cc = self.__dict__.get("_cc")
+        if cc is None:
+            cc = CCache(_ptr(self.pages), _ptr(self.page_table), _ptr(self.seq_len), _ptr(self.s_quant),
+                        _ptr(self.sink_k), _ptr(self.sink_v), _ptr(self.ring_k), _ptr(self.ring_v),
+                        _ptr(self.counters))
+            object.__setattr__(self, "_cc", cc)
+        return cc
 
 
 @dataclass
@@ -208,8 +227,18 @@ class Transform:
     t_k_inv_t: torch.Tensor | None = None
     t_v: torch.Tensor | None = None
 
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        if name != "_cc":
+            object.__setattr__(self, "_cc", None)
+
     def c(self) -> CTransform:
-        return CTransform(self.kind, 0, _ptr(self.t_k), _ptr(self.t_k_inv_t), _ptr(self.t_v))
+        """The C struct (built once, rebuilt only after a field changes)."""
+        cc = self.__dict__.get("_cc")
+        if cc is None:
+            cc = CTransform(self.kind, 0, _ptr(self.t_k), _ptr(self.t_k_inv_t), _ptr(self.t_v))
+            object.__setattr__(self, "_cc", cc)
+        return cc
 
 
 def kv_rotate_qk(cfg: KVConfig, tr: Transform, q, q_out, k, v, seq_idx, pos, cache: KVCache,

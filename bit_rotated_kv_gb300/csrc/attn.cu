@@ -969,8 +969,9 @@ using namespace kvq;
 // S_flush tokens).
 // INT2 pages per sequence a call with contexts up to max_ctx can touch.
 static int kvq_attn_pages(const kvq_config* cfg, int32_t max_ctx) {
-  const int p = max(0, (max_ctx - cfg->s_sink + kPage - 1) / kPage);
-  return min(p, cfg->max_pages_per_seq);
+  // 64-bit: max_ctx may be anything up to INT32_MAX
+  const long long p = max(0LL, ((long long)max_ctx - cfg->s_sink + kPage - 1) / kPage);
+  return (int)min(p, (long long)cfg->max_pages_per_seq);
 }
 
 extern "C" void kvq_attn_splits(const kvq_config* cfg, int32_t max_ctx, int* n_int2, int* n_win) {
@@ -1105,13 +1106,15 @@ extern "C" int kvq_launch_attn_noalloc(const kvq_config* cfg, const kvq_cache* c
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!addr[dev]) {
+      // set-up, once per device: the array's device address, and the ticket counters zeroed
+      // once -- every completed call leaves the tickets it took at zero again, so later calls
+      // need no clearing (and keep their overlap with the previous kernel on the stream)
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr) return KVQ_ERR_CUDA;
+      if (cudaMemsetAsync(p, 0, (size_t)KVQ_NOALLOC_WORKSPACE_BYTES, stream) != cudaSuccess) return KVQ_ERR_CUDA;
       addr[dev] = p;
     }
     ws = addr[dev];
   }
-  // the ticket counters at the head of the workspace must start at zero on every call
-  if (cudaMemsetAsync(ws, 0, kvq_attn_counter_bytes(cfg, max_ctx), stream) != cudaSuccess) return KVQ_ERR_CUDA;
   return kvq_launch_attn(cfg, cache, q_rot, out, sm_scale, max_ctx, ws, d_status, stream);
 }

@@ -29,12 +29,18 @@ def _rows_for(k_all: torch.Tensor, lengths_lo, lengths_hi):
 
 
 class DecodeRunner:
-    """Owns one cache plus the scratch of a decode step."""
+    """Owns one cache plus the scratch of a decode step.
 
-    def __init__(self, cfg: KVConfig, transform: Transform, max_ctx: int, device="cuda"):
+    Calls go to ``stream`` (default: the current stream of ``device`` when the runner is
+    made, resolved once); a method's own ``stream`` argument overrides it for that call."""
+
+    def __init__(self, cfg: KVConfig, transform: Transform, max_ctx: int, device="cuda", stream=None):
         self.cfg = cfg
         self.tr = transform
         self.device = torch.device(device)
+        if stream is None:
+            stream = torch.cuda.current_stream(self.device)
+        self.stream = int(getattr(stream, "cuda_stream", stream))
         self.cache = KVCache(cfg, device)
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.max_ctx = int(max_ctx)
@@ -49,14 +55,15 @@ class DecodeRunner:
         self.cache.page_table.copy_(torch.from_numpy(np.ascontiguousarray(table, np.int32)))
 
     def append(self, k_rows, v_rows, seq_idx, pos, q=None, q_out=None, stream=None) -> None:
-        kv_rotate_qk(self.cfg, self.tr, q, q_out, k_rows, v_rows, seq_idx, pos, self.cache, self.status, stream)
+        kv_rotate_qk(self.cfg, self.tr, q, q_out, k_rows, v_rows, seq_idx, pos, self.cache, self.status,
+                     self.stream if stream is None else stream)
 
     def flush(self, max_tokens: int, stream=None) -> None:
-        kv_quant_flush(self.cfg, self.cache, max_tokens, self.status, stream)
+        kv_quant_flush(self.cfg, self.cache, max_tokens, self.status, self.stream if stream is None else stream)
 
     def decode(self, q_rot, out, stream=None) -> None:
         kv_attn_decode(self.cfg, self.cache, q_rot, out, self.sm_scale, self.max_ctx, self.ws, self.status,
-                       stream)
+                       self.stream if stream is None else stream)
 
     def prefill(self, k_all: torch.Tensor, v_all: torch.Tensor, lengths, chunk: int) -> None:
         """Append tokens [0, lengths[b]) of k_all / v_all [B, T, Hkv, d] (bf16, device) in chunks,

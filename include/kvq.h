@@ -250,12 +250,17 @@ KVQ_API int kv_attn_decode(const kvq_config* cfg, const kvq_cache* cache, const 
  * device memory inside the library, held by every GPU that loads the library until the
  * process exits.  Arguments, results and errors are those of kv_attn_decode, except:
  *   - KVQ_ERR_WORKSPACE when kv_attn_workspace_bytes(cfg, max_ctx) exceeds the fixed size;
- *   - the first call on a device looks up the array's device address (set-up, once per
- *     device, while that device is current), so make that first call before any stream
- *     capture;
- *   - every call shares the one array: it clears the ticket counters it needs (an async
- *     memset on `stream`), and calls whose work overlaps on the GPU (other streams, other
- *     threads) race on it and give wrong results -- serialize them.
+ *   - the first call on a device does a set-up, once per device, while that device is
+ *     current: it looks up the array's device address and zero-fills the array (an async
+ *     memset on `stream`), so make that first call before any stream capture; later calls
+ *     add nothing to the stream but the decode kernel (each completed call leaves the ticket
+ *     counters at the array's head zero again, as kv_attn_decode does for its workspace);
+ *   - the address is kept for the life of the process: do not use this entry point after a
+ *     cudaDeviceReset (or any other teardown of the device's primary context) in the same
+ *     process, because the kept address no longer names device memory then;
+ *   - every call shares the one array, which keeps the last call's contents; calls whose
+ *     work overlaps on the GPU (other streams, other threads) race on it and give wrong
+ *     results -- serialize them.
  * This entry point has no counterpart on the pages; it only changes where the scratch of
  * kv_attn_decode lives. */
 #define KVQ_NOALLOC_WORKSPACE_BYTES (8u << 20)
