@@ -10,11 +10,14 @@
 // 128x128 float32 matrix times a bf16 vector; every output must be the correctly rounded
 // bf16 of the exact value -- the flush quantizes these rows, so they must not depend on
 // summation order.  The fp32 FMA sum plus a rigorous error bound decides the rounding for
-// almost every output; the rest are recomputed in double-float (error-free products and
-// sums).  The matrices stay L2-resident across decode steps.
+// almost every output; the rest go to exact.cuh (double-float with its own bound, then, only
+// within that bound of a midpoint, an exact fixed-point sum).  The matrices stay L2-resident
+// across decode steps.
 // The Hadamard transform is a warp-wide butterfly (two in-thread stages, five shuffle
-// stages) in double-float, then one scaling by 1/sqrt(d).
+// stages) in double-float with an error bound, then one scaling by 1/sqrt(d); outputs the
+// bound leaves undecided are recomputed exactly (exact.cuh).
 #include "rotate.cuh"
+#include "exact.cuh"
 
 namespace kvq {
 
@@ -28,7 +31,7 @@ namespace kvq {
 // (chains, combining sums and the final v), |v - y| <= u A for y = sum_j T_ij x_j (plus at most
 // 2^-142 from underflow; the fp32 evaluation of A is covered by a factor 1 + 2^-16).  bf16(v)
 // is then the correctly rounded result unless a rounding midpoint lies within that distance;
-// those few outputs are recomputed exactly (double-float) by a warp each after the tile.
+// those few outputs are recomputed by a warp each after the tile (exact_dot_bf16_warp).
 // Loads are issued in the order that overlaps them: the destination's sequence index and
 // position, the matrix, the rows, and only then the dependent s_quant check.
 constexpr int kMaxRT = 16;
@@ -126,18 +129,8 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
       const int r = fallback[f] >> 7, o = fallback[f] & 127;
       const float4 t4 = reinterpret_cast<const float4*>(T.mat + ((size_t)mh * kHeadDim + o) * kHeadDim)[lane];
       const float4 x4 = reinterpret_cast<const float4*>(xs[r])[lane];
-      float hi = 0.f, lo = 0.f;
-      ff_mac(hi, lo, t4.x, x4.x);
-      ff_mac(hi, lo, t4.y, x4.y);
-      ff_mac(hi, lo, t4.z, x4.z);
-      ff_mac(hi, lo, t4.w, x4.w);
-#pragma unroll
-      for (int s2 = 16; s2 > 0; s2 >>= 1) {
-        const float oh = __shfl_xor_sync(0xffffffffu, hi, s2);
-        const float ol = __shfl_xor_sync(0xffffffffu, lo, s2);
-        ff_add(hi, lo, oh, ol, hi, lo);
-      }
-      if (lane == 0) dst_sh[r][o] = ff_to_bf16(hi, lo);
+      const uint32_t res = exact_dot_bf16_warp(t4, x4, lane);
+      if (lane == 0) dst_sh[r][o] = (uint16_t)res;
     }
     __syncthreads();                                    // xs, dst_sh and the list are reused
   }
@@ -197,49 +190,71 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   pdl_wait();                           // (the caller's inputs above: see dense_tile)
   uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
   if (dst == nullptr) return;
-  float hi[4], lo[4];
+  // S = H x in double-float (hi, lo) with a bound bd on |S - (hi + lo)| (every butterfly is a
+  // sum or difference of two such values, ffb_add)
+  float hi[4], lo[4], bd[4];
   hi[0] = __uint_as_float(raw.x << 16);
   hi[1] = __uint_as_float(raw.x & 0xffff0000u);
   hi[2] = __uint_as_float(raw.y << 16);
   hi[3] = __uint_as_float(raw.y & 0xffff0000u);
 #pragma unroll
-  for (int m = 0; m < 4; ++m) lo[m] = 0.f;
+  for (int m = 0; m < 4; ++m) lo[m] = bd[m] = 0.f;
   // in-thread stages: stride 1 then stride 2
 #pragma unroll
   for (int st = 1; st <= 2; st <<= 1) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       if (m & st) continue;
-      float ah = hi[m], al = lo[m], bh = hi[m + st], bl = lo[m + st];
-      ff_add(ah, al, bh, bl, hi[m], lo[m]);
-      ff_add(ah, al, -bh, -bl, hi[m + st], lo[m + st]);
+      const float ah = hi[m], al = lo[m], ab = bd[m], bh = hi[m + st], bl = lo[m + st], bb = bd[m + st];
+      ffb_add(ah, al, ab, bh, bl, bb, hi[m], lo[m], bd[m]);
+      ffb_add(ah, al, ab, -bh, -bl, bb, hi[m + st], lo[m + st], bd[m + st]);
     }
   }
   // cross-lane stages: element stride 4 .. 64 = lane stride 1 .. 16
 #pragma unroll
   for (int ls = 1; ls < 32; ls <<= 1) {
-    bool upper = (lane & ls) != 0;
+    const bool upper = (lane & ls) != 0;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      float ph = __shfl_xor_sync(0xffffffffu, hi[m], ls);
-      float pl = __shfl_xor_sync(0xffffffffu, lo[m], ls);
-      if (upper) ff_add(ph, pl, -hi[m], -lo[m], hi[m], lo[m]);   // a - b, b is mine
-      else       ff_add(hi[m], lo[m], ph, pl, hi[m], lo[m]);     // a + b, a is mine
+      const float ph = __shfl_xor_sync(0xffffffffu, hi[m], ls);
+      const float pl = __shfl_xor_sync(0xffffffffu, lo[m], ls);
+      const float pb = __shfl_xor_sync(0xffffffffu, bd[m], ls);
+      if (upper) ffb_add(ph, pl, pb, -hi[m], -lo[m], bd[m], hi[m], lo[m], bd[m]);   // a - b, b is mine
+      else       ffb_add(hi[m], lo[m], bd[m], ph, pl, pb, hi[m], lo[m], bd[m]);     // a + b, a is mine
     }
   }
-  // scale by 1/sqrt(128) held as a double-float constant
+  // y = S / sqrt(128) = S (ch + cl) + S eps, |eps| <= 2^-48 / sqrt(128): the product in
+  // double-float with every rounding bounded, then the bf16 decision (exact.cuh); outputs it
+  // leaves undecided are recomputed exactly from the row
   const double c = 0.088388347648318440550;  // 1/sqrt(128)
   const float ch = (float)c;
   const float cl = (float)(c - (double)ch);
   uint16_t o[4];
+  uint32_t undecided = 0u;
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    float p = __fmul_rn(hi[m], ch);
-    float e = __fmaf_rn(hi[m], ch, -p);
-    e = __fadd_rn(e, __fadd_rn(__fmul_rn(hi[m], cl), __fmul_rn(lo[m], ch)));
-    o[m] = ff_to_bf16(p, e);
-    if (o[m] == 0x8000u) o[m] = 0;                       // an exact zero is +0
+    const float p = __fmul_rn(hi[m], ch);
+    const float e0 = __fmaf_rn(hi[m], ch, -p);
+    const float e1 = __fmul_rn(hi[m], cl), e2 = __fmul_rn(lo[m], ch);
+    const float e3 = __fadd_rn(e1, e2);
+    const float e4 = __fadd_rn(e0, e3);
+    float yh, yl;
+    two_sum(p, e4, yh, yl);
+    const float by = bd[m] * 0.08838835f + (fabsf(hi[m]) + fabsf(lo[m])) * 0x1p-51f + fabsf(lo[m] * cl) +
+                     kU * (fabsf(e1) + fabsf(e2) + fabsf(e3) + fabsf(e4));
+    int r;
+    if (hi[m] == 0.f && lo[m] == 0.f && bd[m] == 0.f) r = 0;             // S exactly zero: +0
+    else r = ffb_decide(yh, yl, by);
+    if (r < 0) {
+      undecided |= 1u << m;
+      r = ff_to_bf16(yh, yl);                                           // the exact path's start
+    }
+    o[m] = (uint16_t)r;
   }
+  // exact recomputation, one output at a time by its lane (rare: within the bound of a midpoint)
+#pragma unroll 1
+  for (int m = 0; m < 4; ++m)
+    if (undecided & (1u << m)) o[m] = (uint16_t)exact_wht_output(src, 4 * lane + m, o[m]);
   uint2 outv;
   outv.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
   outv.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
@@ -280,7 +295,7 @@ __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
 
 // Warp items only (exact copies, Hadamard rows): the launch that accompanies the tensor-core
 // kernel.  Without the dense path's register footprint it runs at full occupancy.
-__global__ void __launch_bounds__(256) rotate_items_kernel(const RotParams Pk) {
+__global__ void __launch_bounds__(256, 4) rotate_items_kernel(const RotParams Pk) {
   pdl_trigger();
   __shared__ RotParams Ps;
   if (threadIdx.x == 0) Ps = Pk;

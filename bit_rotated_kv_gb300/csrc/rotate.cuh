@@ -3,6 +3,7 @@
 #pragma once
 #include "common.cuh"
 #include "launch.h"
+#include "exact.cuh"
 
 namespace kvq {
 
@@ -87,24 +88,16 @@ __device__ __forceinline__ int bf16_if_decided(float v, float e) {
 }
 
 // Exact recomputation of output o of a bf16 row x (128 values, 8-byte aligned, shared or
-// global memory) against T row o (float32, global): double-float products and sums over one
-// warp; lane 0 stores the correctly rounded bf16 result to dst[o].
+// global memory) against T row o (float32, global), over one warp (exact.cuh); lane 0
+// stores the correctly rounded bf16 result to dst[o].
 __device__ __forceinline__ void exact_output_warp(const float* trow, const uint16_t* xrow, uint16_t* dst, int o,
                                                   int lane) {
   const float4 t4 = reinterpret_cast<const float4*>(trow)[lane];
   const uint2 xr = reinterpret_cast<const uint2*>(xrow)[lane];
-  float hi = 0.f, lo = 0.f;
-  ff_mac(hi, lo, t4.x, __uint_as_float(xr.x << 16));
-  ff_mac(hi, lo, t4.y, __uint_as_float(xr.x & 0xffff0000u));
-  ff_mac(hi, lo, t4.z, __uint_as_float(xr.y << 16));
-  ff_mac(hi, lo, t4.w, __uint_as_float(xr.y & 0xffff0000u));
-#pragma unroll
-  for (int s2 = 16; s2 > 0; s2 >>= 1) {
-    const float oh = __shfl_xor_sync(0xffffffffu, hi, s2);
-    const float ol = __shfl_xor_sync(0xffffffffu, lo, s2);
-    ff_add(hi, lo, oh, ol, hi, lo);
-  }
-  if (lane == 0) dst[o] = ff_to_bf16(hi, lo);
+  const float4 x4 = make_float4(__uint_as_float(xr.x << 16), __uint_as_float(xr.x & 0xffff0000u),
+                                __uint_as_float(xr.y << 16), __uint_as_float(xr.y & 0xffff0000u));
+  const uint32_t r = exact_dot_bf16_warp(t4, x4, lane);
+  if (lane == 0) dst[o] = (uint16_t)r;
 }
 
 // Dense (row, head) pairs from which a call runs its dense tensors on the tensor cores
