@@ -9,20 +9,25 @@
 // one kv head); decode attention softmax(q K^T / sqrt(d)) V.
 //
 // Design (GB300, sm_103a):
-//  * grid (splits, kv_head, sequence); splits [0, n_int2) stream INT2 pages, the rest
-//    the BF16 windows.  Every warp owns a private ring of STAGES page slots in shared
+//  * grid (kv_head, sequence, splits); splits [0, n_int2) stream INT2 pages, the rest
+//    the BF16 windows.  Every warp owns a private ring of kStages page slots in shared
 //    memory filled by 1-D TMA bulk copies (cp.async.bulk + mbarrier complete_tx); lane
 //    0 issues, all lanes wait with a bounded try_wait loop.  No cluster, no multicast.
 //  * one page (16 tokens) is one m16n8k16 tile: scores S[token][head] = codes x q',
-//    all g <= 8 query heads of the kv head share the read (N = 8 columns).
+//    all g <= 8 query heads of the kv head share the read (N = 8 columns).  A warp takes
+//    its pages two at a time: both pages' scores, one softmax maximum test for both, both
+//    P V products -- the loop, the waits and the maximum bookkeeping are shared and the two
+//    pages' instructions interleave.
 //  * 2-bit codes become fp16 tensor-core operands with one AND each: a code c at bit
 //    position 2s of a 16-bit half is the fp16 subnormal c * 4^s * 2^-24, exact; the
-//    4^s and 2^-24 factors are folded into q' (keys) or the output rows (values).  The
-//    group scale / zero point and the l2 norm are applied to the fp32 scores:
-//    s = norm * sum_g Delta_g (q'.c_g - z_g sum(q'_g)).
+//    4^s and 2^-24 factors are folded into q' (keys) or the output rows (values).  Scores
+//    s = norm * mult_h * sum_g Delta_g (q'.c_g - z_g qsum_g): the group terms by FFMA from
+//    the MMA accumulators, the zero-point term sum_g (Delta z)_g qsum_g by one more MMA
+//    (Delta z and qsum as exact fp16 hi + lo pairs).
 //  * P V: the fp32 probabilities times Delta_v become the B operand through
 //    movmatrix (C-fragment -> B-fragment transpose); the zero point is a per-group
-//    correction sum_t W_t z_t.
+//    correction sum_t W_t z_t by MMA, whose row 8 (all ones) also sums P' -- the softmax
+//    denominator from the same fp16 weights as the numerator.
 //  * BF16 windows use bf16 MMA for q'.k (exact inputs) and two bf16 MMAs (hi + lo
 //    split of P) for P V.
 //  * the last CTA of each (sequence, kv head) merges the split partials (atomic ticket,
@@ -37,6 +42,7 @@ namespace kvq {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int kCtasPerSm = 2;               // resident CTAs per SM the launch shape aims at
 constexpr int kStages = 4;
 constexpr long long kWaitLimit = 1LL << 22;
 constexpr int kRow = 4 + kHeadDim;      // one (m, l, -, -, o[d]) record; o 16-byte aligned
@@ -205,7 +211,6 @@ __device__ __forceinline__ void softmax_step(Softmax& sm, float (&s)[4], float (
 // ---- shared memory layout ---------------------------------------------------------------
 struct __align__(16) QShared {
   float mult[kMaxGqa];        // 2^(24 - sigma_h)
-  float qsum[kMaxGqa][4];     // sum of q' over each group
 };
 
 // Per-warp result in canonical order: for each head (m, l, o[d]); warps `wstride` floats apart.
@@ -228,11 +233,56 @@ __device__ __forceinline__ void load_scales(const uint8_t* p, uint32_t (&o)[NG])
   }
 }
 
+// explicit shared-memory loads (addresses in the shared window; the immediate offsets fold
+// into the instruction)
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+template <int NG>
+__device__ __forceinline__ void lds_scales(uint32_t a, uint32_t (&o)[NG]) {
+  if constexpr (NG == 1) {
+    o[0] = lds32(a);
+  } else if constexpr (NG == 2) {
+    const uint2 v = lds64(a);
+    o[0] = v.x; o[1] = v.y;
+  } else {
+    const uint4 v = lds128(a);
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  }
+}
+
+// (Delta z) of one token and group as the fp16 A operand of the key zero-point MMA: (hi, hi)
+// for even quads (k = 4g, 4g + 1), (lo, 0) for odd ones (k = 4g + 2, 4g + 3), where
+// hi = fp16(Delta16 z16) and lo = Delta16 z16 - hi exactly (fused).
+__device__ __forceinline__ uint32_t dz_operand(uint32_t dz, bool odd) {
+  const uint32_t zd = __byte_perm(dz, 0u, 0x1032);       // (z, Delta)
+  const uint32_t hi = hmul2_bits(dz, zd);                  // (Delta z, z Delta), both rounded alike
+  const uint32_t lo = hfma2_neg_bits(dz, zd, hi);          // exact remainders
+  return odd ? (lo & 0xffffu) : hi;
+}
+
 template <int NG, bool L2>
 __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int split, float* res,
                            size_t wstride) {
-  // accumulators per group; with fewer than 4 groups the k-steps alternate between two
-  // accumulators so that consecutive MMAs do not wait on each other
+  // accumulators per group; with one group the k-steps alternate between two accumulators so
+  // that consecutive MMAs do not wait on each other
   constexpr int NS = NG == 1 ? 2 : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = P.gqa;
@@ -268,18 +318,20 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   int* my_pid = slot_pid + warp * kStages;
   if (lane < kStages) mbar_init(my_bars + lane, 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const uint8_t* const page_base = P.pages + (size_t)h * pb;
+  const int page_stride = P.hkv * pb;
+  const int num_pages = P.num_pages;
   // copy page k of this warp into its slot (lane 0 only); an entry that is not a page id
   // completes the slot without data and is reported when (if) the page is consumed
-  auto issue = [&](int k, int pid) {
-    const int slot = k % kStages;
-    if (pid < 0 || pid >= P.num_pages) {
+  auto refill = [&](int k, int pid) {
+    const int slot = k & (kStages - 1);
+    if ((unsigned)pid >= (unsigned)num_pages) {
       my_pid[slot] = -1;
       mbar_arrive(my_bars + slot);
     } else {
       my_pid[slot] = pid;
       mbar_arrive_tx(my_bars + slot, (uint32_t)pb);
-      tma_load_1d(my_ring + (size_t)slot * pb, P.pages + ((size_t)pid * P.hkv + h) * pb, (uint32_t)pb,
-                  my_bars + slot);
+      tma_load_1d(my_ring + slot * pb, page_base + (size_t)pid * page_stride, (uint32_t)pb, my_bars + slot);
     }
   };
   __syncwarp();
@@ -290,7 +342,7 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
 #pragma unroll
   for (int k = 0; k < kStages; ++k) {
     const int pid = __shfl_sync(0xffffffffu, pid_a, k);
-    if (lane == 0 && k < n_first) issue(k, pid);
+    if (lane == 0 && k < n_first) refill(k, pid);
   }
   const int Lraw = P.seq_len[b];
   const int sqraw = P.s_quant[b];
@@ -305,9 +357,11 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   const int nk = first < pend ? (pend - first + kWarps - 1) / kWarps : 0;
 
   // ---- queries (their loads fly while the first pages are copied): B fragments scaled into
-  // fp16 range, per-head multipliers and group sums
+  // fp16 range (head lane/4: q' 2^(sigma - 2 slot), sigma per head), per-head multipliers, and
+  // the B operand of the key zero-point MMA: group sums of q' 2^(sigma - 24) as fp16 hi + lo
   const uint16_t* qb = P.q + ((size_t)b * P.hkv * g + (size_t)h * g) * kHeadDim;
   const int hrow = lane >> 2, quad = lane & 3;
+  const bool qodd = (quad & 1) != 0;
   uint32_t qraw[8][2];
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
@@ -316,6 +370,7 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     qraw[s][1] = (hrow < g) ? *reinterpret_cast<const uint32_t*>(src + 8) : 0u;
   }
   uint32_t bq[8][2];
+  uint32_t bz0 = 0u, bz1 = 0u;            // B fragment of the zero-point MMA (k = 2 quad .., + 8 ..)
   {
     float qv[8][4];
     float amax = 0.f;
@@ -340,6 +395,10 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
       bq[s][0] = pack_half2(qv[s][0] * f, qv[s][1] * f);
       bq[s][1] = pack_half2(qv[s][2] * f, qv[s][3] * f);
     }
+    // group sums in units 2^(sigma - 5) (|qsum| 2^(sigma - 5) < 2^14: hi and lo normal fp16); the
+    // product lands in acc units after an exact scaling by 2^-19
+    const float fz = ldexpf(1.0f, sigma - 5);
+    float qsg[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
       float acc = 0.f;
@@ -348,37 +407,27 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
         if ((16 * s) / (kHeadDim / NG) == gi) acc += qv[s][0] + qv[s][1] + qv[s][2] + qv[s][3];
       acc += __shfl_xor_sync(0xffffffffu, acc, 1);
       acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (warp == 0 && quad == 0) qs->qsum[hrow][gi] = acc;
+      qsg[gi] = acc * fz;
+    }
+    // zero-point MMA, group q = quad (q < NG): k = 2q, 2q + 1 carry (hi, lo) of (Delta z) against
+    // the group sum's hi part twice; k = 8 + 2q carries hi against the sum's lo part
+    {
+      const float v = quad == 0 ? qsg[0] : quad == 1 ? qsg[1] : quad == 2 ? qsg[2] : qsg[3];
+      const __half hh = __float2half_rn(quad < NG ? v : 0.f);
+      const __half hl = __float2half_rn(quad < NG ? v - __half2float(hh) : 0.f);
+      __half2 r0 = __halves2half2(hh, hh), r1 = __halves2half2(hl, __float2half_rn(0.f));
+      bz0 = *reinterpret_cast<uint32_t*>(&r0);
+      bz1 = *reinterpret_cast<uint32_t*>(&r1);
     }
     if (warp == 0 && quad == 0) qs->mult[hrow] = ldexpf(1.0f, 24 - sigma);
   }
   __syncthreads();
 
   const int hA = 2 * quad, hB = 2 * quad + 1;
-  // Loop constants in registers: the parameter block lives in shared memory and would be
-  // re-read after every barrier operation.  Scores are
-  //   s = x_t (mult_h sum_g Delta_g acc_g - sum_g Delta_g z_g qsum_g),
-  // x_t = scale_log2 * norm_t with key norms, else scale_log2 folded into mult and qsum here.
+  // scores s = x_t mult_h (sum_g Delta_g acc_g - C), C the zero-point MMA in acc units;
+  // x_t = scale_log2 * norm_t with key norms, else scale_log2 folded into mult here
   const float xs = P.scale_log2;
-  const float fx = L2 ? 1.f : xs;
-  const float multA = qs->mult[hA] * fx, multB = qs->mult[hB] * fx;
-  float qsA[NG], qsB[NG];
-#pragma unroll
-  for (int gi = 0; gi < NG; ++gi) { qsA[gi] = qs->qsum[hA][gi] * fx; qsB[gi] = qs->qsum[hB][gi] * fx; }
-  const int num_pages = P.num_pages;
-  const uint8_t* const page_base = P.pages + (size_t)h * pb;
-  const int page_stride = P.hkv * pb;
-  auto refill = [&](int kk, int pid) {     // lane 0 only: page kk of this warp into its slot
-    const int slot = kk & (kStages - 1);
-    if ((unsigned)pid >= (unsigned)num_pages) {
-      my_pid[slot] = -1;
-      mbar_arrive(my_bars + slot);
-    } else {
-      my_pid[slot] = pid;
-      mbar_arrive_tx(my_bars + slot, (uint32_t)pb);
-      tma_load_1d(my_ring + slot * pb, page_base + (size_t)pid * page_stride, (uint32_t)pb, my_bars + slot);
-    }
-  };
+  const float multA = qs->mult[hA] * xs, multB = qs->mult[hB] * xs;
 
   // Online softmax with a lazy reference maximum m: probabilities are p = exp2(s - m), with m
   // moved only when a score exceeds it by more than 8, so p <= 2^8.  The loop keeps
@@ -392,123 +441,155 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
     for (int c = 0; c < 4; ++c) o[mt][c] = 0.f;
-  // zero-point correction sum_t W_g z_g: row g (group) of one m16n8 accumulator, columns = heads
+  // value zero-point correction sum_t W_g z_g: row g (group) of one m16n8 accumulator
   float corr[4] = {0.f, 0.f, 0.f, 0.f};
 
   const int tA = lane >> 2, tB = tA + 8;
-  const int off_kw = 16 * lane, off_vw = kCodeBytes + 16 * lane;
-  const int off_skA = k_scale_off() + tA * NG * 4, off_skB = k_scale_off() + tB * NG * 4;
-  const int off_dv0 = v_delta_off(NG, 2 * quad, 0), off_dv1 = v_delta_off(NG, 2 * quad + 8, 0);
-  const int off_zp0 = v_zero_off(NG, 2 * quad, hrow < NG ? hrow : 0);
-  const int off_zp1 = v_zero_off(NG, 2 * quad + 8, hrow < NG ? hrow : 0);
-  const int off_gd0 = v_delta_off(NG, 2 * quad, hrow < NG ? hrow : 0);
-  const int off_gd1 = v_delta_off(NG, 2 * quad + 8, hrow < NG ? hrow : 0);
+  // per-lane offsets inside a page (all loads of a page are base + these)
+  const uint32_t off_code = 16u * lane;
+  const uint32_t off_sk = (uint32_t)(k_scale_off() + tA * NG * 4);
+  const uint32_t off_dv = (uint32_t)v_delta_off(NG, 2 * quad, 0);
+  const uint32_t off_zg = (uint32_t)v_delta_off(NG, 2 * quad, hrow < NG ? hrow : 0);
+  const uint32_t off_nrm = (uint32_t)(norm_off(NG) + 2 * tA);
+  const uint32_t ring_s = smem_u32(my_ring);
 
-  // One page: scores, softmax, P V.  MASKED pages (the sequence's last, partial page, or an
-  // entry that is not a page id) keep only their first valid_tok tokens.
-  auto page = [&](const uint8_t* pg, int valid_tok, auto masked) {
-    constexpr bool MASKED = decltype(masked)::value;
-    const uint4 wk = *reinterpret_cast<const uint4*>(pg + off_kw);
+  // ---- one page, split in three parts so that two pages can share the softmax bookkeeping and
+  // the loop overhead: scores (kside), lazy maximum (softmax), P V (vside)
+  auto kside = [&](uint32_t sa, float (&sc)[4]) {
+    const uint4 wk = lds128(sa + off_code);
     uint32_t skA[NG], skB[NG];
-    load_scales<NG>(pg + off_skA, skA);
-    load_scales<NG>(pg + off_skB, skB);
-    float xA = 1.f, xB = 1.f;
-    if constexpr (L2) {
-      const __half* nrm = reinterpret_cast<const __half*>(pg + norm_off(NG));
-      xA = xs * __half2float(nrm[tA]);
-      xB = xs * __half2float(nrm[tB]);
+    lds_scales<NG>(sa + off_sk, skA);
+    lds_scales<NG>(sa + off_sk + 32 * NG, skB);
+    // ---- key zero points: C = sum_g (Delta z)_g qsum_g, one MMA; this lane carries group quad
+    float cz[4];
+    {
+      uint32_t a[4] = {0u, 0u, 0u, 0u};
+      if (quad < NG) {
+        const uint32_t wA = lds32(sa + off_sk + 4 * quad), wB = lds32(sa + off_sk + 32 * NG + 4 * quad);
+        const uint32_t zA = __byte_perm(wA, 0u, 0x1032), zB = __byte_perm(wB, 0u, 0x1032);   // (z, Delta)
+        const uint32_t hA2 = hmul2_bits(wA, zA), hB2 = hmul2_bits(wB, zB);   // (Delta z, Delta z) rounded
+        const uint32_t lA2 = hfma2_neg_bits(wA, zA, hA2), lB2 = hfma2_neg_bits(wB, zB, hB2);   // exact rests
+        a[0] = __byte_perm(hA2, lA2, 0x5410);          // (hi, lo)
+        a[1] = __byte_perm(hB2, lB2, 0x5410);
+        a[2] = hA2 & 0xffffu;                          // (hi, 0)
+        a[3] = hB2 & 0xffffu;
+      }
+      mma_f16_z(cz, a, bz0, bz1);
     }
-    // ---- scores: codes x q' per group
+    // ---- codes x q' per group, combined with Delta as they complete (the zero-point product
+    // enters in acc units: an exact scaling by 2^-19)
     const uint32_t kw[4] = {wk.x, wk.y, wk.z, wk.w};
     const uint32_t kw10[4] = {wk.x >> 10, wk.y >> 10, wk.z >> 10, wk.w >> 10};
-    float acc[NG][NS][4];
+    float sum[4] = {cz[0] * -0x1p-19f, cz[1] * -0x1p-19f, cz[2] * -0x1p-19f, cz[3] * -0x1p-19f};
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      uint32_t a[4];
+    for (int gi = 0; gi < NG; ++gi) {
+      float acc[NS][4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) a[r] = code_pair(kw[r], kw10[r], s);
-      const int gi = (16 * s) / (kHeadDim / NG), u = s % NS;
-      const int first_of = gi * (8 / NG) + u;            // first k-step feeding acc[gi][u]
-      if (s == first_of) mma_f16_z(acc[gi][u], a, bq[s][0], bq[s][1]);
-      else mma_f16(acc[gi][u], a, bq[s][0], bq[s][1]);
-    }
-    float sc[4];
-    {
-      float sA0 = 0.f, sA1 = 0.f, sB0 = 0.f, sB1 = 0.f, cA0 = 0.f, cA1 = 0.f, cB0 = 0.f, cB1 = 0.f;
+      for (int ss = 0; ss < 8 / NG; ++ss) {
+        const int s = gi * (8 / NG) + ss, u = ss % NS;
+        uint32_t a[4];
 #pragma unroll
-      for (int gi = 0; gi < NG; ++gi) {
-        float a0 = acc[gi][0][0], a1 = acc[gi][0][1], a2 = acc[gi][0][2], a3 = acc[gi][0][3];
-        if constexpr (NS == 2) {
-          a0 += acc[gi][1][0]; a1 += acc[gi][1][1]; a2 += acc[gi][1][2]; a3 += acc[gi][1][3];
-        }
-        const float2 dzA = unpack_half2(skA[gi]), dzB = unpack_half2(skB[gi]);
-        const float pzA = dzA.x * dzA.y, pzB = dzB.x * dzB.y;      // exact: 11 x 11 bits
-        sA0 = fmaf(dzA.x, a0, sA0); sA1 = fmaf(dzA.x, a1, sA1);
-        sB0 = fmaf(dzB.x, a2, sB0); sB1 = fmaf(dzB.x, a3, sB1);
-        cA0 = fmaf(pzA, qsA[gi], cA0); cA1 = fmaf(pzA, qsB[gi], cA1);
-        cB0 = fmaf(pzB, qsA[gi], cB0); cB1 = fmaf(pzB, qsB[gi], cB1);
+        for (int r = 0; r < 4; ++r) a[r] = code_pair(kw[r], kw10[r], s);
+        if (ss < NS) mma_f16_z(acc[u], a, bq[s][0], bq[s][1]);
+        else mma_f16(acc[u], a, bq[s][0], bq[s][1]);
       }
-      sc[0] = fmaf(sA0, multA, -cA0);
-      sc[1] = fmaf(sA1, multB, -cA1);
-      sc[2] = fmaf(sB0, multA, -cB0);
-      sc[3] = fmaf(sB1, multB, -cB1);
-      if constexpr (L2) {
-        sc[0] *= xA; sc[1] *= xA; sc[2] *= xB; sc[3] *= xB;
-      }
-      if constexpr (MASKED) {
-        if (tA >= valid_tok) sc[0] = sc[1] = -INFINITY;
-        if (tB >= valid_tok) sc[2] = sc[3] = -INFINITY;
+      const float dA = __low2float(*reinterpret_cast<const __half2*>(&skA[gi]));
+      const float dB = __low2float(*reinterpret_cast<const __half2*>(&skB[gi]));
+#pragma unroll
+      for (int u = 0; u < NS; ++u) {
+        sum[0] = fmaf(dA, acc[u][0], sum[0]);
+        sum[1] = fmaf(dA, acc[u][1], sum[1]);
+        sum[2] = fmaf(dB, acc[u][2], sum[2]);
+        sum[3] = fmaf(dB, acc[u][3], sum[3]);
       }
     }
-    float p[4];
-    {
-      const bool up = (fmaxf(sc[0], sc[2]) > mb[0]) || (fmaxf(sc[1], sc[3]) > mb[1]);
-      if (__any_sync(0xffffffffu, up)) {
+    if constexpr (L2) {
+      const float nA = __half2float(__ushort_as_half((unsigned short)lds16(sa + off_nrm)));
+      const float nB = __half2float(__ushort_as_half((unsigned short)lds16(sa + off_nrm + 16)));
+      sc[0] = sum[0] * (multA * nA);                   // multA, multB carry scale_log2 here
+      sc[1] = sum[1] * (multB * nA);
+      sc[2] = sum[2] * (multA * nB);
+      sc[3] = sum[3] * (multB * nB);
+    } else {
+      sc[0] = sum[0] * multA;
+      sc[1] = sum[1] * multB;
+      sc[2] = sum[2] * multA;
+      sc[3] = sum[3] * multB;
+    }
+  };
+  // the reference moves (rarely): scale everything accumulated so far by alpha (heads hA, hB)
+  auto rescale = [&](float aA, float aB) {
+    const float2 al = make_float2(aA, aB);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          float mx = fmaxf(sc[c], sc[c + 2]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          // the new reference: the running maximum (never below the old reference)
-          const float nb = fmaxf(mb[c], mx + 8.f);
-          const float alpha = ex2_approx(mb[c] - nb);
-          mb[c] = nb;
-          p[c] = ex2_approx(sc[c] - nb);
-          p[c + 2] = ex2_approx(sc[c + 2] - nb);
-          lsum[c] = fmaf(lsum[c], alpha, p[c] + p[c + 2]);
+    for (int mt = 0; mt < 8; ++mt) {
+      float2 v0 = __fmul2_rn(make_float2(o[mt][0], o[mt][1]), al);
+      float2 v1 = __fmul2_rn(make_float2(o[mt][2], o[mt][3]), al);
+      o[mt][0] = v0.x; o[mt][1] = v0.y; o[mt][2] = v1.x; o[mt][3] = v1.y;
+    }
+    const float2 c = __fmul2_rn(make_float2(corr[0], corr[1]), al);
+    corr[0] = c.x; corr[1] = c.y;
+    if constexpr (NG > 1) {
+      const float2 c2 = __fmul2_rn(make_float2(corr[2], corr[3]), al);
+      corr[2] = c2.x; corr[3] = c2.y;
+    }
+    lsum[0] *= aA;
+    lsum[1] *= aB;
+  };
+  // lazy maximum over the scores of NP pages (sc[NP][4]); probabilities p' = exp2(s - mb)
+  auto softmax_n = [&](auto& sc, auto& p, auto np_tag) {
+    constexpr int NP = decltype(np_tag)::value;
+    float mxA = fmaxf(sc[0][0], sc[0][2]), mxB = fmaxf(sc[0][1], sc[0][3]);
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) { o[mt][c] *= alpha; o[mt][c + 2] *= alpha; }
-          corr[c] *= alpha;
-        }
-      } else {
-        p[0] = ex2_approx(sc[0] - mb[0]);
-        p[1] = ex2_approx(sc[1] - mb[1]);
-        p[2] = ex2_approx(sc[2] - mb[0]);
-        p[3] = ex2_approx(sc[3] - mb[1]);
-        lsum[0] += p[0] + p[2];
-        lsum[1] += p[1] + p[3];
+    for (int j = 1; j < NP; ++j) {
+      mxA = fmaxf(mxA, fmaxf(sc[j][0], sc[j][2]));
+      mxB = fmaxf(mxB, fmaxf(sc[j][1], sc[j][3]));
+    }
+    if (__any_sync(0xffffffffu, mxA > mb[0] || mxB > mb[1])) {
+#pragma unroll
+      for (int o2 = 4; o2 < 32; o2 <<= 1) {
+        mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, o2));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, o2));
+      }
+      // the new reference: the running maximum (never below the old reference)
+      const float nA = fmaxf(mb[0], mxA + 8.f), nB = fmaxf(mb[1], mxB + 8.f);
+      rescale(ex2_approx(mb[0] - nA), ex2_approx(mb[1] - nB));
+      mb[0] = nA;
+      mb[1] = nB;
+    }
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      p[j][0] = ex2_approx(sc[j][0] - mb[0]);
+      p[j][1] = ex2_approx(sc[j][1] - mb[1]);
+      p[j][2] = ex2_approx(sc[j][2] - mb[0]);
+      p[j][3] = ex2_approx(sc[j][3] - mb[1]);
+      if constexpr (NG == 1) {           // (NG > 1: the value zero-point MMA sums P')
+        lsum[0] += p[j][0] + p[j][2];
+        lsum[1] += p[j][1] + p[j][3];
       }
     }
-    // ---- P V: per value group, W = P' * Delta_v as the B operand (fp16)
+  };
+  // P V of one page (MASKED: only its first valid_tok tokens)
+  auto vside = [&](uint32_t sa, const float (&p)[4], int valid_tok, auto masked) {
+    constexpr bool MASKED = decltype(masked)::value;
+    const uint4 wv = lds128(sa + kCodeBytes + off_code);
+    uint32_t dv0[NG], dv1[NG];
+    lds_scales<NG>(sa + off_dv, dv0);
+    lds_scales<NG>(sa + off_dv + 16 * NG, dv1);
+    uint32_t zp0 = 0u, zp1 = 0u, gd0 = 0u, gd1 = 0u;   // z_v, Delta_v pairs of group lane/4
+    (void)gd0;
+    (void)gd1;
+    if (hrow < NG) {
+      zp0 = lds32(sa + off_zg + 32 * NG);
+      zp1 = lds32(sa + off_zg + 48 * NG);
+      if constexpr (NG > 1) {
+        gd0 = lds32(sa + off_zg);
+        gd1 = lds32(sa + off_zg + 16 * NG);
+      }
+    }
     // P' in the B-fragment layout (tokens 2q, 2q+1 | 2q+8, 2q+9 of head lane/4), then one
     // HMUL2 per group with the Delta_v pairs of the same tokens
     const uint32_t pb0 = movmatrix_trans(pack_half2(p[0], p[1]));
     const uint32_t pb1 = movmatrix_trans(pack_half2(p[2], p[3]));
-    const uint4 wv = *reinterpret_cast<const uint4*>(pg + off_vw);
-    uint32_t dv0[NG], dv1[NG];
-    load_scales<NG>(pg + off_dv0, dv0);
-    load_scales<NG>(pg + off_dv1, dv1);
-    uint32_t zp0 = 0u, zp1 = 0u;                       // z_v pairs of group lane/4
-    uint32_t gd0 = 0u, gd1 = 0u;                       // Delta_v pairs of group lane/4 (NG > 1)
-    if (hrow < NG) {
-      zp0 = *reinterpret_cast<const uint32_t*>(pg + off_zp0);
-      zp1 = *reinterpret_cast<const uint32_t*>(pg + off_zp1);
-      if constexpr (NG > 1) {
-        gd0 = *reinterpret_cast<const uint32_t*>(pg + off_gd0);
-        gd1 = *reinterpret_cast<const uint32_t*>(pg + off_gd1);
-      }
-    }
     if constexpr (MASKED) {                            // clear the dead tokens' scale data
       const uint32_t m0 = (2 * quad < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 1 < valid_tok ? 0xffff0000u : 0u);
       const uint32_t m1 = (2 * quad + 8 < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 9 < valid_tok ? 0xffff0000u : 0u);
@@ -532,7 +613,9 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
       // an fp16 hi + lo pair (the product is 22 bits; the lo part is exact by the fused HFMA2)
       const uint32_t hi0 = hmul2_bits(zp0, gd0), hi1 = hmul2_bits(zp1, gd1);
       const uint32_t lo0 = hfma2_neg_bits(zp0, gd0, hi0), lo1 = hfma2_neg_bits(zp1, gd1, hi1);
-      const uint32_t ah[4] = {hi0, 0u, hi1, 0u}, al[4] = {lo0, 0u, lo1, 0u};
+      // row 8: ones -- C[8][h] = sum_t P'_t (the softmax denominator, from the same fp16 P')
+      const uint32_t ones = lane < 4 ? 0x3C003C00u : 0u;
+      const uint32_t ah[4] = {hi0, ones, hi1, ones}, al[4] = {lo0, 0u, lo1, 0u};
       mma_f16(corr, ah, pb0, pb1);
       mma_f16(corr, al, pb0, pb1);
     }
@@ -547,41 +630,90 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
       mma_f16(o[mt], a, bw[gi][0], bw[gi][1]);
     }
   };
+  // one page on its own (partial pages, bad entries, an odd last page)
+  auto page1 = [&](uint32_t sa, int valid_tok, auto masked) {
+    constexpr bool MASKED = decltype(masked)::value;
+    float sc[1][4], p[1][4];
+    kside(sa, sc[0]);
+    if constexpr (MASKED) {
+      if (tA >= valid_tok) sc[0][0] = sc[0][1] = -INFINITY;
+      if (tB >= valid_tok) sc[0][2] = sc[0][3] = -INFINITY;
+    }
+    softmax_n(sc, p, std::integral_constant<int, 1>{});
+    vside(sa, p[0], valid_tok, masked);
+  };
 
   bool timed_out = false;
   int chunk_a = 0;               // page-table chunk held in pid_a
   int k = 0;
-  for (; k < nk; ++k) {
-    const int slot = k & (kStages - 1);
-    if (!mbar_wait(my_bars + slot, ((unsigned)k / kStages) & 1u)) {
-      timed_out = true;
-      break;
-    }
-    const uint8_t* pg = my_ring + slot * pb;
-    const int pid = my_pid[slot];
-    const int lp = first + k * kWarps;
-    if (pid >= 0 && kPage * (lp + 1) <= n_tok) {
-      page(pg, kPage, std::false_type{});
-    } else {
-      if (pid < 0 && lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
-      page(pg, pid < 0 ? 0 : min(kPage, n_tok - kPage * lp), std::true_type{});
-    }
-    // every lane has consumed this slot: refill it with the page kStages ahead, whose
-    // page-table entry was fetched a chunk earlier
-    const int kk = k + kStages;
+  // every lane has consumed slots: refill them with the pages kStages ahead, whose page-table
+  // entries were fetched a chunk earlier
+  auto refill_from = [&](int kk) {
     if ((kk >> 5) > chunk_a) {
       pid_a = pid_b;
       ++chunk_a;
       pid_b = load_pids(chunk_a + 1);
     }
-    const int pid_next = __shfl_sync(0xffffffffu, pid_a, kk & 31);
+    return __shfl_sync(0xffffffffu, pid_a, kk & 31);
+  };
+  // pages in pairs (two full pages share the loop, the waits and the softmax maximum)
+  for (; k + 1 < nk; k += 2) {
+    const int s0 = k & (kStages - 1), s1 = s0 + 1;          // k even: same phase for both
+    const uint32_t ph = ((unsigned)k / kStages) & 1u;
+    if (!mbar_wait(my_bars + s0, ph) || !mbar_wait(my_bars + s1, ph)) {
+      timed_out = true;
+      break;
+    }
+    const uint32_t sa0 = ring_s + (uint32_t)(s0 * pb), sa1 = sa0 + (uint32_t)pb;
+    const int pid0 = my_pid[s0], pid1 = my_pid[s1];
+    const int lp0 = first + k * kWarps, lp1 = lp0 + kWarps;
+    if (pid0 >= 0 && pid1 >= 0 && kPage * (lp1 + 1) <= n_tok) {
+      float sc[2][4], p[2][4];
+      kside(sa0, sc[0]);
+      kside(sa1, sc[1]);
+      softmax_n(sc, p, std::integral_constant<int, 2>{});
+      vside(sa0, p[0], kPage, std::false_type{});
+      vside(sa1, p[1], kPage, std::false_type{});
+    } else {
+      if ((pid0 < 0 || pid1 < 0) && lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
+      if (pid0 >= 0 && kPage * (lp0 + 1) <= n_tok) page1(sa0, kPage, std::false_type{});
+      else page1(sa0, pid0 < 0 ? 0 : max(0, min(kPage, n_tok - kPage * lp0)), std::true_type{});
+      page1(sa1, pid1 < 0 ? 0 : max(0, min(kPage, n_tok - kPage * lp1)), std::true_type{});
+    }
+    const int kk = k + kStages;
+    const int pn0 = refill_from(kk);
+    const int pn1 = __shfl_sync(0xffffffffu, pid_a, (kk + 1) & 31);
     __syncwarp();
-    if (lane == 0 && kk < nk) refill(kk, pid_next);
+    if (lane == 0) {
+      if (kk < nk) refill(kk, pn0);
+      if (kk + 1 < nk) refill(kk + 1, pn1);
+    }
+  }
+  if (k < nk && !timed_out) {                                 // an odd last page
+    const int slot = k & (kStages - 1);
+    if (!mbar_wait(my_bars + slot, ((unsigned)k / kStages) & 1u)) {
+      timed_out = true;
+    } else {
+      const uint32_t sa = ring_s + (uint32_t)(slot * pb);
+      const int pid = my_pid[slot];
+      const int lp = first + k * kWarps;
+      if (pid >= 0 && kPage * (lp + 1) <= n_tok) {
+        page1(sa, kPage, std::false_type{});
+      } else {
+        if (pid < 0 && lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
+        page1(sa, pid < 0 ? 0 : min(kPage, n_tok - kPage * lp), std::true_type{});
+      }
+      ++k;                                                    // (no refill: nothing follows)
+    }
   }
   // l was accumulated in units of 2^-8 (see above); m is the reference without the bias
   Softmax sm;
   sm.m[0] = mb[0] - 8.f;
   sm.m[1] = mb[1] - 8.f;
+  if constexpr (NG > 1) {               // row 8 of the value zero-point MMA: lanes 0..3
+    lsum[0] = __shfl_sync(0xffffffffu, corr[2], quad);
+    lsum[1] = __shfl_sync(0xffffffffu, corr[3], quad);
+  }
   sm.l[0] = lsum[0] * 256.f;
   sm.l[1] = lsum[1] * 256.f;
   if (timed_out && lane == 0) set_status(P.status, KVQ_ERR_TIMEOUT);
@@ -592,10 +724,12 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
 
   // ---- per-warp result: reduce l over the 8 lanes of a column pair; the zero-point
   // correction of group gi, heads (hA, hB) sits in lane 4 gi + quad
+  if constexpr (NG == 1) {
 #pragma unroll
-  for (int c = 0; c < 2; ++c)
+    for (int c = 0; c < 2; ++c)
 #pragma unroll
-    for (int o2 = 4; o2 < 32; o2 <<= 1) sm.l[c] += __shfl_xor_sync(0xffffffffu, sm.l[c], o2);
+      for (int o2 = 4; o2 < 32; o2 <<= 1) sm.l[c] += __shfl_xor_sync(0xffffffffu, sm.l[c], o2);
+  }
   float zcA[NG], zcB[NG];
 #pragma unroll
   for (int gi = 0; gi < NG; ++gi) {
@@ -791,8 +925,8 @@ __device__ __forceinline__ void merge_warps(const float* src, size_t stride, flo
 // with all loads of a chunk of 8 records in flight: warp w handles head w, lane the channels
 // 4*lane .. 4*lane+3.  TO_OUT: dst[head][j] = o / l; otherwise dst holds merged records.
 __device__ __noinline__ void merge_global(const float* src, int n, int g, float* dst, bool to_out) {
-  const int lane = threadIdx.x & 31, hh = threadIdx.x >> 5;
-  if (hh >= g) return;
+  const int lane = threadIdx.x & 31;
+  for (int hh = threadIdx.x >> 5; hh < g; hh += kWarps) {
   const size_t stride = (size_t)g * kRow;
   const float* s0 = src + (size_t)hh * kRow;
   float M = -INFINITY, L = 0.f;
@@ -836,12 +970,13 @@ __device__ __noinline__ void merge_global(const float* src, int n, int g, float*
     if (lane == 0) { r[0] = M; r[1] = L; }
     reinterpret_cast<float4*>(r + 4)[lane] = O;
   }
+  }
 }
 
 // One kernel per (groups per row, key norms) variant, so that each launch's code is only its own
 // page loop (a short loop per warp is sensitive to instruction-fetch misses).
 template <int NG, bool L2>
-__global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnParams Pk) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const AttnParams Pk) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_trigger();
   // shared-memory copy of the parameters (device functions take references to it)
@@ -904,8 +1039,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
       return;
     }
     // warp hh merges head hh, lane the channels 4*lane .. 4*lane + 3
-    const int lane = threadIdx.x & 31, hh = threadIdx.x >> 5;
-    if (hh >= g) return;
+    const int lane = threadIdx.x & 31;
+    for (int hh = threadIdx.x >> 5; hh < g; hh += kWarps) {
     float M = -INFINITY;
     for (int i = lane; i < P.n_split; i += 32) M = fmaxf(M, buf[((size_t)i * g + hh) * kRow]);
 #pragma unroll
@@ -925,6 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode_kernel(const AttnPara
     const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
     reinterpret_cast<float4*>(P.out + ((size_t)unit * g + hh) * kHeadDim)[lane] =
         make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    }
     return;
   }
   // ---- two-level merge tree over the splits of this (sequence, kv head): the last CTA of
@@ -984,7 +1120,7 @@ extern "C" void kvq_attn_splits(const kvq_config* cfg, int32_t max_ctx, int* n_i
   // p = CTAs per unit for one wave of two CTAs per SM.  When the windows are worth at least
   // half a CTA they get their share of the p; otherwise the INT2 splits take all p slots and
   // one short window split per unit comes on top (it fills a slot as the first CTAs retire).
-  const int p = (int)max(1LL, 2LL * kSms / max(units, 1LL));
+  const int p = (int)max(1LL, (long long)kCtasPerSm * kSms / max(units, 1LL));
   int nw = (int)(p * wbytes / (wbytes + ibytes) + 0.5);
   int ni;
   if (p == 1 || nw == 0) {

@@ -176,37 +176,33 @@ __device__ inline int ffb_decide(float hi, float lo, float B) {
   const float r1 = __fadd_rn(h - m_lo, l);                          // h - m_lo, m_hi - h exact (Sterbenz)
   const float r2 = __fadd_rn(m_hi - h, -l);
   const float Bs = __fmaf_rn(B, 1.0f + 0x1p-16f, 0x1p-140f);
-  const bool ok = __fmaf_rn(-kU, fabsf(r1), r1) > Bs && __fmaf_rn(-kU, fabsf(r2), r2) > Bs;
-  return ok ? (int)(b | (neg ? 0x8000u : 0u)) : -1;
+  // V - m_lo and m_hi - V, each within u |r| + Bs of r1, r2.  h lies in b's cell, |l| is far
+  // below a bf16 step, so V is in b's cell or just across one of its two midpoints (h itself
+  // on a midpoint, l deciding the side).
+  const float s1 = __fmaf_rn(-kU, fabsf(r1), fabsf(r1)), s2 = __fmaf_rn(-kU, fabsf(r2), fabsf(r2));
+  uint32_t res;
+  if (r1 > 0.f && r2 > 0.f && s1 > Bs && s2 > Bs) res = b;            // inside b's cell
+  else if (r1 < 0.f && s1 > Bs) res = b - 1u;                         // below m_lo
+  else if (r2 < 0.f && s2 > Bs) res = b + 1u;                         // above m_hi
+  else return -1;
+  return (int)(res | (neg ? 0x8000u : 0u));
 }
 
 // ---- dense outputs --------------------------------------------------------------------------
-// bf16 bits of the exact sum_j t_j x_j over one warp: lane l holds terms 4l .. 4l + 3 (t float32,
-// x bf16 values held exactly as floats).  Every lane returns the result.
-static __device__ __noinline__ uint32_t exact_dot_bf16_warp(float4 t4, float4 x4, int lane) {
-  float hi = 0.f, lo = 0.f, bnd = 0.f;
-  ffb_mac(hi, lo, bnd, t4.x, x4.x);
-  ffb_mac(hi, lo, bnd, t4.y, x4.y);
-  ffb_mac(hi, lo, bnd, t4.z, x4.z);
-  ffb_mac(hi, lo, bnd, t4.w, x4.w);
-#pragma unroll
-  for (int s2 = 16; s2 > 0; s2 >>= 1) {
-    const float oh = __shfl_xor_sync(0xffffffffu, hi, s2);
-    const float ol = __shfl_xor_sync(0xffffffffu, lo, s2);
-    const float ob = __shfl_xor_sync(0xffffffffu, bnd, s2);
-    ffb_add(hi, lo, bnd, oh, ol, ob, hi, lo, bnd);       // symmetric: every lane gets the same bits
-  }
-  const int d = ffb_decide(hi, lo, bnd);
-  if (d >= 0) return (uint32_t)d;
-  // tier 3: lane 0 sums every term exactly (the terms reach it through shuffles)
+// Tier 3 of a dense output: lane 0 sums every term exactly (the terms reach it through
+// shuffles); every lane returns the bf16 bits.  Out of line: it runs only for outputs within the
+// tier-2 bound of a midpoint.
+static __device__ __noinline__ uint32_t exact_dot_tier3(float4 t4, float4 x4, int lane) {
   BigInt acc;
   if (lane == 0) big_zero(acc);
+#pragma unroll 1
   for (int src = 0; src < 32; ++src) {
     const float tv[4] = {__shfl_sync(0xffffffffu, t4.x, src), __shfl_sync(0xffffffffu, t4.y, src),
                          __shfl_sync(0xffffffffu, t4.z, src), __shfl_sync(0xffffffffu, t4.w, src)};
     const float xv[4] = {__shfl_sync(0xffffffffu, x4.x, src), __shfl_sync(0xffffffffu, x4.y, src),
                          __shfl_sync(0xffffffffu, x4.z, src), __shfl_sync(0xffffffffu, x4.w, src)};
     if (lane == 0) {
+#pragma unroll 1
       for (int k = 0; k < 4; ++k) {
         uint32_t ma, mx;
         int ea, ex;
@@ -224,6 +220,33 @@ static __device__ __noinline__ uint32_t exact_dot_bf16_warp(float4 t4, float4 x4
     r = big_to_bf16(acc, neg);
   }
   return __shfl_sync(0xffffffffu, r, 0);
+}
+
+
+
+// Tier 2 alone: the bf16 bits, or -1 when only tier 3 can decide (same value in every lane).
+__device__ __forceinline__ int exact_dot_tier2(float4 t4, float4 x4) {
+  float hi = 0.f, lo = 0.f, bnd = 0.f;
+  ffb_mac(hi, lo, bnd, t4.x, x4.x);
+  ffb_mac(hi, lo, bnd, t4.y, x4.y);
+  ffb_mac(hi, lo, bnd, t4.z, x4.z);
+  ffb_mac(hi, lo, bnd, t4.w, x4.w);
+#pragma unroll
+  for (int s2 = 16; s2 > 0; s2 >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, hi, s2);
+    const float ol = __shfl_xor_sync(0xffffffffu, lo, s2);
+    const float ob = __shfl_xor_sync(0xffffffffu, bnd, s2);
+    ffb_add(hi, lo, bnd, oh, ol, ob, hi, lo, bnd);       // symmetric: every lane gets the same bits
+  }
+  return ffb_decide(hi, lo, bnd);
+}
+
+// bf16 bits of the exact sum_j t_j x_j over one warp: lane l holds terms 4l .. 4l + 3 (t float32,
+// x bf16 values held exactly as floats).  Every lane returns the result.  Tier 2 inline, tier 3
+// out of line.
+__device__ __forceinline__ uint32_t exact_dot_bf16_warp(float4 t4, float4 x4, int lane) {
+  const int d = exact_dot_tier2(t4, x4);
+  return d >= 0 ? (uint32_t)d : exact_dot_tier3(t4, x4, lane);
 }
 
 // ---- Walsh-Hadamard outputs -----------------------------------------------------------------

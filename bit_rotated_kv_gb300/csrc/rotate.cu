@@ -191,7 +191,12 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
   if (dst == nullptr) return;
   // S = H x in double-float (hi, lo) with a bound bd on |S - (hi + lo)| (every butterfly is a
-  // sum or difference of two such values, ffb_add)
+  // sum or difference of two such values, ffb_add).  When the row's nonzero elements span fewer
+  // than 40 binades every partial sum has at most 48 significant bits and the double-float
+  // butterflies are exact (bd = 0): that path keeps no bound.  (A partial sum of +-x_j is a
+  // multiple of the smallest element's last place, 2^(emin - 7), below 2^(emax + 8): at most
+  // span + 15 <= 46 bits, which hi + lo holds, and each rounding inside a two-sum
+  // addition is then exact.)
   float hi[4], lo[4], bd[4];
   hi[0] = __uint_as_float(raw.x << 16);
   hi[1] = __uint_as_float(raw.x & 0xffff0000u);
@@ -199,6 +204,43 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   hi[3] = __uint_as_float(raw.y & 0xffff0000u);
 #pragma unroll
   for (int m = 0; m < 4; ++m) lo[m] = bd[m] = 0.f;
+  uint32_t emax = 0u, emin = 255u;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t e = (__float_as_uint(hi[m]) >> 23) & 0xffu;
+    if ((__float_as_uint(hi[m]) & 0x7fffffffu) != 0u) {
+      emax = max(emax, max(e, 1u));
+      emin = min(emin, max(e, 1u));
+    }
+  }
+  emax = __reduce_max_sync(0xffffffffu, emax);
+  emin = __reduce_min_sync(0xffffffffu, emin);
+  if (emax < emin + 32u) {
+    // exact butterflies (every partial sum fits hi + lo; the bound part of ffb_add is unused)
+#pragma unroll
+    for (int st = 1; st <= 2; st <<= 1) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        if (m & st) continue;
+        const float ah = hi[m], al = lo[m], bh = hi[m + st], bl = lo[m + st];
+        float unused;
+        ffb_add(ah, al, 0.f, bh, bl, 0.f, hi[m], lo[m], unused);
+        ffb_add(ah, al, 0.f, -bh, -bl, 0.f, hi[m + st], lo[m + st], unused);
+      }
+    }
+#pragma unroll
+    for (int ls = 1; ls < 32; ls <<= 1) {
+      const bool upper = (lane & ls) != 0;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float ph = __shfl_xor_sync(0xffffffffu, hi[m], ls);
+        const float pl = __shfl_xor_sync(0xffffffffu, lo[m], ls);
+        float unused;
+        if (upper) ffb_add(ph, pl, 0.f, -hi[m], -lo[m], 0.f, hi[m], lo[m], unused);
+        else       ffb_add(hi[m], lo[m], 0.f, ph, pl, 0.f, hi[m], lo[m], unused);
+      }
+    }
+  } else {
   // in-thread stages: stride 1 then stride 2
 #pragma unroll
   for (int st = 1; st <= 2; st <<= 1) {
@@ -222,6 +264,7 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
       if (upper) ffb_add(ph, pl, pb, -hi[m], -lo[m], bd[m], hi[m], lo[m], bd[m]);   // a - b, b is mine
       else       ffb_add(hi[m], lo[m], bd[m], ph, pl, pb, hi[m], lo[m], bd[m]);     // a + b, a is mine
     }
+  }
   }
   // y = S / sqrt(128) = S (ch + cl) + S eps, |eps| <= 2^-48 / sqrt(128): the product in
   // double-float with every rounding bounded, then the bf16 decision (exact.cuh); outputs it
@@ -294,8 +337,11 @@ __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
 
 
 // Warp items only (exact copies, Hadamard rows): the launch that accompanies the tensor-core
-// kernel.  Without the dense path's register footprint it runs at full occupancy.
-__global__ void __launch_bounds__(256, 4) rotate_items_kernel(const RotParams Pk) {
+// kernel.  Without the dense path's register footprint it runs at full occupancy; the
+// copies-only instantiation (kWht = false: no Walsh-Hadamard rows in the call) leaves out the
+// Hadamard path's bounds and exact recomputation as well.
+template <bool kWht>
+__global__ void __launch_bounds__(256, kWht ? 4 : 6) rotate_items_kernel(const RotParams Pk) {
   pdl_trigger();
   __shared__ RotParams Ps;
   if (threadIdx.x == 0) Ps = Pk;
@@ -308,7 +354,7 @@ __global__ void __launch_bounds__(256, 4) rotate_items_kernel(const RotParams Pk
   }
   int tt, item;
   find_item(P.n_warp, w, tt, item);
-  if (P.t[tt].mode == ROT_COPY) warp_copies(P, tt, item, threadIdx.x & 31);
+  if (!kWht || P.t[tt].mode == ROT_COPY) warp_copies(P, tt, item, threadIdx.x & 31);
   else warp_item(P, tt, item, threadIdx.x & 31);
 }
 
@@ -368,8 +414,9 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
       W.dense_total = 0;
       W.n_dense[0] = W.n_dense[1] = W.n_dense[2] = 0;
       W.rt = W.rpc = 1;
-      if (launch_pdl(rotate_items_kernel, dim3((unsigned)((P.warp_total + 7) / 8)), dim3(256), 0, stream, W) !=
-          cudaSuccess)
+      const bool wht = P.t[0].mode == ROT_WHT || P.t[1].mode == ROT_WHT || P.t[2].mode == ROT_WHT;
+      if (launch_pdl(wht ? rotate_items_kernel<true> : rotate_items_kernel<false>,
+                     dim3((unsigned)((P.warp_total + 7) / 8)), dim3(256), 0, stream, W) != cudaSuccess)
         return KVQ_ERR_CUDA;
     }
     return launch_rotate_tc(P, stream);

@@ -358,6 +358,8 @@ __device__ __forceinline__ void x_slice(const RotParams& P, const RotTensor& T, 
 }
 
 // The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly; returns 0.
+// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly (exact.cuh);
+// returns 0.
 __device__ __noinline__ int exact_list(const uint16_t* list, int count, const UmRow* mrow, const float* tmat,
                                        int lane) {
   __syncwarp();
