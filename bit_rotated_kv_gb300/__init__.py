@@ -6,7 +6,7 @@ in-tree (``bit_rotated_kv_gb300/_build/libkvq.so``, see ``build_lib.py``); impor
 this module fails loudly when it is missing -- there is no CPU fallback.
 
 Entry points (same names as the C ABI in include/kvq.h):
-  kv_rotate_qk, kv_quant_flush, kv_attn_decode, kv_attn_workspace_bytes,
+  kv_rotate_qk, kv_quant_flush, kv_attn_decode, kv_attn_decode_bf16, kv_attn_workspace_bytes,
   kvq_page_head_bytes, kvq_page_bytes, kvq_status_string
 plus ``KVConfig`` / ``KVCache`` helpers that allocate the caller-owned buffers.
 """
@@ -36,7 +36,8 @@ KVQ_QUANT_QUEST_RMS = 1
 KVQ_TRANSFORM_DENSE = 0
 KVQ_TRANSFORM_HADAMARD = 1
 
-EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_attn_decode", "kv_attn_decode_noalloc", "kv_attn_workspace_bytes",
+EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_attn_decode", "kv_attn_decode_bf16", "kv_attn_decode_noalloc",
+            "kv_attn_workspace_bytes",
             "kvq_page_head_bytes", "kvq_page_bytes", "kvq_status_string", "kvq_version",
             "kvq_selftest_scale_division", "kvq_selftest_tc_integer_sums")
 
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         l.kv_quant_flush.restype = ctypes.c_int
         l.kv_attn_decode.argtypes = [P(CConfig), P(CCache), vp, vp, ctypes.c_float, i32, vp, sz, vp, vp]
         l.kv_attn_decode.restype = ctypes.c_int
+        l.kv_attn_decode_bf16.argtypes = [P(CConfig), P(CCache), vp, vp, ctypes.c_float, i32, vp, sz, vp, vp]
+        l.kv_attn_decode_bf16.restype = ctypes.c_int
         l.kv_attn_decode_noalloc.argtypes = [P(CConfig), P(CCache), vp, vp, ctypes.c_float, i32, vp, vp]
         l.kv_attn_decode_noalloc.restype = ctypes.c_int
         l.kv_attn_workspace_bytes.argtypes = [P(CConfig), i32]
@@ -267,6 +270,16 @@ def kv_attn_decode(cfg: KVConfig, cache: KVCache, q_rot, out, sm_scale: float, m
     rc = lib().kv_attn_decode(ctypes.byref(c), ctypes.byref(cc), _ptr(q_rot), _ptr(out), float(sm_scale),
                               int(max_ctx), _ptr(workspace), nbytes, _ptr(status), _stream(stream))
     _check(rc, "kv_attn_decode")
+
+
+def kv_attn_decode_bf16(cfg: KVConfig, cache: KVCache, q_rot, out, sm_scale: float, max_ctx: int, workspace,
+                        status, stream=None) -> None:
+    """kv_attn_decode with a bf16 output tensor [B, Hq, d] (the float32 result rounded once)."""
+    c, cc = cfg.c(), cache.c()
+    nbytes = int(workspace.numel() * workspace.element_size())
+    rc = lib().kv_attn_decode_bf16(ctypes.byref(c), ctypes.byref(cc), _ptr(q_rot), _ptr(out), float(sm_scale),
+                                   int(max_ctx), _ptr(workspace), nbytes, _ptr(status), _stream(stream))
+    _check(rc, "kv_attn_decode_bf16")
 
 
 NOALLOC_WORKSPACE_BYTES = 8 << 20

@@ -132,7 +132,21 @@ KVQ_API int kv_attn_decode(const kvq_config* cfg, const kvq_cache* cache, const 
   if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
   if (!workspace || !aligned(workspace, 256)) return KVQ_ERR_INVALID_ARG;
   if (ws_bytes < kvq_attn_ws_bytes(cfg, max_ctx)) return KVQ_ERR_WORKSPACE;
-  return kvq_launch_attn(cfg, cache, q_rot, out, sm_scale, max_ctx, workspace, d_status, (cudaStream_t)stream);
+  return kvq_launch_attn(cfg, cache, q_rot, out, 0, sm_scale, max_ctx, workspace, d_status, (cudaStream_t)stream);
+}
+
+KVQ_API int kv_attn_decode_bf16(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, uint16_t* out,
+                                float sm_scale, int32_t max_ctx, void* workspace, size_t ws_bytes, int32_t* d_status,
+                                void* stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  rc = check_cache(cfg, cache);
+  if (rc) return rc;
+  if (!q_rot || !out || !aligned(q_rot, 16) || !aligned(out, 8) || max_ctx < 0) return KVQ_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return KVQ_ERR_INVALID_ARG;
+  if (ws_bytes < kvq_attn_ws_bytes(cfg, max_ctx)) return KVQ_ERR_WORKSPACE;
+  return kvq_launch_attn(cfg, cache, q_rot, out, 1, sm_scale, max_ctx, workspace, d_status, (cudaStream_t)stream);
 }
 
 KVQ_API int kv_attn_decode_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,

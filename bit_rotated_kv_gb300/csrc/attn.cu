@@ -61,7 +61,7 @@ struct AttnParams {
   const uint16_t* ring_k;
   const uint16_t* ring_v;
   const uint16_t* q;
-  float* out;
+  void* out;          // [B][Hq][d] float32, or bf16 when out_bf16
   float* part;        // [B * Hkv][n_split][g][kRow]   per-CTA partials
   float* part2;       // [B * Hkv][n_groups][g][kRow]  merged groups of kGroup splits
   int32_t* count;     // [B * Hkv][n_groups + 1]       tickets of the merge tree
@@ -70,6 +70,7 @@ struct AttnParams {
   int n_int2, n_win, n_split;
   int mp;             // INT2 pages per sequence covered by the splits (host-known bound)
   int merge1;         // 1: the last CTA of a unit merges every split partial from shared memory
+  int out_bf16;       // 1: the output is rounded once to bf16 (nearest-even)
   float scale_log2;   // sm_scale * log2(e)
 };
 
@@ -921,10 +922,22 @@ __device__ __forceinline__ void merge_warps(const float* src, size_t stride, flo
   if (j == 0) { dst[0] = M; dst[1] = Lsum; }
 }
 
+// Output row element j = 4 lane .. 4 lane + 3 of (unit row) `row`: float32, or bf16 rounded once.
+__device__ __forceinline__ void store_out(void* out, bool bf16, size_t row, int lane, float4 v) {
+  if (bf16) {
+    uint2 b;
+    b.x = pack_bf162(v.x, v.y);
+    b.y = pack_bf162(v.z, v.w);
+    reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + row * kHeadDim)[lane] = b;
+  } else {
+    reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + row * kHeadDim)[lane] = v;
+  }
+}
+
 // Merge n records (m, l, o[d]) per head from the workspace (other CTAs' writes: read past L1)
 // with all loads of a chunk of 8 records in flight: warp w handles head w, lane the channels
 // 4*lane .. 4*lane+3.  TO_OUT: dst[head][j] = o / l; otherwise dst holds merged records.
-__device__ __noinline__ void merge_global(const float* src, int n, int g, float* dst, bool to_out) {
+__device__ __noinline__ void merge_global(const float* src, int n, int g, void* dst, bool to_out, bool bf16) {
   const int lane = threadIdx.x & 31;
   for (int hh = threadIdx.x >> 5; hh < g; hh += kWarps) {
   const size_t stride = (size_t)g * kRow;
@@ -963,10 +976,9 @@ __device__ __noinline__ void merge_global(const float* src, int n, int g, float*
   }
   if (to_out) {
     const float inv = (L > 0.f) ? 1.f / L : 0.f;
-    reinterpret_cast<float4*>(dst + (size_t)hh * kHeadDim)[lane] =
-        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    store_out(dst, bf16, (size_t)hh, lane, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
   } else {
-    float* r = dst + (size_t)hh * kRow;
+    float* r = reinterpret_cast<float*>(dst) + (size_t)hh * kRow;
     if (lane == 0) { r[0] = M; r[1] = L; }
     reinterpret_cast<float4*>(r + 4)[lane] = O;
   }
@@ -1058,8 +1070,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const
       }
     }
     const float inv = (Ls > 0.f) ? 1.f / Ls : 0.f;
-    reinterpret_cast<float4*>(P.out + ((size_t)unit * g + hh) * kHeadDim)[lane] =
-        make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv);
+    store_out(P.out, P.out_bf16 != 0, (size_t)unit * g + hh, lane, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
     }
     return;
   }
@@ -1077,13 +1088,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const
   }
   __syncthreads();
   if (!role) return;
-  float* out_unit = P.out + (size_t)unit * g * kHeadDim;
+  void* out_unit = P.out_bf16 ? (void*)(reinterpret_cast<uint16_t*>(P.out) + (size_t)unit * g * kHeadDim)
+                              : (void*)(reinterpret_cast<float*>(P.out) + (size_t)unit * g * kHeadDim);
   const float* gsrc = P.part + ((size_t)unit * P.n_split + (size_t)grp * kGroup) * g * kRow;
   if (n_grp == 1) {
-    merge_global(gsrc, gsize, g, out_unit, true);
+    merge_global(gsrc, gsize, g, out_unit, true, P.out_bf16 != 0);
     return;
   }
-  merge_global(gsrc, gsize, g, P.part2 + ((size_t)unit * n_grp + grp) * g * kRow, false);
+  merge_global(gsrc, gsize, g, P.part2 + ((size_t)unit * n_grp + grp) * g * kRow, false, false);
   __syncthreads();
   if (threadIdx.x == 0) {
     const int t = atomic_add_acq_rel_gpu(cnt + n_grp, 1);
@@ -1092,7 +1104,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const
   }
   __syncthreads();
   if (!role) return;
-  merge_global(P.part2 + (size_t)unit * n_grp * g * kRow, n_grp, g, out_unit, true);
+  merge_global(P.part2 + (size_t)unit * n_grp * g * kRow, n_grp, g, out_unit, true, P.out_bf16 != 0);
 }
 
 }  // namespace kvq
@@ -1156,7 +1168,7 @@ extern "C" size_t kvq_attn_ws_bytes(const kvq_config* cfg, int32_t max_ctx) {
 }
 
 extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
-                               float* out, float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status,
+                               void* out, int out_bf16, float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status,
                                cudaStream_t stream) {
   AttnParams P{};
   P.pages = (const uint8_t*)cache->pages;
@@ -1169,6 +1181,7 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
   P.ring_v = cache->ring_v;
   P.q = q_rot;
   P.out = out;
+  P.out_bf16 = out_bf16 ? 1 : 0;
   P.status = d_status;
   P.batch = cfg->batch;
   P.hkv = cfg->n_kv_heads;
@@ -1252,5 +1265,5 @@ extern "C" int kvq_launch_attn_noalloc(const kvq_config* cfg, const kvq_cache* c
     }
     ws = addr[dev];
   }
-  return kvq_launch_attn(cfg, cache, q_rot, out, sm_scale, max_ctx, ws, d_status, stream);
+  return kvq_launch_attn(cfg, cache, q_rot, out, 0, sm_scale, max_ctx, ws, d_status, stream);
 }

@@ -11,7 +11,7 @@ int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr, const uint
                       cudaStream_t stream);
 int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens, int32_t* d_status,
                      cudaStream_t stream);
-int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, float* out,
+int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, void* out, int out_bf16,
                     float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status, cudaStream_t stream);
 int kvq_launch_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, float* out,
                             float sm_scale, int32_t max_ctx, int32_t* d_status, cudaStream_t stream);

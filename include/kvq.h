@@ -242,6 +242,18 @@ KVQ_API int kv_attn_decode(const kvq_config* cfg, const kvq_cache* cache, const 
                    float* out, float sm_scale, int32_t max_ctx,
                    void* workspace, size_t ws_bytes, int32_t* d_status, void* stream);
 
+/* kv_attn_decode_bf16: kv_attn_decode with a bf16 output.
+ *   out     [B][Hq][d] bf16 (8-byte aligned): the float32 result of kv_attn_decode rounded
+ *           once to bf16 (nearest-even) -- the same kernel, only the final store differs.
+ * Arguments, workspace and errors as kv_attn_decode.  For callers whose next GEMM (the
+ * output projection, in the T_V space) takes bf16 activations; the rounding adds up to
+ * 2^-9 relative per element on top of the float32 result.
+ * Source: [OSCAR] section 4 "Decoding Attention Kernel" (decode attention over the mixed
+ * cache); the output precision is not fixed by the pages. */
+KVQ_API int kv_attn_decode_bf16(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
+                                uint16_t* out, float sm_scale, int32_t max_ctx,
+                                void* workspace, size_t ws_bytes, int32_t* d_status, void* stream);
+
 /* kv_attn_decode_noalloc: kv_attn_decode without a caller-supplied workspace, for callers
  * that cannot allocate device memory on this path -- for example a plugin running inside a
  * serving framework whose memory pool owns the whole device and forbids direct cudaMalloc,
