@@ -399,6 +399,14 @@ def measure_chunk(args, w, run, k_new, v_new, sidx, pos, reset, stream, peak):
         reset()
         kv()
     t_kv = _timed_avg(kv, args.steps, stream, reset)
+    # the same append through the fused call (transform and quantize-on-write in one pass)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(np.full(w.batch, w.n_new))]), dtype=torch.int32,
+                      device=r.device)
+    fused = lambda: r.append_chunk(k_new, v_new, cu)
+    for _ in range(args.warmup):
+        reset()
+        fused()
+    t_fused = _timed_avg(fused, args.steps, stream, reset)
     # the chunk queries, [B * n_new, Hq, d] (sequence-major, then token)
     g = w.gqa
     qc = np.zeros((w.batch, w.n_new, w.n_q_heads, w.head_dim), np.uint16)
@@ -425,6 +433,12 @@ def measure_chunk(args, w, run, k_new, v_new, sidx, pos, reset, stream, peak):
                                "key_tflops": round(flops_kv / (t_kv * 1e-3) / 1e12, 2),
                                "bytes_basis": "fused minimum (each new row read once, INT2 / BF16 written once)",
                                "quantized_tokens_per_seq": cb["quantized_tokens_per_seq"]},
+        "kv_append_fused": {"calls": "kv_append_chunk", "ms": round(t_fused, 5),
+                            "bytes": cb["kv_rotate_quantize"],
+                            "achieved_gbs": round(cb["kv_rotate_quantize"] / (t_fused * 1e-3) / 1e9, 2),
+                            "frac_of_peak": round(cb["kv_rotate_quantize"] / (t_fused * 1e-3) / 1e9 / peak, 4),
+                            "key_tflops": round(flops_kv / (t_fused * 1e-3) / 1e12, 2),
+                            "bytes_basis": "fused minimum (each new row read once, INT2 / BF16 written once)"},
         "query_rotation": {"calls": "kv_rotate_qk (queries only)", "rows": cb["query_rows"], "ms": round(t_q, 5),
                            "bytes": cb["query_rotation"],
                            "achieved_gbs": round(cb["query_rotation"] / (t_q * 1e-3) / 1e9, 2),

@@ -36,7 +36,7 @@ KVQ_QUANT_QUEST_RMS = 1
 KVQ_TRANSFORM_DENSE = 0
 KVQ_TRANSFORM_HADAMARD = 1
 
-EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_attn_decode", "kv_attn_decode_bf16", "kv_attn_decode_noalloc",
+EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_append_chunk", "kv_attn_decode", "kv_attn_decode_bf16", "kv_attn_decode_noalloc",
             "kv_attn_workspace_bytes",
             "kvq_page_head_bytes", "kvq_page_bytes", "kvq_status_string", "kvq_version",
             "kvq_selftest_scale_division", "kvq_selftest_tc_integer_sums")
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         l.kv_rotate_qk.argtypes = [P(CConfig), P(CTransform), vp, vp, i32, vp, vp, vp, vp, i32, P(CCache), vp, vp]
         l.kv_rotate_qk.restype = ctypes.c_int
         l.kv_quant_flush.argtypes = [P(CConfig), P(CCache), i32, vp, vp]
+        l.kv_append_chunk.restype = ctypes.c_int
+        l.kv_append_chunk.argtypes = [P(CConfig), P(CTransform), vp, vp, vp, i32, P(CCache), vp, vp]
         l.kv_quant_flush.restype = ctypes.c_int
         l.kv_attn_decode.argtypes = [P(CConfig), P(CCache), vp, vp, ctypes.c_float, i32, vp, sz, vp, vp]
         l.kv_attn_decode.restype = ctypes.c_int
@@ -254,6 +256,17 @@ def kv_rotate_qk(cfg: KVConfig, tr: Transform, q, q_out, k, v, seq_idx, pos, cac
     rc = lib().kv_rotate_qk(ctypes.byref(c), ctypes.byref(t), _ptr(q), _ptr(q_out), n_q, _ptr(k), _ptr(v),
                             _ptr(seq_idx), _ptr(pos), n_kv, ctypes.byref(cc), _ptr(status), _stream(stream))
     _check(rc, "kv_rotate_qk")
+
+
+def kv_append_chunk(cfg: KVConfig, tr: Transform, k, v, cu_rows, cache: KVCache, status, stream=None) -> None:
+    """k, v [n, Hkv, d]: rows cu_rows[b] .. cu_rows[b+1]-1 appended to sequence b, transformed
+    and quantized on write in one pass (the effect of kv_rotate_qk + kv_quant_flush)."""
+    c, t = cfg.c(), tr.c()
+    n = 0 if k is None else int(k.shape[0])
+    cc = cache.c()
+    rc = lib().kv_append_chunk(ctypes.byref(c), ctypes.byref(t), _ptr(k), _ptr(v), _ptr(cu_rows), n,
+                               ctypes.byref(cc), _ptr(status), _stream(stream))
+    _check(rc, "kv_append_chunk")
 
 
 def kv_quant_flush(cfg: KVConfig, cache: KVCache, max_tokens_per_seq: int, status, stream=None) -> None:

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libkvq.so")
-SOURCES = ["api.cu", "rotate.cu", "rotate_tc.cu", "flush.cu", "attn.cu"]
+SOURCES = ["api.cu", "rotate.cu", "rotate_tc.cu", "flush.cu", "attn.cu", "chunk.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

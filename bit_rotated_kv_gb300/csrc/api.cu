@@ -1,5 +1,5 @@
 // The C ABI: argument validation (host only, before any CUDA call) and dispatch to the
-// three kernels.  See include/kvq.h for the contract of every entry point.
+// kernels.  See include/kvq.h for the contract of every entry point.
 #include "common.cuh"
 #include "launch.h"
 
@@ -119,6 +119,24 @@ KVQ_API int kv_quant_flush(const kvq_config* cfg, const kvq_cache* cache, int32_
   if (rc) return rc;
   if (max_tokens_per_seq < 0) return KVQ_ERR_INVALID_ARG;
   return kvq_launch_flush(cfg, cache, max_tokens_per_seq, d_status, (cudaStream_t)stream);
+}
+
+KVQ_API int kv_append_chunk(const kvq_config* cfg, const kvq_transform* tr, const uint16_t* k, const uint16_t* v,
+                            const int32_t* cu_rows, int32_t n_rows, const kvq_cache* cache, int32_t* d_status,
+                            void* stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  rc = check_cache(cfg, cache);
+  if (rc) return rc;
+  if (!tr || (tr->kind != KVQ_TRANSFORM_DENSE && tr->kind != KVQ_TRANSFORM_HADAMARD)) return KVQ_ERR_INVALID_ARG;
+  if (tr->kind == KVQ_TRANSFORM_HADAMARD) return KVQ_ERR_UNSUPPORTED;
+  if (n_rows < 0 || !cu_rows || !aligned(cu_rows, 4)) return KVQ_ERR_INVALID_ARG;
+  if (n_rows > 0) {
+    if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return KVQ_ERR_INVALID_ARG;
+    if (!tr->t_k || !aligned(tr->t_k, 16)) return KVQ_ERR_INVALID_ARG;
+    if (tr->t_v && !aligned(tr->t_v, 16)) return KVQ_ERR_INVALID_ARG;
+  }
+  return kvq_launch_append(cfg, tr, k, v, cu_rows, n_rows, cache, d_status, (cudaStream_t)stream);
 }
 
 KVQ_API int kv_attn_decode(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, float* out,

@@ -20,14 +20,22 @@
 // float32 / float64 definition.
 #include "common.cuh"
 #include "launch.h"
+#include "quant.cuh"
+
+#include <algorithm>
 
 namespace kvq {
 
 struct FlushParams {
   uint8_t* pages;
   const int32_t* page_table;
-  const int32_t* seq_len;
+  int32_t* seq_len;
   int32_t* s_quant;
+  // kv_append_chunk: cu_rows[b + 1] - cu_rows[b] rows are appended to sequence b by this
+  // call; the flush schedule runs on the advanced length, only the tokens already in the ring
+  // are quantized here (the appended ones are quantized as they are transformed), and the
+  // last CTA of a sequence publishes both seq_len and s_quant.  nullptr: kv_quant_flush.
+  const int32_t* cu_rows;
   const uint16_t* ring_k;
   const uint16_t* ring_v;
   int32_t* counters;
@@ -115,47 +123,6 @@ __device__ __forceinline__ void order_stats(const float s[4], int n, int nl, uns
   }
 }
 
-// y / d for a positive float16 scale d, correctly rounded.  With r = RN(1/d) and
-// q0 = RN(y r) (within one ulp of y / d), Markstein's theorem gives RN(y / d) =
-// RN(q0 + (y - q0 d) r), the remainder exact by FMA -- as long as nothing underflows or
-// overflows, which holds for 2^-96 <= |y| <= 2^96 since 2^-24 <= d <= 65504.  Other y (and
-// y = 0, NaN or infinity) take the IEEE division.
-__device__ __forceinline__ bool div_fast_ok(float y) {
-  const float ay = fabsf(y);
-  return ay >= 0x1p-96f && ay <= 0x1p96f;
-}
-__device__ __forceinline__ float div_fast(float y, float d, float r) {
-  const float q0 = __fmul_rn(y, r);
-  const float rem = __fmaf_rn(-q0, d, y);
-  return __fmaf_rn(rem, r, q0);
-}
-__device__ __forceinline__ float div_by_scale(float y, float d, float r) {
-  return div_fast_ok(y) ? div_fast(y, d, r) : __fdiv_rn(y, d);
-}
-// The four quotients of a lane, branch-free unless some lane of the warp holds a dividend
-// outside the fast range (then those quotients are redone by IEEE division).
-__device__ __forceinline__ void div4_by_scale(const float (&y)[4], float d, float (&q)[4]) {
-  const float r = __frcp_rn(d);
-  bool ok = true;
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    q[m] = div_fast(y[m], d, r);
-    ok = ok && div_fast_ok(y[m]);
-  }
-  if (!__all_sync(0xffffffffu, ok)) {
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
-      if (!div_fast_ok(y[m])) q[m] = __fdiv_rn(y[m], d);
-  }
-}
-
-// Quantizer constants of one warp's rows (keys or values), held in registers.
-struct QuantConsts {
-  int nl, group, affine, n_hi, n_lo, i_hi, i_lo;
-  float f_hi, f_lo;
-  double alpha;
-};
-
 // Quantize one row held as 4 float32 values per lane; returns the lane's 4 codes and the
 // group's Delta16 / z16 in dz (valid on all lanes).
 __device__ __forceinline__ void quant_row(const QuantConsts& Q, const float (&y)[4], int lane,
@@ -200,6 +167,39 @@ __device__ __forceinline__ void quant_row(const QuantConsts& Q, const float (&y)
   dz = __halves2half2(d16, z16);
 }
 
+// The flush span of sequence b from its length L_in and s_quant sq (both as read after the
+// dependency wait): n tokens from sq on are quantized from the ring by this launch, s_quant
+// advances by n_adv, and the length becomes L_new.  Invalid states quantize nothing.
+__device__ __forceinline__ void flush_span(const FlushParams& P, int b, int L_in, int sq, bool leader, int& n,
+                                           int& n_adv, int& L_new) {
+  const int nb = P.cu_rows ? __ldg(P.cu_rows + b + 1) - __ldg(P.cu_rows + b) : 0;
+  L_new = L_in + nb;
+  const int avail = L_new - sq - P.s_keep;
+  n_adv = avail >= P.s_flush ? (avail / P.s_flush) * P.s_flush : 0;
+  if (P.cu_rows) {
+    n = min(n_adv, max(0, L_in - sq));       // the rest of the span arrives with this call
+    if (n > P.max_tokens) {                  // more than the ring can hold: not a valid state
+      if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+      n = P.max_tokens;
+    }
+  } else {
+    const int cap = (P.max_tokens / P.s_flush) * P.s_flush;
+    n_adv = n_adv < cap ? n_adv : cap;
+    n = n_adv;
+  }
+  if (sq < P.s_sink || L_in < 0 || nb < 0) {
+    if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+    n = n_adv = 0;
+    L_new = L_in;
+  }
+}
+
+// Publication of the new state of sequence b (s_quant, and seq_len for an append).
+__device__ __forceinline__ void flush_publish(const FlushParams& P, int b, int sq, int n_adv, int L_new) {
+  P.s_quant[b] = sq + n_adv;
+  if (P.cu_rows) P.seq_len[b] = L_new;
+}
+
 __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   // shared-memory copy of the parameters (see rotate_kernel)
   pdl_trigger();
@@ -228,17 +228,8 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   const int nwarps = blockDim.x >> 5;
   // every warp derives the span itself (no block barrier before the first load)
   const int L = P.seq_len[b], sq = P.s_quant[b];
-  int n;
-  {
-    const int avail = L - sq - P.s_keep;
-    n = avail >= P.s_flush ? (avail / P.s_flush) * P.s_flush : 0;
-    const int cap = (P.max_tokens / P.s_flush) * P.s_flush;
-    n = n < cap ? n : cap;
-    if (sq < P.s_sink || L < 0) {
-      if (lane == 0 && warp == 0) set_status(P.status, KVQ_ERR_BOUNDS);
-      n = 0;
-    }
-  }
+  int n, n_adv, L_new;
+  flush_span(P, b, L, sq, lane == 0 && warp == 0, n, n_adv, L_new);
   // Every warp has read s_quant once the CTA passes this barrier.  A single CTA publishes the
   // new value at once (later kernels read it only after this grid completes); otherwise each
   // CTA takes a ticket now -- a release atomic whose result is only needed at the end, so its
@@ -246,7 +237,7 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   __syncthreads();
   int ticket = -1;
   if (threadIdx.x == 0) {
-    if (gridDim.x == 1) P.s_quant[b] = sq + n;
+    if (gridDim.x == 1) flush_publish(P, b, sq, n_adv, L_new);
     else ticket = atomic_add_release_gpu(P.counters + b, 1);
   }
   const int ng = kHeadDim / P.group;
@@ -257,7 +248,8 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   // quantized.
   const int n_items = n * P.hkv * 2;
   const int i0 = blockIdx.x * P.items_per_cta;
-  const int i1 = min(n_items, i0 + P.items_per_cta);
+  // an append's grid covers the usual ring occupancy; the last CTA takes whatever is beyond
+  const int i1 = (P.cu_rows && blockIdx.x == gridDim.x - 1) ? n_items : min(n_items, i0 + P.items_per_cta);
   const int which = warp & 1;
   const uint16_t* ring = which ? P.ring_v : P.ring_k;
   const int hkv = P.hkv, rcap = P.ring_cap, dh = nwarps >> 1;
@@ -381,7 +373,7 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   // the ticket (its fence orders that store after every other CTA's read)
   if (threadIdx.x == 0 && ticket == (int)gridDim.x - 1) {
     __threadfence();
-    P.s_quant[b] = sq + n;
+    flush_publish(P, b, sq, n_adv, L_new);
     P.counters[b] = 0;
   }
 }
@@ -392,11 +384,6 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
 // warp executes once per row (order-statistic merges, the scale arithmetic, the code packing,
 // the stores) is shared by two rows.  The arithmetic is the one-row kernel's, step for step.
 
-__device__ __forceinline__ void cswap(float& a, float& b) {
-  const float t = fminf(a, b);
-  b = fmaxf(a, b);
-  a = t;
-}
 // ascending; an optimal 19-comparator network for 8 inputs
 __device__ __forceinline__ void sort8(float (&s)[8]) {
   cswap(s[0], s[1]); cswap(s[2], s[3]); cswap(s[4], s[5]); cswap(s[6], s[7]);
@@ -538,21 +525,12 @@ __global__ void __launch_bounds__(256, 3) flush_kernel2(const FlushParams Pk) {
   }
   pdl_wait();
   const int L = P.seq_len[b], sq = P.s_quant[b];
-  int n;
-  {
-    const int avail = L - sq - P.s_keep;
-    n = avail >= P.s_flush ? (avail / P.s_flush) * P.s_flush : 0;
-    const int cap = (P.max_tokens / P.s_flush) * P.s_flush;
-    n = n < cap ? n : cap;
-    if (sq < P.s_sink || L < 0) {
-      if (lane == 0 && warp == 0) set_status(P.status, KVQ_ERR_BOUNDS);
-      n = 0;
-    }
-  }
+  int n, n_adv, L_new;
+  flush_span(P, b, L, sq, lane == 0 && warp == 0, n, n_adv, L_new);
   __syncthreads();
   int ticket = -1;
   if (threadIdx.x == 0) {
-    if (gridDim.x == 1) P.s_quant[b] = sq + n;
+    if (gridDim.x == 1) flush_publish(P, b, sq, n_adv, L_new);
     else ticket = atomic_add_release_gpu(P.counters + b, 1);
   }
   const int ng = kHeadDim / P.group;
@@ -560,7 +538,8 @@ __global__ void __launch_bounds__(256, 3) flush_kernel2(const FlushParams Pk) {
   // (all of kind w & 1), half hr the ones with k = hr mod 2
   const int n_items = n * P.hkv * 2;
   const int i0 = blockIdx.x * P.items_per_cta;
-  const int i1 = min(n_items, i0 + P.items_per_cta);
+  // an append's grid covers the usual ring occupancy; the last CTA takes whatever is beyond
+  const int i1 = (P.cu_rows && blockIdx.x == gridDim.x - 1) ? n_items : min(n_items, i0 + P.items_per_cta);
   const int which = warp & 1;
   const uint16_t* ring = which ? P.ring_v : P.ring_k;
   const int hkv = P.hkv, rcap = P.ring_cap;
@@ -698,7 +677,7 @@ __global__ void __launch_bounds__(256, 3) flush_kernel2(const FlushParams Pk) {
   }
   if (threadIdx.x == 0 && ticket == (int)gridDim.x - 1) {
     __threadfence();
-    P.s_quant[b] = sq + n;
+    flush_publish(P, b, sq, n_adv, L_new);
     P.counters[b] = 0;
   }
 }
@@ -746,25 +725,7 @@ extern "C" int kvq_launch_div_selftest(unsigned long long* d_mismatches, cudaStr
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
-static void kappa_pos(int g, double kappa, int& i, float& f) {
-  double pos = (double)(g - 1) * kappa;
-  double fl = floor(pos);
-  i = (int)fl;
-  f = (float)(pos - fl);
-}
-
-static int kvq_flush_extractions(int g, double kappa, int* n_lo, int* n_hi) {
-  int ilo, ihi;
-  float f;
-  kappa_pos(g, 1.0 - kappa, ilo, f);
-  kappa_pos(g, kappa, ihi, f);
-  *n_hi = ihi >= g - 1 ? 1 : g - ihi;
-  *n_lo = ilo + 2 > g ? g : ilo + 2;
-  return 0;
-}
-
-extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens,
-                                int32_t* d_status, cudaStream_t stream) {
+static FlushParams flush_params(const kvq_config* cfg, const kvq_cache* cache, int32_t* d_status) {
   FlushParams P{};
   P.pages = (uint8_t*)cache->pages;
   P.page_table = cache->page_table;
@@ -782,7 +743,6 @@ extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, i
   P.ring_cap = cfg->ring_cap;
   P.max_pages = cfg->max_pages_per_seq;
   P.num_pages = cfg->num_pages;
-  P.max_tokens = max_tokens;
   P.group = cfg->group_size;
   P.quantizer = cfg->quantizer;
   P.l2 = cfg->key_l2norm;
@@ -790,23 +750,24 @@ extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, i
   P.alpha = cfg->quest_alpha;
   const double kap[2] = {cfg->kappa_k, cfg->kappa_v};
   for (int w = 0; w < 2; ++w) {
-    kappa_pos(cfg->group_size, kap[w], P.i_hi[w], P.f_hi[w]);
-    kappa_pos(cfg->group_size, 1.0 - kap[w], P.i_lo[w], P.f_lo[w]);
-    kvq_flush_extractions(cfg->group_size, kap[w], &P.n_lo[w], &P.n_hi[w]);
+    const QuantSpec q = make_quant_spec(cfg->group_size, cfg->quantizer, kap[w], cfg->quest_alpha);
+    P.i_hi[w] = q.i_hi;
+    P.f_hi[w] = q.f_hi;
+    P.i_lo[w] = q.i_lo;
+    P.f_lo[w] = q.f_lo;
+    P.n_hi[w] = q.n_hi;
+    P.n_lo[w] = q.n_lo;
   }
-  // no call can quantize more than the ring holds beyond S_keep (tokens [s_quant, L) live in
-  // the ring), which bounds the launch whatever max_tokens says
-  const int ring_limit = cfg->ring_cap - cfg->s_keep;
-  if (max_tokens > ring_limit) max_tokens = ring_limit;
-  int cap = max_tokens > 0 ? (max_tokens / cfg->s_flush) * cfg->s_flush : 0;
-  if (cap <= 0) return KVQ_OK;
-  P.max_tokens = cap;
-  // Work items are (token, kv head, K|V) rows, one warp each.  Decode-sized flushes: CTAs of
-  // 4 warps with one item per warp, spread over many SMs so the flush costs about one row's
-  // latency.  Prefill-sized flushes: CTAs of 8 warps, enough items per warp to fill one wave
-  // of the GPU, each warp prefetching its next row.  The last CTA of a sequence publishes
-  // s_quant.
-  const long long items = 2LL * cap * cfg->n_kv_heads;
+  return P;
+}
+
+// Work items are (token, kv head, K|V) rows, one warp each, over `grid_tokens` tokens per
+// sequence.  Decode-sized flushes: CTAs of 4 warps with one item per warp, spread over many
+// SMs so the flush costs about one row's latency.  Prefill-sized flushes: CTAs of 8 warps,
+// enough items per warp to fill one wave of the GPU, each warp prefetching its next row and
+// taking two rows at a time.  The last CTA of a sequence publishes s_quant.
+static int launch_flush_grid(FlushParams& P, const kvq_config* cfg, int grid_tokens, cudaStream_t stream) {
+  const long long items = 2LL * grid_tokens * cfg->n_kv_heads;
   const long long total = items * cfg->batch;
   int threads = 128, ipw = 1;
   if (total > 4LL * kSms * 16) {
@@ -817,10 +778,32 @@ extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, i
   const long long ipc = (long long)ipw * (threads / 32);
   if (ipc > (1LL << 30) || (items + ipc - 1) / ipc > 0x7fffffffLL || cfg->batch > 65535) return KVQ_ERR_UNSUPPORTED;
   P.items_per_cta = (int)ipc;
-  const int ctas = (int)((items + ipc - 1) / ipc);
+  const int ctas = (int)std::max(1LL, (items + ipc - 1) / ipc);
   dim3 grid(ctas, cfg->batch);
-  // prefill-sized flushes take two rows per warp (the per-row warp work is shared)
   return launch_pdl(threads == 256 ? flush_kernel2 : flush_kernel, grid, dim3(threads), 0, stream, P) == cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
+}
+
+extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens,
+                                int32_t* d_status, cudaStream_t stream) {
+  FlushParams P = flush_params(cfg, cache, d_status);
+  // no call can quantize more than the ring holds beyond S_keep (tokens [s_quant, L) live in
+  // the ring), which bounds the launch whatever max_tokens says
+  const int ring_limit = cfg->ring_cap - cfg->s_keep;
+  if (max_tokens > ring_limit) max_tokens = ring_limit;
+  int cap = max_tokens > 0 ? (max_tokens / cfg->s_flush) * cfg->s_flush : 0;
+  if (cap <= 0) return KVQ_OK;
+  P.max_tokens = cap;
+  return launch_flush_grid(P, cfg, cap, stream);
+}
+
+extern "C" int kvq_launch_flush_append(const kvq_config* cfg, const kvq_cache* cache, const int32_t* cu_rows,
+                                       int32_t* d_status, cudaStream_t stream) {
+  FlushParams P = flush_params(cfg, cache, d_status);
+  P.cu_rows = cu_rows;
+  // the tokens still in the ring (at most ring_cap); the grid covers what a ring holds between
+  // complete steps (fewer than S_keep + S_flush tokens), the last CTA of a sequence the rest
+  P.max_tokens = cfg->ring_cap;
+  return launch_flush_grid(P, cfg, std::min(cfg->ring_cap, cfg->s_keep + cfg->s_flush), stream);
 }

@@ -11,6 +11,11 @@ int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr, const uint
                       cudaStream_t stream);
 int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens, int32_t* d_status,
                      cudaStream_t stream);
+int kvq_launch_flush_append(const kvq_config* cfg, const kvq_cache* cache, const int32_t* cu_rows,
+                            int32_t* d_status, cudaStream_t stream);
+int kvq_launch_append(const kvq_config* cfg, const kvq_transform* tr, const uint16_t* k, const uint16_t* v,
+                      const int32_t* cu_rows, int32_t n_rows, const kvq_cache* cache, int32_t* d_status,
+                      cudaStream_t stream);
 int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, void* out, int out_bf16,
                     float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status, cudaStream_t stream);
 int kvq_launch_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, float* out,

@@ -372,13 +372,13 @@ extern "C" int kvq_launch_rotate(const kvq_config* cfg, const kvq_transform* tr,
   bool had = tr->kind == KVQ_TRANSFORM_HADAMARD;
   // queries
   P.t[0] = RotTensor{q, n_q_rows, cfg->n_q_heads, had ? ROT_WHT : ROT_DENSE, tr->t_k_inv_t, gqa, 1,
-                     q_out, nullptr, nullptr, 0};
+                     q_out, nullptr, nullptr, 0, 0};
   // keys
   P.t[1] = RotTensor{k, n_kv_rows, cfg->n_kv_heads, had ? ROT_WHT : ROT_DENSE, tr->t_k, 1, 0,
-                     nullptr, cache->sink_k, cache->ring_k, 1};
+                     nullptr, cache->sink_k, cache->ring_k, 1, 0};
   // values
   P.t[2] = RotTensor{v, n_kv_rows, cfg->n_kv_heads, tr->t_v ? ROT_DENSE : ROT_COPY, tr->t_v, 1, 0,
-                     nullptr, cache->sink_v, cache->ring_v, 0};
+                     nullptr, cache->sink_v, cache->ring_v, 0, 1};
   P.seq_idx = seq_idx;
   P.pos = pos;
   P.seq_len = cache->seq_len;

@@ -4,6 +4,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "exact.cuh"
+#include "quant.cuh"
 
 namespace kvq {
 
@@ -20,6 +21,7 @@ struct RotTensor {
   uint16_t* sink;        // cache destination (keys or values)
   uint16_t* ring;
   int update_len;        // raise seq_len (keys only)
+  int which;             // 0 keys, 1 values (quantizer constants of appended rows)
 };
 
 struct RotParams {
@@ -36,7 +38,70 @@ struct RotParams {
   const int32_t* s_quant;
   int s_sink, ring_cap, batch, hkv;
   int32_t* status;
+  // kv_append_chunk: the rows of sequence b are cu_rows[b] .. cu_rows[b+1] - 1, at positions
+  // seq_len[b] - (cu_rows[b+1] - row) (seq_len and s_quant already advanced by the flush
+  // step of the call); rows below s_quant[b] are quantized straight into their page.
+  const int32_t* cu_rows;   // nullptr: kv_rotate_qk (rows placed by seq_idx / pos)
+  uint8_t* pages;
+  const int32_t* page_table;
+  int max_pages, num_pages, page_bytes, ng, l2;
+  QuantSpec qs[2];          // keys, values
 };
+
+// Sequence of appended row `row`: the b with cu_rows[b] <= row < cu_rows[b + 1] (-1 if none).
+__device__ __forceinline__ int append_seq(const int32_t* cu_rows, int batch, int row) {
+  if (row < __ldg(cu_rows) || row >= __ldg(cu_rows + batch)) return -1;
+  int lo = 0, hi = batch - 1;            // cu_rows[lo] <= row < cu_rows[hi + 1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu_rows + mid) <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Destination kinds of an appended row.
+constexpr int kDstNone = 0, kDstRow = 1, kDstPage = 2;
+
+// Destination of appended row `row`, head h of tensor T (b = append_seq(row)): the BF16 sink
+// or ring row (kDstRow), or the (page, kv head) chunk and token slot tp of its INT2 page
+// (kDstPage).  Reads seq_len and s_quant: only after the flush step of the call.
+__device__ __forceinline__ int append_dst(const RotParams& P, const RotTensor& T, int row, int h, int b,
+                                          bool leader, void*& dst, int& tp) {
+  dst = nullptr;
+  tp = 0;
+  if (b < 0) {
+    if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+    return kDstNone;
+  }
+  const int L = P.seq_len[b], sq = P.s_quant[b];
+  const int p = L - (__ldg(P.cu_rows + b + 1) - row);
+  if (p < 0 || sq < P.s_sink) {
+    if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+    return kDstNone;
+  }
+  if (p < P.s_sink) {
+    dst = T.sink + (((size_t)b * P.hkv + h) * P.s_sink + p) * kHeadDim;
+    return kDstRow;
+  }
+  if (p < sq) {
+    const int lp = p - P.s_sink, pidx = lp >> 4;
+    const int pid = pidx < P.max_pages ? P.page_table[(size_t)b * P.max_pages + pidx] : -1;
+    if (pid < 0 || pid >= P.num_pages) {
+      if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+      return kDstNone;
+    }
+    dst = P.pages + ((size_t)pid * P.hkv + h) * P.page_bytes;
+    tp = lp & (kPage - 1);
+    return kDstPage;
+  }
+  if (p >= sq + P.ring_cap) {
+    if (leader) set_status(P.status, KVQ_ERR_BOUNDS);
+    return kDstNone;
+  }
+  dst = T.ring + (((size_t)b * P.hkv + h) * P.ring_cap + (p % P.ring_cap)) * kHeadDim;
+  return kDstRow;
+}
 
 // Destination of row `row`, head `h` of tensor tt (b = seq_idx[row], p = pos[row] for cache
 // rows, loaded by the caller; sq_loaded = s_quant[b] when the caller has loaded it, else -1);
@@ -107,5 +172,9 @@ constexpr long long kTcMinPairs = 128LL * kSms;
 // Launch of the dense tensors of P on the tensor cores (P.n_dense and the tile sizes are set
 // here; the warp items must already have been launched).
 int launch_rotate_tc(RotParams P, cudaStream_t stream);
+
+// Launch of the copied (identity-transform) tensors of an append (P.cu_rows set): each row
+// goes to its window row or is quantized into its page.
+int launch_append_copy(const RotParams& P, cudaStream_t stream);
 
 }  // namespace kvq

@@ -51,14 +51,15 @@ constexpr int kList = 256;                           // queued undecided outputs
 
 // per-row metadata of a chunk (four buffers: warps run up to three chunks apart)
 struct UmRow {
-  uint16_t* dst;         // destination row (nullptr: nothing to write)
+  void* dst;             // BF16 destination row, or the (page, kv head) chunk (kRowPage)
   const uint16_t* src;   // the source row (for exact recomputation)
   int fr;                // exponent field f_r of the row's units
-  int flags;             // kRowZero | kRowBad | kRowLossy
-  int pad[2];
+  int flags;             // kRowZero | kRowBad | kRowLossy | kRowLive | kRowPage
+  int tp;                // token slot in the page (kRowPage)
+  int pad;
 };
 static_assert(sizeof(UmRow) == 32, "UmRow layout");
-constexpr int kRowZero = 1, kRowBad = 2, kRowLossy = 4;
+constexpr int kRowZero = 1, kRowBad = 2, kRowLossy = 4, kRowLive = 8, kRowPage = 16;
 
 constexpr int kWorkers = 16;                         // warps that slice rows and decide outputs
 constexpr int kThreads = 32 * (kWorkers + 1);        // + one warp that issues the MMAs
@@ -70,9 +71,14 @@ constexpr int kTSpan = kHeadDim / kParts;            // entries of a T row per t
 constexpr int kMetaOff = 2 * kXBuf;
 constexpr int kListOff = kMetaOff + 4 * kUmRows * (int)sizeof(UmRow);
 constexpr int kExchOff = kListOff + kWorkers * kList * 2;
-constexpr int kUmUsed = kExchOff + 2 * kParts * 128 * 4;   // exponent and |T| sum exchange
+constexpr int kStgOff = kExchOff + 2 * kParts * 128 * 4;   // after the exponent and |T| sum exchange
+// decided rows of a chunk, row-major (128 bf16 + 16 bytes per row: an octet's 16-byte loads
+// of one row fall in distinct banks), double-buffered
+constexpr int kStgStride = 272;
+constexpr int kStgBuf = kUmRows * kStgStride;
+constexpr int kUmUsed = kStgOff + 2 * kStgBuf;
 // more than half of an SM's shared memory: never two CTAs on one SM (each holds all of TMEM)
-constexpr int kUmSmem = 120 * 1024;
+constexpr int kUmSmem = 156 * 1024;
 static_assert(kUmUsed + 1024 <= kUmSmem, "shared memory layout");
 
 constexpr uint32_t kTmemCols = 512;
@@ -101,6 +107,20 @@ __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   uint2 x;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x.x), "=r"(x.y) : "r"(a) : "memory");
   return x;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 x;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w) : "r"(a)
+               : "memory");
+  return x;
+}
+__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t x) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)x) : "memory");
+}
+// barrier 1 + part: the four worker warps of one part (rows 16 part .. 16 part + 15 of a
+// chunk, all 128 outputs); the MMA warp never takes part
+__device__ __forceinline__ void part_sync(int part) {
+  asm volatile("bar.sync %0, 128;" ::"r"(1 + part) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -279,7 +299,8 @@ __device__ __forceinline__ float slice_t_part(const float* trow, int e_i, uint32
 // One worker warp's rows of a chunk, loaded ahead of slicing.
 struct XPre {
   uint2 x[kRowsPerWarp];  // this lane's 4 bf16 (k = 4 lane .. 4 lane + 3) of rows R w + j
-  int row, head, b, p;    // lanes 0..R-1: indices of row R w + lane (b, p for cache rows)
+  int row, head, b, p;    // lanes 0..R-1: indices of row R w + lane (b, p for cache rows;
+                          // appended rows: b from cu_rows, p found after the dependency wait)
   int sq;                 // lanes 0..R-1: s_quant[b] (cache rows, loaded after the dependency wait)
   int valid;              // lanes 0..R-1: the row exists
 };
@@ -297,9 +318,13 @@ __device__ __forceinline__ void x_prefetch(const RotParams& P, const RotTensor& 
   pre.b = pre.p = 0;
   pre.sq = -1;
   if (pre.valid && !T.is_query) {
-    pre.b = __ldg(P.seq_idx + row);
-    pre.p = __ldg(P.pos + row);
-    if (after_wait && pre.b >= 0 && pre.b < P.batch) pre.sq = P.s_quant[pre.b];
+    if (P.cu_rows) {
+      pre.b = append_seq(P.cu_rows, P.batch, row);
+    } else {
+      pre.b = __ldg(P.seq_idx + row);
+      pre.p = __ldg(P.pos + row);
+      if (after_wait && pre.b >= 0 && pre.b < P.batch) pre.sq = P.s_quant[pre.b];
+    }
   }
 #pragma unroll
   for (int j = 0; j < kRowsPerWarp; ++j) {
@@ -314,11 +339,18 @@ __device__ __forceinline__ void x_prefetch(const RotParams& P, const RotTensor& 
 // the dependency wait (destinations read s_quant).
 __device__ __forceinline__ void x_slice(const RotParams& P, const RotTensor& T, const XPre& pre, uint8_t* xb,
                                         UmRow* meta, int warp, int lane) {
-  uint16_t* dst = nullptr;
+  void* dst = nullptr;
   const uint16_t* src = nullptr;
+  int dflags = 0, tp = 0;
   if (pre.valid) {
     src = T.src + ((size_t)pre.row * T.heads + pre.head) * kHeadDim;
-    dst = rot_dst(P, T, pre.row, pre.head, pre.b, pre.p, true, pre.sq);
+    if (P.cu_rows && !T.is_query) {
+      const int kind = append_dst(P, T, pre.row, pre.head, pre.b, true, dst, tp);
+      dflags = kind == kDstPage ? (kRowLive | kRowPage) : kind == kDstRow ? kRowLive : 0;
+    } else {
+      dst = rot_dst(P, T, pre.row, pre.head, pre.b, pre.p, true, pre.sq);
+      dflags = dst ? kRowLive : 0;
+    }
   }
 #pragma unroll
   for (int j = 0; j < kRowsPerWarp; ++j) {
@@ -346,29 +378,76 @@ __device__ __forceinline__ void x_slice(const RotParams& P, const RotTensor& T, 
     for (int a = 0; a < 3; ++a)
       sts_v2(um_saddr(xb) + (uint32_t)(a * kXSlice + offj), pack_digits(d[a][0], d[a][1]),
              pack_digits(d[a][2], d[a][3]));
-    uint16_t* dj = (uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)dst, j);
-    const uint16_t* sj = (const uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)src, j);
+    const unsigned long long dj = __shfl_sync(0xffffffffu, (unsigned long long)dst, j);
+    const unsigned long long sj = __shfl_sync(0xffffffffu, (unsigned long long)src, j);
+    const int fj = __shfl_sync(0xffffffffu, dflags, j), tj = __shfl_sync(0xffffffffu, tp, j);
     if (lane == 0) {
       const uint32_t ma = um_saddr(meta + kRowsPerWarp * warp + j);
-      sts_u64(ma, (unsigned long long)dj);
-      sts_u64(ma + 8, (unsigned long long)sj);
-      sts_v2(ma + 16, (uint32_t)fr, (uint32_t)((zero ? kRowZero : 0) | (bad ? kRowBad : 0) | (lossy ? kRowLossy : 0)));
+      sts_u64(ma, dj);
+      sts_u64(ma + 8, sj);
+      sts_v2(ma + 16, (uint32_t)fr,
+             (uint32_t)(fj | (zero ? kRowZero : 0) | (bad ? kRowBad : 0) | (lossy ? kRowLossy : 0)));
+      sts_v2(ma + 24, (uint32_t)tj, 0u);
     }
   }
 }
 
-// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly; returns 0.
-// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly (exact.cuh);
-// returns 0.
+// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly (exact.cuh)
+// into the chunk's staged rows; returns 0.
 __device__ __noinline__ int exact_list(const uint16_t* list, int count, const UmRow* mrow, const float* tmat,
-                                       int lane) {
+                                       uint8_t* stg, int lane) {
   __syncwarp();
   for (int f = 0; f < count; ++f) {
     const int r = list[f] >> 7, o = list[f] & 127;
-    exact_output_warp(tmat + (size_t)o * kHeadDim, mrow[r].src, mrow[r].dst, o, lane);
+    exact_output_warp(tmat + (size_t)o * kHeadDim, mrow[r].src, reinterpret_cast<uint16_t*>(stg + r * kStgStride), o,
+                      lane);
   }
   __syncwarp();
   return 0;
+}
+
+// Row phase of a chunk: the octet (lane / 8) of warp w takes staged row 4 w + lane / 8 (a row
+// of the warp's own part), lane j = lane % 8 its channels 16 j .. 16 j + 15.  BF16 destinations get the row with 16-byte
+// stores (8-byte ones when the destination is only 8-byte aligned); page destinations get
+// the quantized token.  The whole warp calls it.
+__device__ __forceinline__ void row_phase(const UmRow* mrow, uint32_t stg_s, const QuantConsts& Qc, bool is_key,
+                                          bool key_norm, int ng, int32_t* status, int warp, int lane) {
+  const int r = 4 * warp + (lane >> 3), j = lane & 7;
+  const uint32_t ma = um_saddr(mrow + r);
+  void* dst = (void*)lds_u64(ma);
+  const int flags = (int)lds_v2(ma + 16).y;
+  const int tp = (int)lds_v2(ma + 24).x;
+  const bool live = (flags & kRowLive) != 0, page = (flags & kRowPage) != 0;
+  // lanes 4..7 of the octet read their upper 16 bytes first, so each quarter-warp's loads
+  // cover the 32 banks once
+  const int first = (j >> 2) & 1;
+  const uint32_t rs = stg_s + (uint32_t)(r * kStgStride + 32 * j);
+  const uint4 a = lds_v4(rs + 16u * (uint32_t)first), c = lds_v4(rs + 16u * (uint32_t)(1 - first));
+  const uint4 lo = first ? c : a, hi = first ? a : c;          // channels 16j..16j+7, 16j+8..16j+15
+  if (live && !page) {
+    uint16_t* d = static_cast<uint16_t*>(dst) + 16 * j;
+    if (((uintptr_t)d & 15u) == 0) {
+      reinterpret_cast<uint4*>(d)[0] = lo;
+      reinterpret_cast<uint4*>(d)[1] = hi;
+    } else {
+      uint2* d2 = reinterpret_cast<uint2*>(d);
+      d2[0] = make_uint2(lo.x, lo.y);
+      d2[1] = make_uint2(lo.z, lo.w);
+      d2[2] = make_uint2(hi.x, hi.y);
+      d2[3] = make_uint2(hi.z, hi.w);
+    }
+  }
+  if (__any_sync(0xffffffffu, page)) {
+    const uint32_t u[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    float y[16];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      y[2 * m] = __uint_as_float(u[m] << 16);
+      y[2 * m + 1] = __uint_as_float(u[m] & 0xffff0000u);
+    }
+    quantize_store_octet(Qc, is_key, key_norm, y, page ? static_cast<uint8_t*>(dst) : nullptr, tp, ng, page, lane,
+                         status);
+  }
 }
 
 // Bounded wait that also gives up when another warp has given up.
@@ -530,9 +609,16 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
       publish(1);
       if (nch > 2) x_prefetch(P, T, mh, c0 + 2, pairs, warp, lane, true, pre);
     }
+    const QuantConsts Qc = quant_consts(P.qs[T.which], 16);
+    const bool is_key = T.which == 0, key_norm = T.which == 0 && P.l2 != 0;
     int count = 0;
+    bool dead = false;      // a bounded wait ran out: the warp only keeps meeting the barrier
     for (int n = 0; n < nch; ++n) {
-      if (!warp_wait(&bar_mma[n & 1], (uint32_t)((n >> 1) & 1), &abort_sh, lane)) break;
+      uint8_t* stg = sm + kStgOff + (n & 1) * kStgBuf;
+      const uint32_t stg_s = um_saddr(stg);
+      const UmRow* mrow = meta + (n & 3) * kUmRows;
+      if (!dead && !warp_wait(&bar_mma[n & 1], (uint32_t)((n >> 1) & 1), &abort_sh, lane)) dead = true;
+      if (!dead) {
       tc_fence_after();
       uint32_t acc[4][kEpiRows];
 #pragma unroll
@@ -543,19 +629,18 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) um_arrive(&bar_acc);
-      // ---- rounding decisions of chunk n: output i, rows kEpiRows part + c ----
-      // All rows first, without control flow (independent chains the scheduler interleaves);
-      // undecided outputs are queued afterwards, only when the warp has any.
-      const UmRow* mrow = meta + (n & 3) * kUmRows;
+      // ---- rounding decisions of chunk n: output i, rows kEpiRows part + c, into the staged
+      // rows.  All rows first, without control flow (independent chains the scheduler
+      // interleaves); undecided outputs are queued afterwards, only when the warp has any.
       const uint32_t mrow_s = um_saddr(mrow);
       uint32_t und_bits = 0;
 #pragma unroll
       for (int c = 0; c < kEpiRows; ++c) {
         const int r = kEpiRows * part + c;
         const uint32_t ma = mrow_s + (uint32_t)r * (uint32_t)sizeof(UmRow);
-        uint16_t* dst = (uint16_t*)lds_u64(ma);
         const uint2 ff = lds_v2(ma + 16);
         const int fr = (int)ff.x, flags = (int)ff.y;
+        const bool live = (flags & kRowLive) != 0;
         const float v = fmaf(__uint_as_float(acc[3][c]), 0x1p-24f,
                              fmaf(__uint_as_float(acc[2][c]), 0x1p-16f,
                                   fmaf(__uint_as_float(acc[1][c]), 0x1p-8f, __uint_as_float(acc[0][c]))));
@@ -570,8 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
         int b = (decided && (unsigned)(ey - 267) < 254u) ? bu + (ey - 266 - ((bu >> 7) & 0xff)) * 128 : -1;
         b = ((flags & kRowZero) || !tnz) ? 0 : b;           // an exact zero is +0
         b = (force || (flags & kRowBad)) ? -1 : b;
-        if (dst != nullptr && b >= 0) __stcg(reinterpret_cast<unsigned short*>(dst + i), (unsigned short)b);
-        und_bits |= (dst != nullptr && b < 0) ? (1u << c) : 0u;
+        if (live && b >= 0) sts_u16(stg_s + (uint32_t)(r * kStgStride + 2 * i), (uint32_t)b);
+        und_bits |= (live && b < 0) ? (1u << c) : 0u;
       }
       if (__any_sync(0xffffffffu, und_bits != 0u)) {
 #pragma unroll 1
@@ -580,12 +665,18 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
           const unsigned mk = __ballot_sync(0xffffffffu, und);
           if (und) list[count + __popc(mk & ((1u << lane) - 1u))] = (uint16_t)(((kEpiRows * part + c) << 7) | i);
           count += __popc(mk);
-          if (count > kList - 32) count = exact_list(list, count, mrow, tmat, lane);
+          if (count > kList - 32) count = exact_list(list, count, mrow, tmat, stg, lane);
         }
       }
-      count = exact_list(list, count, mrow, tmat, lane);
+      count = exact_list(list, count, mrow, tmat, stg, lane);
+      }
+      // ---- the four warps of a part meet here once per chunk (also after a timeout); then the
+      // part's rows of chunk n go out: BF16 rows copied, page rows quantized ----
+      part_sync(part);
+      const int stop = __shfl_sync(0xffffffffu, abort_sh, 0);
+      if (!stop) row_phase(mrow, stg_s, Qc, is_key, key_norm, P.ng, P.status, warp, lane);
       // ---- digits of chunk n + 2 into chunk n's buffer (its MMAs have completed) ----
-      if (n + 2 < nch) {
+      if (!dead && n + 2 < nch) {
         x_slice(P, T, pre, xbuf(n), meta + ((n + 2) & 3) * kUmRows, warp, lane);
         publish(n + 2);
         if (n + 3 < nch) x_prefetch(P, T, mh, c0 + n + 3, pairs, warp, lane, true, pre);

@@ -1,5 +1,5 @@
-"""Drive the three C-ABI calls for a batch of sequences: chunked prefill of the cache and
-one serving step (append n_new tokens, flush, decode).  Argument marshalling only --
+"""Drive the C-ABI calls for a batch of sequences: chunked prefill of the cache and one
+serving step (append n_new tokens, flush, decode -- or the fused append, then decode).  Argument marshalling only --
 torch is used for device buffers, gathers of input rows and streams; every step of the
 method runs in the library's kernels."""
 
@@ -10,7 +10,8 @@ import math
 import numpy as np
 import torch
 
-from . import (KVCache, KVConfig, Transform, kv_attn_decode, kv_quant_flush, kv_rotate_qk, workspace)
+from . import (KVCache, KVConfig, Transform, kv_append_chunk, kv_attn_decode, kv_quant_flush, kv_rotate_qk,
+               workspace)
 
 
 def _rows_for(k_all: torch.Tensor, lengths_lo, lengths_hi):
@@ -58,6 +59,12 @@ class DecodeRunner:
         kv_rotate_qk(self.cfg, self.tr, q, q_out, k_rows, v_rows, seq_idx, pos, self.cache, self.status,
                      self.stream if stream is None else stream)
 
+    def append_chunk(self, k_rows, v_rows, cu_rows, stream=None) -> None:
+        """Rows cu_rows[b] .. cu_rows[b+1]-1 of k_rows / v_rows appended to sequence b, transformed
+        and quantized on write in one pass (seq_len and s_quant advance)."""
+        kv_append_chunk(self.cfg, self.tr, k_rows, v_rows, cu_rows, self.cache, self.status,
+                        self.stream if stream is None else stream)
+
     def flush(self, max_tokens: int, stream=None) -> None:
         kv_quant_flush(self.cfg, self.cache, max_tokens, self.status, self.stream if stream is None else stream)
 
@@ -87,6 +94,14 @@ class DecodeRunner:
         ib, it = _rows_for(k_all, ctx, [c + n_new for c in ctx])
         return (k_all[ib, it].contiguous(), v_all[ib, it].contiguous(), ib.to(torch.int32),
                 it.to(torch.int32))
+
+    def step_fused(self, q, k_rows, v_rows, cu_rows, stream=None) -> None:
+        """The same serving step with the appended chunk transformed and quantized in one pass:
+        append, rotate the queries, decode."""
+        self.append_chunk(k_rows, v_rows, cu_rows, stream)
+        kv_rotate_qk(self.cfg, self.tr, q, self.q_out, None, None, None, None, self.cache, self.status,
+                     self.stream if stream is None else stream)
+        self.decode(self.q_out, self.out, stream)
 
     def step(self, q, k_rows, v_rows, seq_idx, pos, n_new: int, stream=None) -> None:
         """One serving step: rotate the new rows and the queries, flush, decode."""

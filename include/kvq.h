@@ -19,6 +19,10 @@
  *   kv_attn_decode  GQA decode attention reading the mixed BF16 / INT2 cache
  *                   directly ([OSCAR] section 4 "Decoding Attention Kernel";
  *                   [OScaR] "系统设计与 CUDA 实现"; [WUSH] GQA background).
+ *   kv_append_chunk the first two fused for a prefill chunk: transform on write
+ *                   and quantize-on-write in one pass, rows bound for INT2 never
+ *                   written as BF16 ([OScaR] "系统设计与 CUDA 实现", key-quant
+ *                   kernel; [OSCAR] section 4 "KV Cache Update").
  *
  * Conventions shared by every call
  *   - Every pointer inside a struct or argument is a DEVICE pointer unless said
@@ -41,8 +45,9 @@
  *     stream begin early (programmatic dependent launch) and waits for its
  *     predecessor's results before it touches the cache state.  Before that wait a
  *     kernel may already read inputs that no call of this library writes:
- *     kv_rotate_qk reads q, k, v, seq_idx, pos and the transform matrices, and
- *     kv_attn_decode the page table.  These must therefore be complete before the
+ *     kv_rotate_qk reads q, k, v, seq_idx, pos and the transform matrices,
+ *     kv_append_chunk k, v, cu_rows and the matrices, and kv_attn_decode the
+ *     page table.  These must therefore be complete before the
  *     call is made -- the usual case (written by the host, or by a kernel that
  *     finished before the call): only a kernel that itself triggers programmatic
  *     dependent launch and writes them afterwards would violate it.
@@ -224,6 +229,36 @@ KVQ_API int kv_rotate_qk(const kvq_config* cfg, const kvq_transform* tr,
  * integer-quantization formulas. */
 KVQ_API int kv_quant_flush(const kvq_config* cfg, const kvq_cache* cache, int32_t max_tokens_per_seq,
                    int32_t* d_status, void* stream);
+
+/* kv_append_chunk: append a chunk of new tokens to every sequence -- the effect of
+ * kv_rotate_qk on those rows followed by kv_quant_flush, in one pass.
+ *   k, v     [n_rows][Hkv][d] bf16 new keys / values (16-byte aligned; NULL when
+ *            n_rows == 0)
+ *   cu_rows  [B + 1] int32 (device): the rows of sequence b are cu_rows[b] ..
+ *            cu_rows[b+1] - 1, in token order; cu_rows[0] = 0 and cu_rows[B] =
+ *            n_rows (rows outside [cu_rows[0], cu_rows[B]) are skipped with
+ *            KVQ_ERR_BOUNDS).  A sequence may append no rows.
+ * Row r of sequence b gets position p = seq_len[b] + r - cu_rows[b]; seq_len[b]
+ * then advances by cu_rows[b+1] - cu_rows[b], and the flush rule of
+ * kv_quant_flush runs on the advanced length with no cap (s_quant advances by
+ * whole S_flush spans while seq_len - s_quant >= s_keep + s_flush).  Keys are
+ * transformed by T_K (DENSE only: KVQ_ERR_UNSUPPORTED for HADAMARD), values by T_V
+ * or copied.  A row with p < s_sink goes to the sink, one below the new s_quant is
+ * quantized straight into its INT2 page (as kv_quant_flush would), the others go
+ * to their ring slot; tokens already in the ring that the new s_quant passes are
+ * quantized from the ring.  Every byte written -- pages, sink and ring rows,
+ * seq_len, s_quant -- equals what kv_rotate_qk at those positions followed by
+ * kv_quant_flush (max_tokens_per_seq large enough) writes; the ring only has to
+ * hold the tokens that stay in the window, not the whole chunk.
+ * Execution: three kernels (flush of the ring tokens, copied rows, dense rows on
+ * the tensor cores); meant for prefill-sized chunks (decode-sized appends are
+ * cheaper through kv_rotate_qk + kv_quant_flush).
+ * Source: [OScaR] "系统设计与 CUDA 实现" (key-quant kernel: transform, scaling and
+ * INT2 packing on chip, input read once, codes written once); [OSCAR] section 4
+ * "KV Cache Update" (fused prefill clip + quantize); [WUSH] inference algorithm. */
+KVQ_API int kv_append_chunk(const kvq_config* cfg, const kvq_transform* tr,
+                    const uint16_t* k, const uint16_t* v, const int32_t* cu_rows, int32_t n_rows,
+                    const kvq_cache* cache, int32_t* d_status, void* stream);
 
 /* kv_attn_decode: one decode step of GQA attention for every sequence.
  *   q_rot   [B][Hq][d] bf16 compensated queries (kv_rotate_qk output)
