@@ -169,12 +169,13 @@ __device__ __forceinline__ void exact_output_warp(const float* trow, const uint1
 // (rotate_tc.cu): about one 128-row block per SM.
 constexpr long long kTcMinPairs = 128LL * kSms;
 
+// Tiles of the dense tensors of P on the tensor cores: P.rpc, P.n_dense and P.dense_total.
+int plan_rotate_tc(RotParams& P);
+
 // Launch of the dense tensors of P on the tensor cores (P.n_dense and the tile sizes are set
 // here; the warp items must already have been launched).
 int launch_rotate_tc(RotParams P, cudaStream_t stream);
 
-// Launch of the copied (identity-transform) tensors of an append (P.cu_rows set): each row
-// goes to its window row or is quantized into its page.
-int launch_append_copy(const RotParams& P, cudaStream_t stream);
+
 
 }  // namespace kvq

@@ -37,273 +37,12 @@
 // chunk's digits are written and the previous chunk's sums were read; warps 0-15 read the
 // accumulators into registers at once (so the next chunk's MMAs overlap this chunk's rounding
 // decisions and stores), then slice the rows of the chunk after next.
-#include "rotate.cuh"
+#include "tc.cuh"
 
 #include <mutex>
 
 namespace kvq {
 namespace {
-
-constexpr int kUmRows = 64;                          // rows of a chunk (N of every MMA)
-constexpr int kXSlice = kUmRows * kHeadDim * 2;      // one x digit matrix: 16 KB
-constexpr int kXBuf = 3 * kXSlice;                   // three digit matrices per chunk buffer
-constexpr int kList = 256;                           // queued undecided outputs per warp
-
-// per-row metadata of a chunk (four buffers: warps run up to three chunks apart)
-struct UmRow {
-  void* dst;             // BF16 destination row, or the (page, kv head) chunk (kRowPage)
-  const uint16_t* src;   // the source row (for exact recomputation)
-  int fr;                // exponent field f_r of the row's units
-  int flags;             // kRowZero | kRowBad | kRowLossy | kRowLive | kRowPage
-  int tp;                // token slot in the page (kRowPage)
-  int pad;
-};
-static_assert(sizeof(UmRow) == 32, "UmRow layout");
-constexpr int kRowZero = 1, kRowBad = 2, kRowLossy = 4, kRowLive = 8, kRowPage = 16;
-
-constexpr int kWorkers = 16;                         // warps that slice rows and decide outputs
-constexpr int kThreads = 32 * (kWorkers + 1);        // + one warp that issues the MMAs
-constexpr int kRowsPerWarp = kUmRows / kWorkers;     // rows a worker warp slices per chunk
-constexpr int kParts = kWorkers / 4;                 // worker warps per TMEM lane quadrant
-constexpr int kEpiRows = kUmRows / kParts;           // rows (accumulator columns) per thread
-constexpr int kTSpan = kHeadDim / kParts;            // entries of a T row per thread
-
-constexpr int kMetaOff = 2 * kXBuf;
-constexpr int kListOff = kMetaOff + 4 * kUmRows * (int)sizeof(UmRow);
-constexpr int kExchOff = kListOff + kWorkers * kList * 2;
-constexpr int kStgOff = kExchOff + 2 * kParts * 128 * 4;   // after the exponent and |T| sum exchange
-// decided rows of a chunk, row-major (128 bf16 + 16 bytes per row: an octet's 16-byte loads
-// of one row fall in distinct banks), double-buffered
-constexpr int kStgStride = 272;
-constexpr int kStgBuf = kUmRows * kStgStride;
-constexpr int kUmUsed = kStgOff + 2 * kStgBuf;
-// more than half of an SM's shared memory: never two CTAs on one SM (each holds all of TMEM)
-constexpr int kUmSmem = 156 * 1024;
-static_assert(kUmUsed + 1024 <= kUmSmem, "shared memory layout");
-
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCol = 256;
-// instruction descriptor, kind::f16: D f32, A and B bf16, both K-major, N = 64, M = 128
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kUmRows >> 3) << 17) |
-                            ((128u >> 4) << 24);
-constexpr long long kSpinLimit = 1LL << 22;      // try_wait rounds before a wait gives up
-
-// ---- tcgen05 / mbarrier primitives ---------------------------------------------------------
-__device__ __forceinline__ uint32_t um_saddr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-// explicit shared-memory accesses (the buffers are reached through a re-aligned pointer, which
-// the compiler would otherwise treat as generic)
-__device__ __forceinline__ void sts_v2(uint32_t a, uint32_t x, uint32_t y) {
-  asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
-}
-__device__ __forceinline__ void sts_u64(uint32_t a, unsigned long long x) {
-  asm volatile("st.shared.u64 [%0], %1;" ::"r"(a), "l"(x) : "memory");
-}
-__device__ __forceinline__ unsigned long long lds_u64(uint32_t a) {
-  unsigned long long x;
-  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(x) : "r"(a) : "memory");
-  return x;
-}
-__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
-  uint2 x;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x.x), "=r"(x.y) : "r"(a) : "memory");
-  return x;
-}
-__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
-  uint4 x;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w) : "r"(a)
-               : "memory");
-  return x;
-}
-__device__ __forceinline__ void sts_u16(uint32_t a, uint32_t x) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"((unsigned short)x) : "memory");
-}
-// barrier 1 + part: the four worker warps of one part (rows 16 part .. 16 part + 15 of a
-// chunk, all 128 outputs); the MMA warp never takes part
-__device__ __forceinline__ void part_sync(int part) {
-  asm volatile("bar.sync %0, 128;" ::"r"(1 + part) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void um_mbar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(um_saddr(bar)) : "memory");
-}
-__device__ __forceinline__ bool um_mbar_try(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(um_saddr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// bounded wait for phase `parity` of an mbarrier; false when the limit ran out
-__device__ __noinline__ bool um_mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (long long it = 0; it < kSpinLimit; ++it)
-    if (um_mbar_try(bar, parity)) return true;
-  return false;
-}
-
-// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// D (TMEM) [+]= A (TMEM) x B (shared, descriptor)^T
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
-          d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(um_saddr(bar))
-               : "memory");
-}
-
-// 8 consecutive TMEM columns of this warp's 32 lanes <- registers
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
-               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-// 32 consecutive TMEM columns of this warp's 32 lanes -> registers (not yet waited for)
-#define UM_O8(b)                                                                                            \
-  "=r"(v[b]), "=r"(v[b + 1]), "=r"(v[b + 2]), "=r"(v[b + 3]), "=r"(v[b + 4]), "=r"(v[b + 5]), "=r"(v[b + 6]), \
-      "=r"(v[b + 7])
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : UM_O8(0), UM_O8(8), UM_O8(16), UM_O8(24)
-      : "r"(taddr));
-}
-#undef UM_O8
-#define UM_O8(b)                                                                                            \
-  "=r"(v[b]), "=r"(v[b + 1]), "=r"(v[b + 2]), "=r"(v[b + 3]), "=r"(v[b + 4]), "=r"(v[b + 5]), "=r"(v[b + 6]), \
-      "=r"(v[b + 7])
-// 16 consecutive TMEM columns of this warp's 32 lanes -> registers (not yet waited for)
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : UM_O8(0), UM_O8(8)
-      : "r"(taddr));
-}
-#undef UM_O8
-// wait for this thread's TMEM loads; the registers pass through so no use moves above it
-#define UM_IO8(b)                                                                                           \
-  "+r"(v[b]), "+r"(v[b + 1]), "+r"(v[b + 2]), "+r"(v[b + 3]), "+r"(v[b + 4]), "+r"(v[b + 5]), "+r"(v[b + 6]), \
-      "+r"(v[b + 7])
-__device__ __forceinline__ void tmem_wait_ld32(uint32_t* v) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : UM_IO8(0), UM_IO8(8), UM_IO8(16), UM_IO8(24)::"memory");
-}
-__device__ __forceinline__ void tmem_wait_ld16(uint32_t* v) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : UM_IO8(0), UM_IO8(8)::"memory");
-}
-#undef UM_IO8
-
-// ---- digits ---------------------------------------------------------------------------------
-// bf16 bits of an integer d with |d| <= 128 (exact: at most 8 significant bits)
-__device__ __forceinline__ uint32_t digit_bf16(int d) {
-  const float f = __int_as_float(0x4B400000 + d) - 12582912.0f;    // float(d) for |d| < 2^22
-  return __float_as_uint(f) >> 16;
-}
-// lowest balanced base-256 digit (in [-128, 127]) of M, and M advanced past it
-__device__ __forceinline__ int take_digit(uint32_t& M) {
-  const int d = (int)((M + 128u) & 255u) - 128;
-  M = (M - (uint32_t)d) >> 8;
-  return d;
-}
-
-// byte offset of x element (row n < 64, k < 128) in a digit matrix: two 8 KB K halves of
-// 8-row groups (1024 B), rows 128 B apart, 16-byte chunks XOR-swizzled by row
-__device__ __forceinline__ int xs_offset(int n, int k) {
-  return (k >> 6) * 8192 + (n >> 3) * 1024 + (n & 7) * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) + (k & 7) * 2;
-}
-
-
-// The 72 MMAs of a chunk: x digit matrix a (shared memory, buffer at xbuf) against T digit
-// matrix b (TMEM), into the accumulator of level a + b, K = 128 in eight steps of 16.
-__device__ __forceinline__ void issue_chunk(uint32_t tb, uint32_t xbuf) {
-  constexpr int kA[9] = {0, 0, 1, 0, 1, 2, 0, 1, 2};
-  constexpr int kB[9] = {0, 1, 0, 2, 1, 0, 3, 2, 1};
-  constexpr int kFirst[9] = {1, 1, 0, 1, 0, 0, 1, 0, 0};
-#pragma unroll
-  for (int c = 0; c < 9; ++c) {
-    const uint32_t d = tb + kAccCol + 64u * (uint32_t)(kA[c] + kB[c]);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t bd = sw128_desc(xbuf + (uint32_t)(kA[c] * kXSlice + (kk >> 2) * 8192 + (kk & 3) * 32));
-      umma_ts(d, tb + 64u * (uint32_t)kB[c] + 8u * (uint32_t)kk, bd, (kFirst[c] && kk == 0) ? 0u : 1u);
-    }
-  }
-}
-
-// v * 2^k, exact whenever the result is a normal float (k in [-126, 254])
-__device__ __forceinline__ float scale_pow2(float v, int k) {
-  if (k > 127) {
-    v *= 0x1p64f;
-    k -= 64;
-  }
-  return v * __int_as_float((k + 127) << 23);
-}
-
-// bf16 bits of two integer-valued floats of at most 8 significant bits (exact), low = a
-__device__ __forceinline__ uint32_t pack_digits(float a, float b) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Balanced base-256 digits of X (|X| < 128): X = d0 + d1/2^8 + d2/2^16 (+ d3/2^24) + rest,
-// each digit an integer in [-128, 128] (round to nearest, so the rest is at most half a unit
-// of the last digit).  Every step is exact in fp32.
-__device__ __forceinline__ float next_digit(float& r) {
-  const float d = rintf(r);
-  r = (r - d) * 256.0f;
-  return d;
-}
-
-// T row i, entries kTSpan part .. (global) -> the four digit matrices in TMEM columns
-// 64 b + kTSpan / 2 part + ..., this warp's lanes.  Returns sum_j |T_ij| / U_i over them.
-__device__ __forceinline__ float slice_t_part(const float* trow, int e_i, uint32_t taddr) {
-  const int k = 133 - e_i;
-  float asum = 0.f;
-#pragma unroll 1
-  for (int blk = 0; blk < kTSpan / 16; ++blk) {
-    uint32_t out[4][8];
-#pragma unroll
-    for (int j4 = 0; j4 < 4; ++j4) {
-      const float4 t4 = reinterpret_cast<const float4*>(trow)[4 * blk + j4];
-      float d[2][2][4];                                 // [pair element][column][digit]
-      const float tv[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-      for (int m2 = 0; m2 < 4; ++m2) {
-        float r = scale_pow2(tv[m2], k);
-        asum += fabsf(r);
-#pragma unroll
-        for (int b = 0; b < 4; ++b) d[m2 & 1][m2 >> 1][b] = next_digit(r);
-      }
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) out[b][2 * j4 + c2] = pack_digits(d[0][c2][b], d[1][c2][b]);
-    }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) tmem_st8(taddr + 64u * (uint32_t)b + 8u * (uint32_t)blk, out[b]);
-  }
-  return asum;
-}
-
-// One worker warp's rows of a chunk, loaded ahead of slicing.
-struct XPre {
-  uint2 x[kRowsPerWarp];  // this lane's 4 bf16 (k = 4 lane .. 4 lane + 3) of rows R w + j
-  int row, head, b, p;    // lanes 0..R-1: indices of row R w + lane (b, p for cache rows;
-                          // appended rows: b from cu_rows, p found after the dependency wait)
-  int sq;                 // lanes 0..R-1: s_quant[b] (cache rows, loaded after the dependency wait)
-  int valid;              // lanes 0..R-1: the row exists
-};
 
 // after_wait: s_quant may be read (it is written by the previous kernel of a step)
 __device__ __forceinline__ void x_prefetch(const RotParams& P, const RotTensor& T, int mh, int chunk, int pairs,
@@ -318,13 +57,9 @@ __device__ __forceinline__ void x_prefetch(const RotParams& P, const RotTensor& 
   pre.b = pre.p = 0;
   pre.sq = -1;
   if (pre.valid && !T.is_query) {
-    if (P.cu_rows) {
-      pre.b = append_seq(P.cu_rows, P.batch, row);
-    } else {
-      pre.b = __ldg(P.seq_idx + row);
-      pre.p = __ldg(P.pos + row);
-      if (after_wait && pre.b >= 0 && pre.b < P.batch) pre.sq = P.s_quant[pre.b];
-    }
+    pre.b = __ldg(P.seq_idx + row);
+    pre.p = __ldg(P.pos + row);
+    if (after_wait && pre.b >= 0 && pre.b < P.batch) pre.sq = P.s_quant[pre.b];
   }
 #pragma unroll
   for (int j = 0; j < kRowsPerWarp; ++j) {
@@ -339,18 +74,11 @@ __device__ __forceinline__ void x_prefetch(const RotParams& P, const RotTensor& 
 // the dependency wait (destinations read s_quant).
 __device__ __forceinline__ void x_slice(const RotParams& P, const RotTensor& T, const XPre& pre, uint8_t* xb,
                                         UmRow* meta, int warp, int lane) {
-  void* dst = nullptr;
+  uint16_t* dst = nullptr;
   const uint16_t* src = nullptr;
-  int dflags = 0, tp = 0;
   if (pre.valid) {
     src = T.src + ((size_t)pre.row * T.heads + pre.head) * kHeadDim;
-    if (P.cu_rows && !T.is_query) {
-      const int kind = append_dst(P, T, pre.row, pre.head, pre.b, true, dst, tp);
-      dflags = kind == kDstPage ? (kRowLive | kRowPage) : kind == kDstRow ? kRowLive : 0;
-    } else {
-      dst = rot_dst(P, T, pre.row, pre.head, pre.b, pre.p, true, pre.sq);
-      dflags = dst ? kRowLive : 0;
-    }
+    dst = rot_dst(P, T, pre.row, pre.head, pre.b, pre.p, true, pre.sq);
   }
 #pragma unroll
   for (int j = 0; j < kRowsPerWarp; ++j) {
@@ -378,103 +106,31 @@ __device__ __forceinline__ void x_slice(const RotParams& P, const RotTensor& T, 
     for (int a = 0; a < 3; ++a)
       sts_v2(um_saddr(xb) + (uint32_t)(a * kXSlice + offj), pack_digits(d[a][0], d[a][1]),
              pack_digits(d[a][2], d[a][3]));
-    const unsigned long long dj = __shfl_sync(0xffffffffu, (unsigned long long)dst, j);
-    const unsigned long long sj = __shfl_sync(0xffffffffu, (unsigned long long)src, j);
-    const int fj = __shfl_sync(0xffffffffu, dflags, j), tj = __shfl_sync(0xffffffffu, tp, j);
+    uint16_t* dj = (uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)dst, j);
+    const uint16_t* sj = (const uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)src, j);
     if (lane == 0) {
       const uint32_t ma = um_saddr(meta + kRowsPerWarp * warp + j);
-      sts_u64(ma, dj);
-      sts_u64(ma + 8, sj);
-      sts_v2(ma + 16, (uint32_t)fr,
-             (uint32_t)(fj | (zero ? kRowZero : 0) | (bad ? kRowBad : 0) | (lossy ? kRowLossy : 0)));
-      sts_v2(ma + 24, (uint32_t)tj, 0u);
+      sts_u64(ma, (unsigned long long)dj);
+      sts_u64(ma + 8, (unsigned long long)sj);
+      sts_v2(ma + 16, (uint32_t)fr, (uint32_t)((zero ? kRowZero : 0) | (bad ? kRowBad : 0) | (lossy ? kRowLossy : 0)));
     }
   }
 }
 
-// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly (exact.cuh)
-// into the chunk's staged rows; returns 0.
+// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly; returns 0.
+// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly (exact.cuh);
+// returns 0.
 __device__ __noinline__ int exact_list(const uint16_t* list, int count, const UmRow* mrow, const float* tmat,
-                                       uint8_t* stg, int lane) {
+                                       int lane) {
   __syncwarp();
   for (int f = 0; f < count; ++f) {
     const int r = list[f] >> 7, o = list[f] & 127;
-    exact_output_warp(tmat + (size_t)o * kHeadDim, mrow[r].src, reinterpret_cast<uint16_t*>(stg + r * kStgStride), o,
-                      lane);
+    exact_output_warp(tmat + (size_t)o * kHeadDim, mrow[r].src, static_cast<uint16_t*>(mrow[r].dst), o, lane);
   }
   __syncwarp();
   return 0;
 }
 
-// Row phase of a chunk: the octet (lane / 8) of warp w takes staged row 4 w + lane / 8 (a row
-// of the warp's own part), lane j = lane % 8 its channels 16 j .. 16 j + 15.  BF16 destinations get the row with 16-byte
-// stores (8-byte ones when the destination is only 8-byte aligned); page destinations get
-// the quantized token.  The whole warp calls it.
-__device__ __forceinline__ void row_phase(const UmRow* mrow, uint32_t stg_s, const QuantConsts& Qc, bool is_key,
-                                          bool key_norm, int ng, int32_t* status, int warp, int lane) {
-  const int r = 4 * warp + (lane >> 3), j = lane & 7;
-  const uint32_t ma = um_saddr(mrow + r);
-  void* dst = (void*)lds_u64(ma);
-  const int flags = (int)lds_v2(ma + 16).y;
-  const int tp = (int)lds_v2(ma + 24).x;
-  const bool live = (flags & kRowLive) != 0, page = (flags & kRowPage) != 0;
-  // lanes 4..7 of the octet read their upper 16 bytes first, so each quarter-warp's loads
-  // cover the 32 banks once
-  const int first = (j >> 2) & 1;
-  const uint32_t rs = stg_s + (uint32_t)(r * kStgStride + 32 * j);
-  const uint4 a = lds_v4(rs + 16u * (uint32_t)first), c = lds_v4(rs + 16u * (uint32_t)(1 - first));
-  const uint4 lo = first ? c : a, hi = first ? a : c;          // channels 16j..16j+7, 16j+8..16j+15
-  if (live && !page) {
-    uint16_t* d = static_cast<uint16_t*>(dst) + 16 * j;
-    if (((uintptr_t)d & 15u) == 0) {
-      reinterpret_cast<uint4*>(d)[0] = lo;
-      reinterpret_cast<uint4*>(d)[1] = hi;
-    } else {
-      uint2* d2 = reinterpret_cast<uint2*>(d);
-      d2[0] = make_uint2(lo.x, lo.y);
-      d2[1] = make_uint2(lo.z, lo.w);
-      d2[2] = make_uint2(hi.x, hi.y);
-      d2[3] = make_uint2(hi.z, hi.w);
-    }
-  }
-  if (__any_sync(0xffffffffu, page)) {
-    const uint32_t u[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    float y[16];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      y[2 * m] = __uint_as_float(u[m] << 16);
-      y[2 * m + 1] = __uint_as_float(u[m] & 0xffff0000u);
-    }
-    quantize_store_octet(Qc, is_key, key_norm, y, page ? static_cast<uint8_t*>(dst) : nullptr, tp, ng, page, lane,
-                         status);
-  }
-}
-
-// Bounded wait that also gives up when another warp has given up.
-__device__ __noinline__ bool um_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  for (long long it = 0; it < kSpinLimit; ++it) {
-    if (um_mbar_try(bar, parity)) return true;
-    if (*abort_flag) return false;
-  }
-  *abort_flag = 1;
-  return false;
-}
-// The same, decided by lane 0 for the whole warp (so the warp stays converged).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
-  int ok = 0;
-  if (lane == 0) ok = um_wait(bar, parity, abort_flag) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
-}
-__device__ __forceinline__ void um_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(um_saddr(bar)) : "memory");
-}
-
-// Constant part of the bound, units of U_i V_r: T's digits kept to 2^-25 (2^-25 sum |x| <=
-// 2^-11), the digit products dropped ((1,3), (2,2): 2^-11 each; (2,3): 2^-19) and the fp32
-// combination of the levels beyond 3u|v| (2^-17).
-constexpr float kBoundConst = 0x1.9p-10f;
 
 // One CTA per tile: P.rpc chunks of 64 (row, head) pairs that share one matrix.  Warps
 // 0 .. kWorkers - 1 slice rows and decide outputs; the last warp issues the MMAs.
@@ -609,16 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
       publish(1);
       if (nch > 2) x_prefetch(P, T, mh, c0 + 2, pairs, warp, lane, true, pre);
     }
-    const QuantConsts Qc = quant_consts(P.qs[T.which], 16);
-    const bool is_key = T.which == 0, key_norm = T.which == 0 && P.l2 != 0;
     int count = 0;
-    bool dead = false;      // a bounded wait ran out: the warp only keeps meeting the barrier
     for (int n = 0; n < nch; ++n) {
-      uint8_t* stg = sm + kStgOff + (n & 1) * kStgBuf;
-      const uint32_t stg_s = um_saddr(stg);
-      const UmRow* mrow = meta + (n & 3) * kUmRows;
-      if (!dead && !warp_wait(&bar_mma[n & 1], (uint32_t)((n >> 1) & 1), &abort_sh, lane)) dead = true;
-      if (!dead) {
+      if (!warp_wait(&bar_mma[n & 1], (uint32_t)((n >> 1) & 1), &abort_sh, lane)) break;
       tc_fence_after();
       uint32_t acc[4][kEpiRows];
 #pragma unroll
@@ -629,18 +278,19 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
       tc_fence_before();
       __syncwarp();
       if (lane == 0) um_arrive(&bar_acc);
-      // ---- rounding decisions of chunk n: output i, rows kEpiRows part + c, into the staged
-      // rows.  All rows first, without control flow (independent chains the scheduler
-      // interleaves); undecided outputs are queued afterwards, only when the warp has any.
+      // ---- rounding decisions of chunk n: output i, rows kEpiRows part + c ----
+      // All rows first, without control flow (independent chains the scheduler interleaves);
+      // undecided outputs are queued afterwards, only when the warp has any.
+      const UmRow* mrow = meta + (n & 3) * kUmRows;
       const uint32_t mrow_s = um_saddr(mrow);
       uint32_t und_bits = 0;
 #pragma unroll
       for (int c = 0; c < kEpiRows; ++c) {
         const int r = kEpiRows * part + c;
         const uint32_t ma = mrow_s + (uint32_t)r * (uint32_t)sizeof(UmRow);
+        uint16_t* dst = (uint16_t*)lds_u64(ma);
         const uint2 ff = lds_v2(ma + 16);
         const int fr = (int)ff.x, flags = (int)ff.y;
-        const bool live = (flags & kRowLive) != 0;
         const float v = fmaf(__uint_as_float(acc[3][c]), 0x1p-24f,
                              fmaf(__uint_as_float(acc[2][c]), 0x1p-16f,
                                   fmaf(__uint_as_float(acc[1][c]), 0x1p-8f, __uint_as_float(acc[0][c]))));
@@ -655,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
         int b = (decided && (unsigned)(ey - 267) < 254u) ? bu + (ey - 266 - ((bu >> 7) & 0xff)) * 128 : -1;
         b = ((flags & kRowZero) || !tnz) ? 0 : b;           // an exact zero is +0
         b = (force || (flags & kRowBad)) ? -1 : b;
-        if (live && b >= 0) sts_u16(stg_s + (uint32_t)(r * kStgStride + 2 * i), (uint32_t)b);
-        und_bits |= (live && b < 0) ? (1u << c) : 0u;
+        if (dst != nullptr && b >= 0) __stcg(reinterpret_cast<unsigned short*>(dst + i), (unsigned short)b);
+        und_bits |= (dst != nullptr && b < 0) ? (1u << c) : 0u;
       }
       if (__any_sync(0xffffffffu, und_bits != 0u)) {
 #pragma unroll 1
@@ -665,18 +315,12 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
           const unsigned mk = __ballot_sync(0xffffffffu, und);
           if (und) list[count + __popc(mk & ((1u << lane) - 1u))] = (uint16_t)(((kEpiRows * part + c) << 7) | i);
           count += __popc(mk);
-          if (count > kList - 32) count = exact_list(list, count, mrow, tmat, stg, lane);
+          if (count > kList - 32) count = exact_list(list, count, mrow, tmat, lane);
         }
       }
-      count = exact_list(list, count, mrow, tmat, stg, lane);
-      }
-      // ---- the four warps of a part meet here once per chunk (also after a timeout); then the
-      // part's rows of chunk n go out: BF16 rows copied, page rows quantized ----
-      part_sync(part);
-      const int stop = __shfl_sync(0xffffffffu, abort_sh, 0);
-      if (!stop) row_phase(mrow, stg_s, Qc, is_key, key_norm, P.ng, P.status, warp, lane);
+      count = exact_list(list, count, mrow, tmat, lane);
       // ---- digits of chunk n + 2 into chunk n's buffer (its MMAs have completed) ----
-      if (!dead && n + 2 < nch) {
+      if (n + 2 < nch) {
         x_slice(P, T, pre, xbuf(n), meta + ((n + 2) & 3) * kUmRows, warp, lane);
         publish(n + 2);
         if (n + 3 < nch) x_prefetch(P, T, mh, c0 + n + 3, pairs, warp, lane, true, pre);
@@ -798,7 +442,7 @@ __global__ void __launch_bounds__(256, 1) tc_selftest_kernel(unsigned long long*
 
 }  // namespace
 
-int launch_rotate_tc(RotParams P, cudaStream_t stream) {
+int plan_rotate_tc(RotParams& P) {
   // chunks of 64 pairs per matrix; chunks per tile chosen so that the slowest SM's work,
   // ceil(tiles / SMs) x (chunks per tile + one chunk's worth of matrix set-up), is least
   long long chunks_total = 0;
@@ -833,9 +477,14 @@ int launch_rotate_tc(RotParams P, cudaStream_t stream) {
     P.n_dense[t] = (int)tiles;
     dense_total += tiles;
   }
-  if (dense_total == 0) return KVQ_OK;
   if (dense_total > 0x7fffffffLL) return KVQ_ERR_UNSUPPORTED;
   P.dense_total = (int)dense_total;
+  return KVQ_OK;
+}
+
+int launch_rotate_tc(RotParams P, cudaStream_t stream) {
+  const int rc = plan_rotate_tc(P);
+  if (rc != KVQ_OK || P.dense_total == 0) return rc;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
   static std::mutex mu;
@@ -843,12 +492,14 @@ int launch_rotate_tc(RotParams P, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!(attr_done & (1ull << dev))) {
-      if (cudaFuncSetAttribute(rotate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmSmem) != cudaSuccess)
+      if (cudaFuncSetAttribute(rotate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmSmemPlain) !=
+          cudaSuccess)
         return KVQ_ERR_CUDA;
       attr_done |= 1ull << dev;
     }
   }
-  return launch_pdl(rotate_tc_kernel, dim3((unsigned)dense_total), dim3(kThreads), (size_t)kUmSmem, stream, P) ==
+  return launch_pdl(rotate_tc_kernel, dim3((unsigned)P.dense_total), dim3(kThreads), (size_t)kUmSmemPlain, stream,
+                    P) ==
                  cudaSuccess
              ? KVQ_OK
              : KVQ_ERR_CUDA;
