@@ -35,15 +35,21 @@ def flush(L: int, s_quant: int, s_keep: int, s_flush: int) -> int:
 
 def build_unit(k_rot_bits: np.ndarray, v_rot_bits: np.ndarray, L: int, s_quant: int, *,
                s_sink: int, group: int, kappa_k: float, kappa_v: float,
-               quantizer: str = "affine", alpha: float = 1.4935705, key_l2norm: bool = False) -> dict:
+               quantizer: str = "affine", alpha: float = 1.4935705, key_l2norm: bool = False,
+               key_axis: str = "token", key_block: int = 16) -> dict:
     """The cache of one (sequence, kv head) holding tokens [0, L) with INT2 region [S_sink, s_quant).
 
     k_rot_bits / v_rot_bits: transformed BF16 rows [>= L, d] (bit patterns).
-    Per-token groups make a token's codes independent of when it was flushed.
+    Per-token groups make a token's codes independent of when it was flushed.  Per-channel
+    keys (key_axis "channel", [OScaR] algorithm, key processing) take blocks of key_block tokens from
+    S_sink on; the flush spans are then whole blocks, so a block is quantized once, complete.
     """
     lo = min(s_sink, L)
     hi = max(lo, min(s_quant, L))
-    qk = quant.quantize_rows(k_rot_bits[lo:hi], group, kappa_k, quantizer, alpha, key_l2norm)
+    if key_axis == "channel":
+        qk = quant.quantize_keys_per_channel(k_rot_bits[lo:hi], key_block, kappa_k, key_l2norm)
+    else:
+        qk = quant.quantize_rows(k_rot_bits[lo:hi], group, kappa_k, quantizer, alpha, key_l2norm)
     qv = quant.quantize_rows(v_rot_bits[lo:hi], group, kappa_v, quantizer, alpha, False)
     return {"L": L, "s_sink": lo, "s_quant": hi, "k_rot": k_rot_bits[:L], "v_rot": v_rot_bits[:L],
             "qk": qk, "qv": qv}

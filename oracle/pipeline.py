@@ -57,7 +57,7 @@ def run_unit(w, ui, tk, tkit, tv, scale: float | None = None, attend: bool = Tru
     L = ui.ctx + w.n_new
     unit = cache.build_unit(k_rot, v_rot, L, sq1, s_sink=w.s_sink, group=w.group_size,
                             kappa_k=w.kappa_k, kappa_v=w.kappa_v, quantizer=w.quantizer,
-                            alpha=w.quest_alpha, key_l2norm=w.key_l2norm)
+                            alpha=w.quest_alpha, key_l2norm=w.key_l2norm, key_axis=w.key_axis)
     res = {"k_rot": k_rot, "v_rot": v_rot, "q_rot": q_rot, "s_quant_before": sq0,
            "s_quant": sq1, "L": L, "unit": unit}
     if attend:

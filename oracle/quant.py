@@ -139,17 +139,59 @@ def quantize_rows(x_bits: np.ndarray, group: int, kappa: float = 1.0, quantizer:
 
 
 def dequantize(q: dict) -> np.ndarray:
-    """x_hat = s16 * Delta16 * (c - z16) in float64, [n, d] ([OScaR] "步骤二" dequantisation)."""
+    """x_hat = s16 * Delta16 * (c - z16) in float64, [n, d] ([OScaR] "步骤二" dequantisation;
+    the OScaR algorithm's attention part for per-channel keys: k_hat_t = s_t Delta (Q(k_t) - z))."""
     c = q["codes"].astype(np.float64)
     n, d = c.shape
-    ng = q["delta16"].shape[-1]
-    g = d // ng
     dd = q["delta16"].astype(np.float64)
     zz = q["zero16"].astype(np.float64)
-    xh = (dd[..., None] * (c.reshape(n, ng, g) - zz[..., None])).reshape(n, d)
+    if q.get("axis") == "channel":
+        blk = q["block"]
+        xh = (dd[:, None, :] * (c.reshape(n // blk, blk, d) - zz[:, None, :])).reshape(n, d)
+    else:
+        ng = q["delta16"].shape[-1]
+        g = d // ng
+        xh = (dd[..., None] * (c.reshape(n, ng, g) - zz[..., None])).reshape(n, d)
     if q.get("norm16") is not None:
         xh = xh * q["norm16"].astype(np.float64)[:, None]
     return xh
+
+
+def quantize_keys_per_channel(x_bits: np.ndarray, block: int, kappa: float = 1.0, l2: bool = False) -> dict:
+    """KIVI's per-channel key quantization of BF16 rows x_bits [n, d] (bit patterns).
+
+    [OScaR] "背景：KIVI 与逐通道量化范式" and "理论分析：TNI 如何破坏逐通道量化": a block of G
+    consecutive tokens, and for channel j the block's G values K_{1,j} .. K_{G,j} give
+    Delta_{j,g} = (max - min)/(2^b - 1), z_{j,g} = -min/Delta_{j,g}, Q and K_hat as for
+    per-token groups; [OScaR] algorithm, key processing: the buffered, l2-scaled keys are
+    quantized per channel in blocks when the residual buffer is full.  Here the block is `block` tokens (n a multiple of it; block b holds
+    rows [b*block, (b+1)*block)), the optional l2 token scaling comes first (as in
+    quantize_rows), and the range, Delta16 / z16 and code steps are those of the per-token
+    groups (two-sided kappa-quantile, kappa = 1 giving min / max) applied to channel j's
+    `block` values instead of a token's G channels.
+
+    Returns codes [n, d] uint8, delta16 / zero16 [n/block, d] float16 (per block and
+    channel), norm16 [n] float16 (or None) and a per-block flag for non-finite scale data.
+    """
+    x = bf16_to_f32(x_bits)
+    n, d = x.shape
+    if n % block:
+        raise ValueError("the rows must be whole blocks")
+    norm16 = None
+    y = x
+    if l2:
+        y, norm16 = l2_scale(x)
+    # [blocks, channels, tokens of the block]: one group per (block, channel)
+    yc = np.swapaxes(y.reshape(n // block, block, d), 1, 2)
+    lo, hi = group_range(yc, kappa)
+    d16, z16 = affine_params(lo, hi)
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        c = np.swapaxes(codes_from_params(yc, d16, z16), 1, 2).reshape(n, d)
+    bad = ~np.isfinite(d16.astype(np.float64)).all(-1) | ~np.isfinite(z16.astype(np.float64)).all(-1)
+    if norm16 is not None:
+        bad |= ~np.isfinite(norm16.astype(np.float64)).reshape(n // block, block).all(-1)
+    return {"codes": c, "delta16": d16, "zero16": z16, "norm16": norm16, "nonfinite": bad,
+            "axis": "channel", "block": block}
 
 
 def pack_lsb(codes: np.ndarray) -> np.ndarray:

@@ -75,6 +75,7 @@ class Workload:
     quantizer: str = "affine"          # "affine" (kappa-quantile clipped) | "quest"
     quest_alpha: float = 1.4935705     # outer level (in RMS units) of the MSE-optimal uniform 4-level quantizer of N(0,1)
     key_l2norm: bool = False
+    key_axis: str = "token"            # "token" (groups of G channels per token) | "channel" (per channel per page)
     s_sink: int = 64
     s_keep: int = 256
     s_flush: int = 8
