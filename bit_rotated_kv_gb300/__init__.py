@@ -35,6 +35,8 @@ KVQ_QUANT_AFFINE_KAPPA = 0
 KVQ_QUANT_QUEST_RMS = 1
 KVQ_TRANSFORM_DENSE = 0
 KVQ_TRANSFORM_HADAMARD = 1
+KVQ_KEY_PER_TOKEN = 0
+KVQ_KEY_PER_CHANNEL = 1
 
 EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_append_chunk", "kv_attn_decode", "kv_attn_decode_bf16", "kv_attn_decode_noalloc",
             "kv_attn_workspace_bytes",
@@ -46,7 +48,7 @@ class CConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "head_dim", "n_q_heads", "n_kv_heads", "page_size", "group_size", "quantizer", "key_l2norm",
         "s_sink", "s_keep", "s_flush", "ring_cap", "batch", "max_pages_per_seq", "num_pages",
-        "attn_splits", "reserved")] + [("kappa_k", ctypes.c_double), ("kappa_v", ctypes.c_double),
+        "attn_splits", "key_axis")] + [("kappa_k", ctypes.c_double), ("kappa_v", ctypes.c_double),
                                        ("quest_alpha", ctypes.c_double)]
 
 
@@ -139,6 +141,7 @@ class KVConfig:
     kappa_k: float = 0.99
     kappa_v: float = 0.99
     quest_alpha: float = 1.4935705
+    key_axis: int = 0                    # KVQ_KEY_PER_TOKEN / KVQ_KEY_PER_CHANNEL
 
     def __setattr__(self, name, value):
         object.__setattr__(self, name, value)
@@ -152,7 +155,7 @@ class KVConfig:
             cc = CConfig(self.head_dim, self.n_q_heads, self.n_kv_heads, self.page_size, self.group_size,
                          self.quantizer, int(bool(self.key_l2norm)), self.s_sink, self.s_keep, self.s_flush,
                          self.ring_cap, self.batch, self.max_pages_per_seq, self.num_pages, self.attn_splits,
-                         0, float(self.kappa_k), float(self.kappa_v), float(self.quest_alpha))
+                         int(self.key_axis), float(self.kappa_k), float(self.kappa_v), float(self.quest_alpha))
             object.__setattr__(self, "_cc", cc)
         return cc
 

@@ -18,6 +18,9 @@ int check_config(const kvq_config* c) {
   if (g != 1 && g != 2 && g != 4 && g != 8) return KVQ_ERR_UNSUPPORTED;
   if (c->quantizer != KVQ_QUANT_AFFINE_KAPPA && c->quantizer != KVQ_QUANT_QUEST_RMS) return KVQ_ERR_INVALID_ARG;
   if (c->quantizer == KVQ_QUANT_QUEST_RMS && c->key_l2norm) return KVQ_ERR_UNSUPPORTED;
+  if (c->key_axis != KVQ_KEY_PER_TOKEN && c->key_axis != KVQ_KEY_PER_CHANNEL) return KVQ_ERR_INVALID_ARG;
+  if (c->key_axis == KVQ_KEY_PER_CHANNEL && (c->quantizer != KVQ_QUANT_AFFINE_KAPPA || c->s_flush % kPage))
+    return KVQ_ERR_UNSUPPORTED;
   if (c->key_l2norm != 0 && c->key_l2norm != 1) return KVQ_ERR_INVALID_ARG;
   if (!(c->kappa_k >= 0.5 && c->kappa_k <= 1.0) || !(c->kappa_v >= 0.5 && c->kappa_v <= 1.0))
     return KVQ_ERR_INVALID_ARG;
@@ -72,12 +75,12 @@ KVQ_API const char* kvq_status_string(int code) {
 
 KVQ_API size_t kvq_page_head_bytes(const kvq_config* cfg) {
   if (check_config(cfg) != KVQ_OK) return 0;
-  return (size_t)page_head_bytes(cfg->group_size, cfg->key_l2norm);
+  return (size_t)page_head_bytes(cfg->group_size, cfg->key_l2norm, cfg->key_axis);
 }
 
 KVQ_API size_t kvq_page_bytes(const kvq_config* cfg) {
   if (check_config(cfg) != KVQ_OK) return 0;
-  return (size_t)page_head_bytes(cfg->group_size, cfg->key_l2norm) * cfg->n_kv_heads;
+  return (size_t)page_head_bytes(cfg->group_size, cfg->key_l2norm, cfg->key_axis) * cfg->n_kv_heads;
 }
 
 KVQ_API size_t kv_attn_workspace_bytes(const kvq_config* cfg, int32_t max_ctx) {
@@ -129,7 +132,7 @@ KVQ_API int kv_append_chunk(const kvq_config* cfg, const kvq_transform* tr, cons
   rc = check_cache(cfg, cache);
   if (rc) return rc;
   if (!tr || (tr->kind != KVQ_TRANSFORM_DENSE && tr->kind != KVQ_TRANSFORM_HADAMARD)) return KVQ_ERR_INVALID_ARG;
-  if (tr->kind == KVQ_TRANSFORM_HADAMARD) return KVQ_ERR_UNSUPPORTED;
+  if (tr->kind == KVQ_TRANSFORM_HADAMARD || cfg->key_axis != KVQ_KEY_PER_TOKEN) return KVQ_ERR_UNSUPPORTED;
   if (n_rows < 0 || !cu_rows || !aligned(cu_rows, 4)) return KVQ_ERR_INVALID_ARG;
   if (n_rows > 0) {
     if (!k || !v || !aligned(k, 16) || !aligned(v, 16)) return KVQ_ERR_INVALID_ARG;

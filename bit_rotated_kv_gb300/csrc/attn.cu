@@ -279,7 +279,7 @@ __device__ __forceinline__ uint32_t dz_operand(uint32_t dz, bool odd) {
   return odd ? (lo & 0xffffu) : hi;
 }
 
-template <int NG, bool L2>
+template <int NG, bool L2, bool KC>
 __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int split, float* res,
                            size_t wstride) {
   // accumulators per group; with one group the k-steps alternate between two accumulators so
@@ -313,7 +313,9 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [kWarps][kStages]
   int* slot_pid = reinterpret_cast<int*>(smem + kWarps * kStages * 8);     // [kWarps][kStages]
   QShared* qs = reinterpret_cast<QShared*>(smem + kWarps * kStages * 12);
-  constexpr int pb = (2 * kCodeBytes + 2 * kPage * NG * 4 + (L2 ? kPage * 2 : 0) + 31) / 32 * 32;
+  // page bytes: KC (per-channel keys) carries d key Delta16 + d key z16 and the exponent E
+  constexpr int pb = (2 * kCodeBytes + (KC ? 4 * kHeadDim : kPage * NG * 4) + kPage * NG * 4 + (L2 ? kPage * 2 : 0) +
+                      (KC ? 4 : 0) + 31) / 32 * 32;
   uint8_t* my_ring = smem + 1024 + (size_t)warp * kStages * pb;            // [kStages][page_bytes]
   uint64_t* my_bars = bars + warp * kStages;
   int* my_pid = slot_pid + warp * kStages;
@@ -449,15 +451,76 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   // per-lane offsets inside a page (all loads of a page are base + these)
   const uint32_t off_code = 16u * lane;
   const uint32_t off_sk = (uint32_t)(k_scale_off() + tA * NG * 4);
-  const uint32_t off_dv = (uint32_t)v_delta_off(NG, 2 * quad, 0);
-  const uint32_t off_zg = (uint32_t)v_delta_off(NG, 2 * quad, hrow < NG ? hrow : 0);
-  const uint32_t off_nrm = (uint32_t)(norm_off(NG) + 2 * tA);
+  const uint32_t off_dv = (uint32_t)v_delta_off(NG, 2 * quad, 0, KC);
+  const uint32_t off_zg = (uint32_t)v_delta_off(NG, 2 * quad, hrow < NG ? hrow : 0, KC);
+  const uint32_t off_nrm = (uint32_t)(norm_off(NG, KC) + 2 * tA);
+  // per-channel keys: this quad's 16 Delta16 / z16 pairs (k-step s, half h at pair 2 s + h)
+  const uint32_t off_kd = (uint32_t)(kc_delta_off() + 64 * quad);
+  const uint32_t off_kz = (uint32_t)(kc_zero_off() + 64 * quad);
+  const uint32_t off_ke = (uint32_t)kc_exp_off(NG, L2);
   const uint32_t ring_s = smem_u32(my_ring);
 
   // ---- one page, split in three parts so that two pages can share the softmax bookkeeping and
   // the loop overhead: scores (kside), lazy maximum (softmax), P V (vside)
   auto kside = [&](uint32_t sa, float (&sc)[4]) {
     const uint4 wk = lds128(sa + off_code);
+    if constexpr (KC) {
+      // ---- per-channel keys: s = sum_j q'_j Delta_j (c_j - z_j).  The page's Delta_j, scaled by
+      // 2^-E (E the exponent of its largest Delta, so Delta 2^-E < 2), go into the B operand as
+      // an exact fp16 pair B_hi + B_lo = q' 2^(sigma - 2p) Delta 2^-E (the product of two fp16
+      // values has 22 bits; the fused HFMA2 gives the remainder exactly), so every MMA product
+      // is exact as on the per-token path.  The zero-point term takes the same pair times 4^p
+      // (exact) against A = z_j, every token row alike, in its own accumulator.
+      const uint32_t kw[4] = {wk.x, wk.y, wk.z, wk.w};
+      const uint32_t kw10[4] = {wk.x >> 10, wk.y >> 10, wk.z >> 10, wk.w >> 10};
+      const int E = (int)lds32(sa + off_ke);
+      const uint32_t se = E <= 14 ? (uint32_t)(15 - E) << 10 : 0x0200u;    // 2^-E, E in [-14, 15]
+      const uint32_t s2 = se | (se << 16);
+      float acc[2][4], accz[4];
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const uint4 dq = lds128(sa + off_kd + 16 * s4), zq = lds128(sa + off_kz + 16 * s4);
+        const uint32_t dd[4] = {dq.x, dq.y, dq.z, dq.w}, zz[4] = {zq.x, zq.y, zq.z, zq.w};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int s = 2 * s4 + j;
+          const uint32_t d0 = hmul2_bits(dd[2 * j], s2), d1 = hmul2_bits(dd[2 * j + 1], s2);
+          const uint32_t h0 = hmul2_bits(bq[s][0], d0), h1 = hmul2_bits(bq[s][1], d1);
+          const uint32_t l0 = hfma2_neg_bits(bq[s][0], d0, h0), l1 = hfma2_neg_bits(bq[s][1], d1, h1);
+          uint32_t a[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) a[r] = code_pair(kw[r], kw10[r], s);
+          if (s < 2) mma_f16_z(acc[s & 1], a, h0, h1);
+          else mma_f16(acc[s & 1], a, h0, h1);
+          mma_f16(acc[s & 1], a, l0, l1);
+          const uint32_t p4 = (uint32_t)(15 + 2 * slot_pow(s)) << 10;        // 4^p in fp16
+          const uint32_t p4x2 = p4 | (p4 << 16);
+          const uint32_t az[4] = {zz[2 * j], zz[2 * j], zz[2 * j + 1], zz[2 * j + 1]};
+          if (s == 0) mma_f16_z(accz, az, hmul2_bits(h0, p4x2), hmul2_bits(h1, p4x2));
+          else mma_f16(accz, az, hmul2_bits(h0, p4x2), hmul2_bits(h1, p4x2));
+          mma_f16(accz, az, hmul2_bits(l0, p4x2), hmul2_bits(l1, p4x2));
+        }
+      }
+      const float mE = __int_as_float((E + 127) << 23);                     // 2^E
+      float sum[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) sum[i] = __fmaf_rn(accz[i], -0x1p-24f, acc[0][i] + acc[1][i]);
+      const float mA = multA * mE, mB = multB * mE;
+      if constexpr (L2) {
+        const float nA = __half2float(__ushort_as_half((unsigned short)lds16(sa + off_nrm)));
+        const float nB = __half2float(__ushort_as_half((unsigned short)lds16(sa + off_nrm + 16)));
+        sc[0] = sum[0] * (mA * nA);
+        sc[1] = sum[1] * (mB * nA);
+        sc[2] = sum[2] * (mA * nB);
+        sc[3] = sum[3] * (mB * nB);
+      } else {
+        sc[0] = sum[0] * mA;
+        sc[1] = sum[1] * mB;
+        sc[2] = sum[2] * mA;
+        sc[3] = sum[3] * mB;
+      }
+      return;
+    }
     uint32_t skA[NG], skB[NG];
     lds_scales<NG>(sa + off_sk, skA);
     lds_scales<NG>(sa + off_sk + 32 * NG, skB);
@@ -985,9 +1048,9 @@ __device__ __noinline__ void merge_global(const float* src, int n, int g, void* 
   }
 }
 
-// One kernel per (groups per row, key norms) variant, so that each launch's code is only its own
-// page loop (a short loop per warp is sensitive to instruction-fetch misses).
-template <int NG, bool L2>
+// One kernel per (groups per row, key norms, per-channel keys) variant, so that each launch's
+// code is only its own page loop (a short loop per warp is sensitive to instruction-fetch misses).
+template <int NG, bool L2, bool KC>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const AttnParams Pk) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_trigger();
@@ -1007,7 +1070,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const
   size_t wstride;
   if (split < P.n_int2) {
     wstride = (size_t)kStages * P.page_bytes / sizeof(float);
-    int2_split<NG, L2>(P, smem, b, h, split, res, wstride);
+    int2_split<NG, L2, KC>(P, smem, b, h, split, res, wstride);
   } else {
     wstride = (size_t)g * kRow;
     window_split(P, b, h, split - P.n_int2, res, wstride);
@@ -1125,7 +1188,7 @@ static int kvq_attn_pages(const kvq_config* cfg, int32_t max_ctx) {
 extern "C" void kvq_attn_splits(const kvq_config* cfg, int32_t max_ctx, int* n_int2, int* n_win) {
   const long long units = (long long)cfg->batch * cfg->n_kv_heads;
   const int pages = kvq_attn_pages(cfg, max_ctx);
-  const long long pb = page_head_bytes(cfg->group_size, cfg->key_l2norm);
+  const long long pb = page_head_bytes(cfg->group_size, cfg->key_l2norm, cfg->key_axis);
   const long long tile_b = (long long)kPage * kHeadDim * 2 * 2;
   const long long wtiles = (cfg->s_sink + kPage - 1) / kPage + (cfg->s_keep + cfg->s_flush + kPage - 1) / kPage + 1;
   const double wbytes = (double)wtiles * tile_b, ibytes = (double)pages * pb;
@@ -1192,7 +1255,7 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
   P.num_pages = cfg->num_pages;
   P.group = cfg->group_size;
   P.l2 = cfg->key_l2norm;
-  P.page_bytes = page_head_bytes(cfg->group_size, cfg->key_l2norm);
+  P.page_bytes = page_head_bytes(cfg->group_size, cfg->key_l2norm, cfg->key_axis);
   kvq_attn_splits(cfg, max_ctx, &P.n_int2, &P.n_win);
   P.n_split = P.n_int2 + P.n_win;
   P.mp = kvq_attn_pages(cfg, max_ctx);
@@ -1209,19 +1272,26 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
   size_t smem = 1024 + (ring_bytes > res_bytes ? ring_bytes : res_bytes);
   if (P.merge1 && 1024 + merge_bytes > smem) smem = 1024 + merge_bytes;
   void (*kern)(const AttnParams) = nullptr;
-  int vi = 0;
-  if (cfg->key_l2norm) {
-    kern = ng == 1 ? attn_decode_kernel<1, true> : ng == 2 ? attn_decode_kernel<2, true> : attn_decode_kernel<4, true>;
-    vi = ng == 1 ? 3 : ng == 2 ? 4 : 5;
+  const int vi = (ng == 1 ? 0 : ng == 2 ? 1 : 2) + (cfg->key_l2norm ? 3 : 0) + (cfg->key_axis ? 6 : 0);
+  if (cfg->key_axis == KVQ_KEY_PER_CHANNEL) {
+    if (cfg->key_l2norm)
+      kern = ng == 1 ? attn_decode_kernel<1, true, true> : ng == 2 ? attn_decode_kernel<2, true, true>
+                                                                  : attn_decode_kernel<4, true, true>;
+    else
+      kern = ng == 1 ? attn_decode_kernel<1, false, true> : ng == 2 ? attn_decode_kernel<2, false, true>
+                                                                   : attn_decode_kernel<4, false, true>;
+  } else if (cfg->key_l2norm) {
+    kern = ng == 1 ? attn_decode_kernel<1, true, false> : ng == 2 ? attn_decode_kernel<2, true, false>
+                                                                 : attn_decode_kernel<4, true, false>;
   } else {
-    kern = ng == 1 ? attn_decode_kernel<1, false> : ng == 2 ? attn_decode_kernel<2, false> : attn_decode_kernel<4, false>;
-    vi = ng == 1 ? 0 : ng == 2 ? 1 : 2;
+    kern = ng == 1 ? attn_decode_kernel<1, false, false> : ng == 2 ? attn_decode_kernel<2, false, false>
+                                                                  : attn_decode_kernel<4, false, false>;
   }
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ERR_CUDA;
   // the dynamic shared-memory limit is raised once per (device, kernel variant)
   static std::mutex mu;
-  static unsigned long long attr_done[6] = {};
+  static unsigned long long attr_done[12] = {};
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!(attr_done[vi] & (1ull << dev))) {

@@ -486,7 +486,7 @@ extern "C" int kvq_launch_append(const kvq_config* cfg, const kvq_transform* tr,
   P.page_table = cache->page_table;
   P.max_pages = cfg->max_pages_per_seq;
   P.num_pages = cfg->num_pages;
-  P.page_bytes = page_head_bytes(cfg->group_size, cfg->key_l2norm);
+  P.page_bytes = page_head_bytes(cfg->group_size, cfg->key_l2norm, cfg->key_axis);
   P.ng = kHeadDim / cfg->group_size;
   P.l2 = cfg->key_l2norm;
   P.qs[0] = make_quant_spec(cfg->group_size, cfg->quantizer, cfg->kappa_k, cfg->quest_alpha);

@@ -17,21 +17,38 @@ constexpr int kMaxGqa = 8;
 constexpr int kSms = 152;          // SMs of one GB300 (two dies of 76): launch shapes aim at waves of it
 
 // Bytes of one (page, kv head) chunk: K codes, V codes, K scales, V scales, [K norms],
-// padded to 32 bytes.
-__host__ __device__ inline int page_head_bytes(int group_size, int key_l2norm) {
+// [per-channel keys: the exponent E of the largest key Delta], padded to 32 bytes.  Key
+// scales: per token (16 tokens x d/G (Delta16, z16) pairs) or per channel (d Delta16, then
+// d z16, each in the decode's B-fragment order).
+__host__ __device__ inline int key_scale_bytes(int ng, int key_axis) {
+  return key_axis ? 2 * kHeadDim * 2 : kPage * ng * 4;
+}
+__host__ __device__ inline int page_head_bytes(int group_size, int key_l2norm, int key_axis = 0) {
   int ng = kHeadDim / group_size;
-  int b = 2 * kCodeBytes + 2 * kPage * ng * 4 + (key_l2norm ? kPage * 2 : 0);
+  int b = 2 * kCodeBytes + key_scale_bytes(ng, key_axis) + kPage * ng * 4 + (key_l2norm ? kPage * 2 : 0) +
+          (key_axis ? 4 : 0);
   return (b + 31) / 32 * 32;
 }
 __host__ __device__ inline int k_scale_off() { return 2 * kCodeBytes; }
-__host__ __device__ inline int v_scale_off(int ng) { return 2 * kCodeBytes + kPage * ng * 4; }
-__host__ __device__ inline int norm_off(int ng) { return 2 * kCodeBytes + 2 * kPage * ng * 4; }
+// per-channel keys: Delta16 and z16 pairs, pair 16 q + 2 s + h = channels 16 s + 8 h + 2 q, + 1
+__host__ __device__ inline int kc_delta_off() { return 2 * kCodeBytes; }
+__host__ __device__ inline int kc_zero_off() { return 2 * kCodeBytes + kHeadDim * 2; }
+__host__ __device__ inline int kc_pair_index(int channel) {     // channel even
+  return 16 * ((channel & 7) >> 1) + 2 * (channel >> 4) + ((channel >> 3) & 1);
+}
+__host__ __device__ inline int v_scale_off(int ng, int key_axis = 0) {
+  return 2 * kCodeBytes + key_scale_bytes(ng, key_axis);
+}
+__host__ __device__ inline int norm_off(int ng, int key_axis = 0) { return v_scale_off(ng, key_axis) + kPage * ng * 4; }
+__host__ __device__ inline int kc_exp_off(int ng, int key_l2norm) { return norm_off(ng, 1) + (key_l2norm ? kPage * 2 : 0); }
 // Value scales: Delta16 then z16, each laid out [token pair][group][2 tokens] (fp16), so one
 // load gives the two tokens (2i, 2i+1) of every group.
-__host__ __device__ inline int v_delta_off(int ng, int tp, int g) {
-  return v_scale_off(ng) + (((tp >> 1) * ng + g) * 2 + (tp & 1)) * 2;
+__host__ __device__ inline int v_delta_off(int ng, int tp, int g, int key_axis = 0) {
+  return v_scale_off(ng, key_axis) + (((tp >> 1) * ng + g) * 2 + (tp & 1)) * 2;
 }
-__host__ __device__ inline int v_zero_off(int ng, int tp, int g) { return v_delta_off(ng, tp, g) + kPage * ng * 2; }
+__host__ __device__ inline int v_zero_off(int ng, int tp, int g, int key_axis = 0) {
+  return v_delta_off(ng, tp, g, key_axis) + kPage * ng * 2;
+}
 
 // First device fault wins; never traps.
 __device__ __forceinline__ void set_status(int32_t* st, int code) {

@@ -45,6 +45,9 @@ struct FlushParams {
   int i_lo[2], i_hi[2], n_lo[2], n_hi[2];   // [0] keys, [1] values
   float f_lo[2], f_hi[2];
   double alpha;
+  // per-channel keys: quantile positions among the 16 values of a channel in a page
+  int key_axis, kc_i_lo, kc_i_hi;
+  float kc_f_lo, kc_f_hi;
 };
 
 __device__ __forceinline__ void sort4(float& a, float& b, float& c, float& d) {
@@ -248,8 +251,11 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   // quantized.
   const int n_items = n * P.hkv * 2;
   const int i0 = blockIdx.x * P.items_per_cta;
-  // an append's grid covers the usual ring occupancy; the last CTA takes whatever is beyond
-  const int i1 = (P.cu_rows && blockIdx.x == gridDim.x - 1) ? n_items : min(n_items, i0 + P.items_per_cta);
+  // an append's grid covers the usual ring occupancy; the last CTA takes whatever is beyond;
+  // per-channel keys are quantized by their own kernel (the key warps have nothing to do)
+  const int i1 = ((warp & 1) == 0 && P.key_axis) ? i0
+                 : (P.cu_rows && blockIdx.x == gridDim.x - 1) ? n_items
+                                                              : min(n_items, i0 + P.items_per_cta);
   const int which = warp & 1;
   const uint16_t* ring = which ? P.ring_v : P.ring_k;
   const int hkv = P.hkv, rcap = P.ring_cap, dh = nwarps >> 1;
@@ -333,8 +339,8 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
       if (which == 0) {
         *reinterpret_cast<__half2*>(chunk + k_scale_off() + (tp * ng + g) * 4) = dz;
       } else {
-        *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g)) = __low2half(dz);
-        *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g)) = __high2half(dz);
+        *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g, P.key_axis)) = __low2half(dz);
+        *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g, P.key_axis)) = __high2half(dz);
       }
     }
     // Pack the codes with shuffles.  Lane l holds channels 4l..4l+3; with s = l / 4 its pairs
@@ -376,6 +382,191 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
     flush_publish(P, b, sq, n_adv, L_new);
     P.counters[b] = 0;
   }
+}
+
+// ---- per-channel keys: one warp per (page, kv head) of the flush span -------------------------
+// Lane l owns channels 4l .. 4l+3 of the page's 16 tokens, so each channel's 16 values sit in
+// one lane: its range, Delta16, z16 and codes need no other lane.  The token norms (l2 keys)
+// are summed by a reduce-scatter whose additions are those of the one-row flush's butterfly
+// (partners 16, 8, 4, 2, 1 in that order), so the norms equal the per-token path's bit for bit.
+// Runs before the value flush of the same call, which publishes s_quant: both see the same
+// span.  Source: OScaR reading note, "背景：KIVI 与逐通道量化范式" (Delta_{j,g}, z_{j,g} over a
+// block of tokens) and the algorithm's key processing (l2-scaled keys quantized per channel).
+__global__ void __launch_bounds__(128) flush_keys_channel_kernel(const FlushParams Pk) {
+  pdl_trigger();
+  __shared__ FlushParams Ps;
+  if (threadIdx.x == 0) Ps = Pk;
+  __syncthreads();
+  const FlushParams& P = Ps;
+  const int b = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();
+  const int L = P.seq_len[b], sq = P.s_quant[b];
+  int n, n_adv, L_new;
+  flush_span(P, b, L, sq, false, n, n_adv, L_new);      // the value flush reports bad states
+  const int item = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (item >= (n / kPage) * P.hkv) return;
+  const int pi = item / P.hkv, h = item - pi * P.hkv;
+  const int tok0 = sq + kPage * pi;
+  const int lp = tok0 - P.s_sink;
+  const int pidx = lp >> 4;
+  const int pid = (pidx < P.max_pages) ? P.page_table[(size_t)b * P.max_pages + pidx] : -1;
+  if (pid < 0 || pid >= P.num_pages || (lp & (kPage - 1))) {
+    if (lane == 0) set_status(P.status, KVQ_ERR_BOUNDS);
+    return;
+  }
+  const int ng = kHeadDim / P.group;
+  uint8_t* chunk = P.pages + ((size_t)pid * P.hkv + h) * P.page_bytes;
+  const uint16_t* ring = P.ring_k + ((size_t)b * P.hkv + h) * P.ring_cap * kHeadDim + 4 * lane;
+  float y[kPage][4];
+#pragma unroll
+  for (int t = 0; t < kPage; ++t) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(ring + (size_t)((tok0 + t) % P.ring_cap) * kHeadDim);
+    y[t][0] = __uint_as_float(raw.x << 16);
+    y[t][1] = __uint_as_float(raw.x & 0xffff0000u);
+    y[t][2] = __uint_as_float(raw.y << 16);
+    y[t][3] = __uint_as_float(raw.y & 0xffff0000u);
+  }
+  bool bad = false;
+  if (P.l2) {
+    // sums of squares: lane l ends with token (l >> 1) & 15 (both lanes of a pair)
+    double v[kPage];
+#pragma unroll
+    for (int t = 0; t < kPage; ++t) {
+      double ss = 0.0;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) ss = __dadd_rn(ss, __dmul_rn((double)y[t][m], (double)y[t][m]));
+      v[t] = ss;
+    }
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+      const int o = 16 >> st, half = 8 >> st;
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const double send = up ? v[i] : v[half + i];
+        const double keep = up ? v[half + i] : v[i];
+        v[i] = __dadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+      }
+    }
+    const double ss = __dadd_rn(v[0], __shfl_xor_sync(0xffffffffu, v[0], 1));
+    const __half s16 = double_to_half_rn(__dsqrt_rn(ss));
+    const float sf_mine = __half2float(s16);
+    if (!isfinite(sf_mine)) bad = true;
+    if ((lane & 1) == 0) reinterpret_cast<__half*>(chunk + norm_off(ng, 1))[lane >> 1] = s16;
+    const uint32_t s16b = __half_as_ushort(s16);
+#pragma unroll
+    for (int t = 0; t < kPage; ++t) {
+      const float sf = __half2float(__ushort_as_half((unsigned short)__shfl_sync(0xffffffffu, s16b, 2 * t)));
+      const float sdiv = sf == 0.0f ? 1.0f : sf;
+      float yn[4];
+      div4_by_scale(y[t], sdiv, yn);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) y[t][m] = sf == 0.0f ? 0.0f : yn[m];
+    }
+  }
+  const int s = lane >> 2;                               // the lane's 16-channel block
+  uint32_t W[kPage][2];                                  // key words 2 (lane & 3) + k' of each token
+#pragma unroll
+  for (int t = 0; t < kPage; ++t) W[t][0] = W[t][1] = 0u;
+  uint32_t dpair[2] = {0u, 0u}, zpair[2] = {0u, 0u};
+  int emax = -14;
+  const bool minmax = P.kc_i_hi >= kPage - 1 && P.kc_i_lo == 0 && P.kc_f_lo == 0.0f;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    float v[kPage];
+#pragma unroll
+    for (int t = 0; t < kPage; ++t) v[t] = y[t][m];
+    float hi, lo;
+    if (minmax) {
+      hi = lo = v[0];
+#pragma unroll
+      for (int t = 1; t < kPage; ++t) {
+        hi = fmaxf(hi, v[t]);
+        lo = fminf(lo, v[t]);
+      }
+    } else {
+      float a[kPage];
+#pragma unroll
+      for (int t = 0; t < kPage; ++t) a[t] = v[t];
+      sort16(a);
+      float h0 = a[kPage - 1], h1 = a[kPage - 1], l0 = a[0], l1 = a[0];
+#pragma unroll
+      for (int q = 0; q < kPage - 1; ++q) {
+        if (q == P.kc_i_hi) { h0 = a[q]; h1 = a[q + 1]; }
+        if (q == P.kc_i_lo) { l0 = a[q]; l1 = a[q + 1]; }
+      }
+      hi = (P.kc_i_hi >= kPage - 1) ? a[kPage - 1] : __fadd_rn(h0, __fmul_rn(P.kc_f_hi, __fsub_rn(h1, h0)));
+      lo = (P.kc_i_lo >= kPage - 1) ? a[kPage - 1] : __fadd_rn(l0, __fmul_rn(P.kc_f_lo, __fsub_rn(l1, l0)));
+    }
+    __half d16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 3.0f));
+    if (__half2float(d16) == 0.0f) d16 = __float2half_rn(1.0f);
+    const __half z16 = __float2half_rn(-__fdiv_rn(lo, __half2float(d16)));
+    const float df = __half2float(d16), zf = __half2float(z16);
+    if (!isfinite(df) || !isfinite(zf)) bad = true;
+    float qv[kPage];
+    divn_by_scale<kPage>(v, df, qv);
+#pragma unroll
+    for (int t = 0; t < kPage; ++t) {
+      const uint32_t c = (uint32_t)min(max(__float2int_rn(__fadd_rn(qv[t], zf)), 0), 3);
+      W[t][m >> 1] |= c << ((m & 1) ? 16 + 2 * s : 2 * s);
+    }
+    const uint32_t db = __half_as_ushort(d16), zb = __half_as_ushort(z16);
+    dpair[m >> 1] |= db << (16 * (m & 1));
+    zpair[m >> 1] |= zb << (16 * (m & 1));
+    emax = max(emax, (int)((db >> 10) & 31u) - 15);
+  }
+  // OR over the 8 lanes of equal lane % 4, scattered: lane l keeps tokens 2 (l >> 2), + 1
+  uint32_t W8[8][2], W4[4][2], W2[2][2];
+  {
+    const bool up = (lane & 16) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t send = up ? W[i][k] : W[8 + i][k];
+        W8[i][k] = (up ? W[8 + i][k] : W[i][k]) | __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+  }
+  {
+    const bool up = (lane & 8) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t send = up ? W8[i][k] : W8[4 + i][k];
+        W4[i][k] = (up ? W8[4 + i][k] : W8[i][k]) | __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+  }
+  {
+    const bool up = (lane & 4) != 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t send = up ? W4[i][k] : W4[2 + i][k];
+        W2[i][k] = (up ? W4[2 + i][k] : W4[i][k]) | __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+  }
+  uint32_t* kw = reinterpret_cast<uint32_t*>(chunk);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int t = 2 * (lane >> 2) + i;
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int k = 2 * (lane & 3) + k2;                 // word k: channel offset 2k in each block
+      kw[16 * (t & 7) + 4 * (k & 3) + 2 * (k >> 2) + (t >> 3)] = W2[i][k2];
+    }
+  }
+  uint32_t* dk = reinterpret_cast<uint32_t*>(chunk + kc_delta_off());
+  uint32_t* zk = reinterpret_cast<uint32_t*>(chunk + kc_zero_off());
+  dk[kc_pair_index(4 * lane)] = dpair[0];
+  dk[kc_pair_index(4 * lane + 2)] = dpair[1];
+  zk[kc_pair_index(4 * lane)] = zpair[0];
+  zk[kc_pair_index(4 * lane + 2)] = zpair[1];
+  emax = __reduce_max_sync(0xffffffffu, (unsigned)(emax + 64)) - 64;
+  if (lane == 0) *reinterpret_cast<int*>(chunk + kc_exp_off(ng, P.l2)) = emax;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(P.status, KVQ_ERR_NONFINITE);
 }
 
 // ---- prefill-sized flushes: two rows per warp -----------------------------------------------
@@ -538,8 +729,11 @@ __global__ void __launch_bounds__(256, 3) flush_kernel2(const FlushParams Pk) {
   // (all of kind w & 1), half hr the ones with k = hr mod 2
   const int n_items = n * P.hkv * 2;
   const int i0 = blockIdx.x * P.items_per_cta;
-  // an append's grid covers the usual ring occupancy; the last CTA takes whatever is beyond
-  const int i1 = (P.cu_rows && blockIdx.x == gridDim.x - 1) ? n_items : min(n_items, i0 + P.items_per_cta);
+  // an append's grid covers the usual ring occupancy; the last CTA takes whatever is beyond;
+  // per-channel keys are quantized by their own kernel (the key warps have nothing to do)
+  const int i1 = ((warp & 1) == 0 && P.key_axis) ? i0
+                 : (P.cu_rows && blockIdx.x == gridDim.x - 1) ? n_items
+                                                              : min(n_items, i0 + P.items_per_cta);
   const int which = warp & 1;
   const uint16_t* ring = which ? P.ring_v : P.ring_k;
   const int hkv = P.hkv, rcap = P.ring_cap;
@@ -632,8 +826,8 @@ __global__ void __launch_bounds__(256, 3) flush_kernel2(const FlushParams Pk) {
       if (which == 0) {
         *reinterpret_cast<__half2*>(chunk + k_scale_off() + (tp * ng + g) * 4) = dz;
       } else {
-        *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g)) = __low2half(dz);
-        *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g)) = __high2half(dz);
+        *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g, P.key_axis)) = __low2half(dz);
+        *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g, P.key_axis)) = __high2half(dz);
       }
     }
     // Pack as flush_kernel does: channels 8 hl + 4 j + m are those of the one-row kernel's lane
@@ -746,8 +940,16 @@ static FlushParams flush_params(const kvq_config* cfg, const kvq_cache* cache, i
   P.group = cfg->group_size;
   P.quantizer = cfg->quantizer;
   P.l2 = cfg->key_l2norm;
-  P.page_bytes = page_head_bytes(cfg->group_size, cfg->key_l2norm);
+  P.page_bytes = page_head_bytes(cfg->group_size, cfg->key_l2norm, cfg->key_axis);
   P.alpha = cfg->quest_alpha;
+  P.key_axis = cfg->key_axis;
+  {
+    const QuantSpec kc = make_quant_spec(kPage, KVQ_QUANT_AFFINE_KAPPA, cfg->kappa_k, cfg->quest_alpha);
+    P.kc_i_lo = kc.i_lo;
+    P.kc_i_hi = kc.i_hi;
+    P.kc_f_lo = kc.f_lo;
+    P.kc_f_hi = kc.f_hi;
+  }
   const double kap[2] = {cfg->kappa_k, cfg->kappa_v};
   for (int w = 0; w < 2; ++w) {
     const QuantSpec q = make_quant_spec(cfg->group_size, cfg->quantizer, kap[w], cfg->quest_alpha);
@@ -795,6 +997,15 @@ extern "C" int kvq_launch_flush(const kvq_config* cfg, const kvq_cache* cache, i
   int cap = max_tokens > 0 ? (max_tokens / cfg->s_flush) * cfg->s_flush : 0;
   if (cap <= 0) return KVQ_OK;
   P.max_tokens = cap;
+  if (cfg->key_axis == KVQ_KEY_PER_CHANNEL) {
+    // key pages first (they read s_quant before the value flush publishes it)
+    const long long items = (long long)(cap / kPage) * cfg->n_kv_heads;
+    const long long ctas = (items + 3) / 4;
+    if (ctas > 0x7fffffffLL || cfg->batch > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (ctas > 0 &&
+        launch_pdl(flush_keys_channel_kernel, dim3((unsigned)ctas, cfg->batch), dim3(128), 0, stream, P) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+  }
   return launch_flush_grid(P, cfg, cap, stream);
 }
 

@@ -85,6 +85,9 @@ extern "C" {
 #define KVQ_QUANT_AFFINE_KAPPA 0  /* kappa-quantile clipped asymmetric affine (OSCAR / WUSH) */
 #define KVQ_QUANT_QUEST_RMS    1  /* QuEST RMS grid: Delta = 2 alpha rms / 3, z = 1.5 (WUSH) */
 
+#define KVQ_KEY_PER_TOKEN      0  /* keys: Delta, z per token and group of G channels (OSCAR / WUSH) */
+#define KVQ_KEY_PER_CHANNEL    1  /* keys: Delta, z per channel and 16-token page (KIVI, OScaR)     */
+
 #define KVQ_TRANSFORM_DENSE    0  /* dense per-head float32 matrices T_K, T_K^{-T}, T_V       */
 #define KVQ_TRANSFORM_HADAMARD 1  /* normalised Walsh-Hadamard on keys and queries (OScaR)    */
 
@@ -98,7 +101,14 @@ extern "C" {
  * s_flush.  ring_cap: capacity of the BF16 recent ring in tokens (a multiple of
  * page_size; at least s_keep + s_flush + the most tokens appended between two
  * flushes).  attn_splits: INT2 splits per (sequence, kv head) in kv_attn_decode
- * (0 = automatic). */
+ * (0 = automatic).  key_axis: KVQ_KEY_PER_TOKEN quantizes each key like each value,
+ * per token and group of G channels; KVQ_KEY_PER_CHANNEL quantizes keys per channel
+ * over the 16 tokens of a page -- KIVI's blocks along the token axis, the range of
+ * channel j being the kappa-quantile range of its 16 values ([OScaR] "背景：KIVI 与逐通道
+ * 量化范式" and algorithm, key processing) -- after the l2 scaling when key_l2norm;
+ * it needs the AFFINE_KAPPA quantizer and s_flush a multiple of 16 (every flush then
+ * quantizes whole pages; KVQ_ERR_UNSUPPORTED otherwise).  Values are per token either
+ * way. */
 typedef struct kvq_config {
   int32_t head_dim;          /* d  (128)                               */
   int32_t n_q_heads;         /* Hq                                     */
@@ -115,7 +125,7 @@ typedef struct kvq_config {
   int32_t max_pages_per_seq; /* columns of the page table              */
   int32_t num_pages;         /* physical pages in the pool             */
   int32_t attn_splits;       /* 0 = automatic                          */
-  int32_t reserved;
+  int32_t key_axis;          /* KVQ_KEY_PER_*                          */
   double  kappa_k;           /* key clipping quantile                  */
   double  kappa_v;           /* value clipping quantile                */
   double  quest_alpha;       /* QuEST clip in RMS units                */
@@ -135,13 +145,21 @@ typedef struct kvq_config {
  *              [512, 1024)   value codes in MMA-fragment order: u32 word 4*l + r,
  *                            bits 2m + 16e (m = 0..7) hold the code of channel
  *                            16m + (l/4) + 8*(r%2) of token 2*(l%4) + 8*(r/2) + e.
- *              [1024, ...)   key (Delta16, z16) float16 pairs [16 tokens][d/G]; then
+ *              [1024, ...)   key scales: KVQ_KEY_PER_TOKEN: (Delta16, z16) float16
+ *                            pairs [16 tokens][d/G] (64 d/G bytes); KVQ_KEY_PER_CHANNEL:
+ *                            Delta16 [256 bytes] then z16 [256 bytes], each 64 u32
+ *                            pairs, pair 16 q + 2 s + h holding channels
+ *                            16 s + 8 h + 2 q and + 1 (the B-fragment order of the
+ *                            decode's MMAs: q = 0..3, s = 0..7, h = 0..1); then
  *                            value Delta16 [8 token pairs][d/G][2] and value z16
  *                            [8 token pairs][d/G][2] (token t at pair t/2, slot t%2);
  *                            then (only when key_l2norm) key norms s16 float16 [16];
+ *                            then (KVQ_KEY_PER_CHANNEL only) int32 E: the binary
+ *                            exponent of the page's largest key Delta16 (at least -14);
  *                            the chunk is padded to a multiple of 32 bytes.
  *            Token t dequantizes as x_hat_c = s16 * Delta16 * (code_c - z16), with
- *            s16 = 1 without key_l2norm ([OScaR] step 2 dequantisation).
+ *            s16 = 1 without key_l2norm ([OScaR] step 2 dequantisation), Delta16 and
+ *            z16 those of its group or, for per-channel keys, of channel c.
  * page_table [B][max_pages_per_seq] int32 physical page ids (-1 = none).
  * seq_len    [B] int32 tokens in each sequence; kv_rotate_qk raises it to
  *            pos + 1 for every row it writes.

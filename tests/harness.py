@@ -25,7 +25,8 @@ def kv_config(w: synth.Workload, lengths_after, ring_extra: int = 1024, attn_spl
         num_pages=num_pages, ring_cap=ring, group_size=w.group_size,
         quantizer=kvq.KVQ_QUANT_QUEST_RMS if w.quantizer == "quest" else kvq.KVQ_QUANT_AFFINE_KAPPA,
         key_l2norm=w.key_l2norm, s_sink=w.s_sink, s_keep=w.s_keep, s_flush=w.s_flush,
-        attn_splits=attn_splits, kappa_k=w.kappa_k, kappa_v=w.kappa_v, quest_alpha=w.quest_alpha)
+        attn_splits=attn_splits, kappa_k=w.kappa_k, kappa_v=w.kappa_v, quest_alpha=w.quest_alpha,
+        key_axis=kvq.KVQ_KEY_PER_CHANNEL if w.key_axis == "channel" else kvq.KVQ_KEY_PER_TOKEN)
     return cfg, table
 
 

@@ -38,7 +38,8 @@ def compare_unit(run: GpuRun, snap: dict, b: int, h: int) -> dict:
         mm += int(np.sum(snap["ring_v"][b, h, toks % R] != ref["v_rot"][toks]))
     rep["window_mismatch"] = mm
     # INT2 region
-    dec = layout.decode_unit(snap["pages"], run.table[b], h, w.s_sink, sq, w.group_size, w.key_l2norm)
+    axis = 1 if w.key_axis == "channel" else 0
+    dec = layout.decode_unit(snap["pages"], run.table[b], h, w.s_sink, sq, w.group_size, w.key_l2norm, axis)
     qk, qv = ref["unit"]["qk"], ref["unit"]["qv"]
     rep["n_codes"] = int(qk["codes"].size + qv["codes"].size)
     rep["code_mismatch"] = int(np.sum(dec["codes_k"] != qk["codes"]) + np.sum(dec["codes_v"] != qv["codes"]))
@@ -47,6 +48,11 @@ def compare_unit(run: GpuRun, snap: dict, b: int, h: int) -> dict:
                              same16(dec["delta_v"], qv["delta16"]) + same16(dec["zero_v"], qv["zero16"]))
     if w.key_l2norm:
         rep["scale_mismatch"] += same16(dec["norm_k"], qk["norm16"])
+    if axis:
+        # the page exponent: that of the largest key Delta16 of the page, at least -14
+        d = qk["delta16"].astype(np.float64)
+        want = np.maximum(np.floor(np.log2(np.maximum(d.max(axis=1), 2.0 ** -30))).astype(np.int64), -14)
+        rep["scale_mismatch"] += int(np.sum(dec["exp_k"] != want))
     # attention output: normwise max relative error per query head
     o = snap["out"][b, h * g:(h + 1) * g].astype(np.float64)
     r = ref["out"]

@@ -53,6 +53,8 @@ def test_sizes(kvq):
     assert kvq.kvq_page_bytes(c) == 8 * 1152
     assert kvq.kvq_page_head_bytes(_cfg(kvq, group_size=64)) == 1280
     assert kvq.kvq_page_head_bytes(_cfg(kvq, group_size=32, key_l2norm=True)) == 1568
+    # per-channel keys: d Delta16 + d z16 instead of 16 x d/G pairs, plus the page exponent
+    assert kvq.kvq_page_head_bytes(_cfg(kvq, group_size=32, key_l2norm=True, key_axis=1, s_flush=128, s_keep=0)) == 1856
     assert kvq.kv_attn_workspace_bytes(c, 4096) > 0
     assert kvq.kvq_page_head_bytes(_cfg(kvq, head_dim=64)) == 0
 
@@ -62,6 +64,7 @@ def test_sizes(kvq):
     (dict(n_q_heads=24, n_kv_heads=2), -2), (dict(kappa_k=0.3), -1), (dict(kappa_v=1.5), -1),
     (dict(ring_cap=100), -1), (dict(ring_cap=16), -1), (dict(s_flush=0), -1),
     (dict(quantizer=1, key_l2norm=True), -2), (dict(quantizer=7), -1), (dict(batch=0), -1),
+    (dict(key_axis=2), -1), (dict(key_axis=1, s_flush=8), -2), (dict(key_axis=1, s_flush=16, quantizer=1), -2),
 ])
 def test_config_validation(kvq, kw, code):
     c = _cfg(kvq, **kw).c()
