@@ -43,7 +43,7 @@ import synth  # noqa: E402
 METRIC = "INT2 paged decode attention: effective HBM GB/s (% of ~8 TB/s), tokens/s"
 UNIT = "GB/s"
 DEFAULT_CONFIG = 4                 # the largest single-GPU workload (128K context)
-SUB_CONFIGS = "2,3,5"              # measured in the same run, reported as sub-records
+SUB_CONFIGS = "2,3,5,6"            # measured in the same run, reported as sub-records
 NOMINAL_HBM_GBS = 7900.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -54,14 +54,18 @@ def step_bytes(w: synth.Workload, ctx: np.ndarray, sq_before: np.ndarray, sq_aft
     rotate / flush traffic of the new tokens."""
     d, hkv, g, B = w.head_dim, w.n_kv_heads, w.gqa, w.batch
     ng = d // w.group_size
-    int2_tok = 2 * (d // 4) + 2 * 4 * ng + (2 if w.key_l2norm else 0)
+    # K + V bytes of one INT2 token: codes, scales (per-channel keys: d Delta16 + d z16 and the
+    # 4-byte page exponent per 16 tokens), key norm
+    chan = w.key_axis == "channel"
+    int2_tok = (2 * (d // 4) + 4 * ng + (4 * d / w.page_size + 4 / w.page_size if chan else 4 * ng)
+                + (2 if w.key_l2norm else 0))
     L = ctx + w.n_new
     dec_int2 = dec_win = ptab = 0
     for Lb, sqb in zip(L, sq_after):
         Lb, sqb = int(Lb), int(sqb)
         n_int2 = max(0, min(sqb, Lb) - w.s_sink)
         n_win = min(w.s_sink, Lb) + max(0, Lb - max(sqb, w.s_sink))
-        dec_int2 += n_int2 * hkv * int2_tok
+        dec_int2 += int(round(n_int2 * hkv * int2_tok))
         dec_win += n_win * hkv * 4 * d
         ptab += -(-n_int2 // w.page_size) * 4
     qb = B * w.n_q_heads * d * 2
@@ -74,7 +78,7 @@ def step_bytes(w: synth.Workload, ctx: np.ndarray, sq_before: np.ndarray, sq_aft
         mats += hkv * d * d * 4
     rotate = mats + 2 * qb + 2 * n_new_rows * d * 2 * 2
     n_fl = int(np.sum(sq_after - sq_before)) * hkv
-    flush = n_fl * (2 * d * 2 + int2_tok)
+    flush = int(round(n_fl * (2 * d * 2 + int2_tok)))
     return {"decode": int(decode), "decode_int2": int(dec_int2), "decode_window": int(dec_win),
             "rotate": int(rotate), "flush": int(flush), "total": int(decode + rotate + flush)}
 
@@ -336,7 +340,7 @@ def measure_config(args, w: synth.Workload, rank: int, world: int, local_rank: i
                    "head_dim": w.head_dim, "context": int(ctx.max()) + w.n_new, "n_new_tokens": w.n_new,
                    "group_size": w.group_size, "kappa": [w.kappa_k, w.kappa_v],
                    "windows_sink_keep_flush": [w.s_sink, w.s_keep, w.s_flush], "transform": w.transform,
-                   "key_l2norm": bool(w.key_l2norm),
+                   "key_l2norm": bool(w.key_l2norm), "key_axis": w.key_axis,
                    "l2": "flushed between timed steps (512 MB memset, untimed)",
                    "bytes_per_step": nbytes, "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * w.batch / (t_step_max * 1e-3), 1),
@@ -545,7 +549,7 @@ def oracle_step_sample(config: int, budget_s: float) -> dict:
         sqb = int(sq_b[b])
         unit = cache.build_unit(k_rot, v_rot, ui.ctx, sqb, s_sink=w.s_sink, group=w.group_size,
                                 kappa_k=w.kappa_k, kappa_v=w.kappa_v, quantizer=w.quantizer,
-                                alpha=w.quest_alpha, key_l2norm=w.key_l2norm)
+                                alpha=w.quest_alpha, key_l2norm=w.key_l2norm, key_axis=w.key_axis)
         t0 = time.process_time()
         # the step: rotate new rows + queries, flush, dequantize the cache, attend
         kn = f32_to_bf16_bits(transform.rotate_rows(None if tk is None else tk[h], ui.k[ui.ctx:L], kind))
@@ -561,8 +565,12 @@ def oracle_step_sample(config: int, budget_s: float) -> dict:
             kh[lo:sqb] = quant.dequantize(unit["qk"])
             vh[lo:sqb] = quant.dequantize(unit["qv"])
         if sqa > sqb:
-            kh[sqb:sqa] = quant.dequantize(quant.quantize_rows(k_all[sqb:sqa], w.group_size, w.kappa_k, w.quantizer,
-                                                               w.quest_alpha, w.key_l2norm))
+            if w.key_axis == "channel":
+                qk = quant.quantize_keys_per_channel(k_all[sqb:sqa], w.page_size, w.kappa_k, w.key_l2norm)
+            else:
+                qk = quant.quantize_rows(k_all[sqb:sqa], w.group_size, w.kappa_k, w.quantizer, w.quest_alpha,
+                                         w.key_l2norm)
+            kh[sqb:sqa] = quant.dequantize(qk)
             vh[sqb:sqa] = quant.dequantize(quant.quantize_rows(v_all[sqb:sqa], w.group_size, w.kappa_v, w.quantizer,
                                                                w.quest_alpha, False))
         attention.decode(qr.astype(np.float64), kh, vh, 1.0 / math.sqrt(w.head_dim))

@@ -126,8 +126,10 @@ WUSH_CHUNK_B16 = Workload(name="wush-qwen3-8b-b16-chunk2048-on-16k", seed=5, bat
                           n_kv_heads=8, ctx_lo=16384, ctx_hi=16384, n_new=2048, group_size=128,
                           kappa_k=0.99, kappa_v=0.99, transform="invertible", value_transform="identity",
                           chunk_queries=True)
+# the 128K OScaR cache with KIVI's per-channel keys (Delta, z per channel per 16-token page)
+QWEN3_32B_128K_KIVI = QWEN3_32B_128K.replace(name="qwen3-32b-ctx128k-b4-oscar-kivi", seed=6, key_axis="channel")
 WORKLOADS: dict[int, Workload] = {1: TINY_GQA4, 2: QWEN3_8B_32K, 3: QWEN3_4B_B64, 4: QWEN3_32B_128K,
-                                  5: WUSH_CHUNK_B16}
+                                  5: WUSH_CHUNK_B16, 6: QWEN3_32B_128K_KIVI}
 
 
 # ---- transforms handed over by offline calibration -----------------------------
