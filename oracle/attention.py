@@ -15,6 +15,14 @@ from __future__ import annotations
 import numpy as np
 
 
+def chunk(q: np.ndarray, pos: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
+    """Causal attention of chunk queries: q [n, g, d], query i at position pos[i] attends to
+    tokens [0, pos[i]] of k / v [L, d] (the cache as it stands after the chunk was appended:
+    [WUSH] "方法步骤详情", mixed-precision attention over the windows and the INT2 middle;
+    [OSCAR] section 4 "Decoding Attention Kernel", BF16 and INT2 segments).  -> [n, g, d]."""
+    return np.stack([decode(q[i], k[:int(pos[i]) + 1], v[:int(pos[i]) + 1], scale) for i in range(len(pos))])
+
+
 def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
     """q [g, d], k / v [L, d] (float64 values) -> out [g, d] float64.
 

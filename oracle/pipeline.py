@@ -65,3 +65,18 @@ def run_unit(w, ui, tk, tkit, tv, scale: float | None = None, attend: bool = Tru
         sc = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
         res["out"] = attention.decode(bf16_to_f32(q_rot).astype(np.float64), kh, vh, sc)
     return res
+
+
+def run_unit_chunk_attention(w, ui, tk, tkit, tv, q_chunk_bits, scale: float | None = None) -> dict:
+    """The step of run_unit with its appended chunk's queries q_chunk_bits [n_new, g, d]
+    (bit patterns) attending causally to the cache after the step: query i at position
+    ctx + i sees tokens [0, ctx + i] as the cache holds them (BF16 sink and recent rows,
+    the INT2 middle dequantized)."""
+    res = run_unit(w, ui, tk, tkit, tv, scale, attend=False)
+    kh, vh = cache.dequantized_kv(res["unit"])
+    q_rot = rotate_chunk_queries(w, ui.h, q_chunk_bits, tkit)
+    sc = 1.0 / math.sqrt(w.head_dim) if scale is None else scale
+    pos = ui.ctx + np.arange(q_chunk_bits.shape[0])
+    res["q_chunk_rot"] = q_rot
+    res["out_chunk"] = attention.chunk(bf16_to_f32(q_rot).astype(np.float64), pos, kh, vh, sc)
+    return res

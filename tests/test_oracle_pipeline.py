@@ -20,7 +20,7 @@ import numpy as np
 import pytest
 
 import synth
-from oracle import cache, pipeline, quant
+from oracle import attention, cache, pipeline, quant
 from oracle.fp import bf16_to_f32
 
 U_BF16 = 2.0 ** -8          # unit roundoff of bfloat16 (8-bit significand)
@@ -145,3 +145,50 @@ def test_planted_region_shift_same_bounds_is_caught(monkeypatch):
     monkeypatch.setattr(cache, "build_unit", bad)
     with pytest.raises(AssertionError):
         test_quantized_region_row_by_row()
+
+
+# ---- chunk attention (causal queries of an appended chunk over the mixed cache) ---------------
+
+def _brute_prefix(q, pos, k, v, scale):
+    """Softmax attention written out with loops: q [n, g, d], query i sees k[0..pos[i]]."""
+    n, g, d = q.shape
+    out = np.zeros((n, g, d))
+    for i in range(n):
+        for hh in range(g):
+            s = np.array([sum(q[i, hh, c] * k[t, c] for c in range(d)) * scale for t in range(int(pos[i]) + 1)])
+            e = np.exp(s - s.max())
+            out[i, hh] = (e[:, None] * v[:int(pos[i]) + 1]).sum(0) / e.sum()
+    return out
+
+
+def test_chunk_attention_brute_force_causal():
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((5, 2, 6))
+    k = rng.standard_normal((7, 6))
+    v = rng.standard_normal((7, 6))
+    pos = np.arange(2, 7)
+    got = attention.chunk(q, pos, k, v, 0.4)
+    assert np.allclose(got, _brute_prefix(q, pos, k, v, 0.4), rtol=1e-12, atol=1e-12)
+    # an off-by-one prefix (tokens [0, p) instead of [0, p]) differs
+    assert not np.allclose(attention.chunk(q, pos - 1, k, v, 0.4), got)
+
+
+def test_chunk_attention_last_query_is_the_decode_query():
+    """The chunk query at the last position with the decode query's values gives the decode
+    output; a chunk inside the BF16 sink is causal attention over the rotated BF16 rows."""
+    w = synth.TINY_GQA4.replace(ctx_lo=200, ctx_hi=200, n_new=40, s_sink=16, s_keep=64, s_flush=8)
+    tk, tkit, tv = synth.transforms(w)
+    ui = synth.unit_inputs(w, 0, 0, synth.context_lengths(w))
+    qc = synth.chunk_query_rows(w, 0, 0)
+    qc[-1] = ui.q
+    r = pipeline.run_unit_chunk_attention(w, ui, tk, tkit, tv, qc)
+    d = pipeline.run_unit(w, ui, tk, tkit, tv)
+    assert np.allclose(r["out_chunk"][-1], d["out"], rtol=1e-12, atol=1e-14)
+    w2 = w.replace(ctx_lo=5, ctx_hi=5, n_new=6, s_sink=16)
+    ui2 = synth.unit_inputs(w2, 0, 0, synth.context_lengths(w2))
+    r2 = pipeline.run_unit_chunk_attention(w2, ui2, tk, tkit, tv, synth.chunk_query_rows(w2, 0, 0))
+    k = bf16_to_f32(r2["k_rot"]).astype(np.float64)
+    v = bf16_to_f32(r2["v_rot"]).astype(np.float64)
+    q = bf16_to_f32(r2["q_chunk_rot"]).astype(np.float64)
+    want = _brute_prefix(q, 5 + np.arange(6), k, v, 1 / np.sqrt(128))
+    assert np.allclose(r2["out_chunk"], want, rtol=1e-10, atol=1e-12)
