@@ -38,7 +38,7 @@ KVQ_TRANSFORM_HADAMARD = 1
 KVQ_KEY_PER_TOKEN = 0
 KVQ_KEY_PER_CHANNEL = 1
 
-EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_append_chunk", "kv_attn_decode", "kv_attn_decode_bf16", "kv_attn_decode_noalloc",
+EXPORTED = ("kv_rotate_qk", "kv_quant_flush", "kv_append_chunk", "kv_attn_chunk", "kv_attn_chunk_workspace_bytes", "kv_attn_decode", "kv_attn_decode_bf16", "kv_attn_decode_noalloc",
             "kv_attn_workspace_bytes",
             "kvq_page_head_bytes", "kvq_page_bytes", "kvq_status_string", "kvq_version",
             "kvq_selftest_scale_division", "kvq_selftest_tc_integer_sums")
@@ -85,6 +85,10 @@ def lib() -> ctypes.CDLL:
         l.kv_rotate_qk.restype = ctypes.c_int
         l.kv_quant_flush.argtypes = [P(CConfig), P(CCache), i32, vp, vp]
         l.kv_append_chunk.restype = ctypes.c_int
+        l.kv_attn_chunk.argtypes = [P(CConfig), P(CCache), vp, vp, i32, vp, ctypes.c_float, i32, vp, sz, vp, vp]
+        l.kv_attn_chunk.restype = ctypes.c_int
+        l.kv_attn_chunk_workspace_bytes.argtypes = [P(CConfig), i32, i32]
+        l.kv_attn_chunk_workspace_bytes.restype = sz
         l.kv_append_chunk.argtypes = [P(CConfig), P(CTransform), vp, vp, vp, i32, P(CCache), vp, vp]
         l.kv_quant_flush.restype = ctypes.c_int
         l.kv_attn_decode.argtypes = [P(CConfig), P(CCache), vp, vp, ctypes.c_float, i32, vp, sz, vp, vp]
@@ -270,6 +274,22 @@ def kv_append_chunk(cfg: KVConfig, tr: Transform, k, v, cu_rows, cache: KVCache,
     rc = lib().kv_append_chunk(ctypes.byref(c), ctypes.byref(t), _ptr(k), _ptr(v), _ptr(cu_rows), n,
                                ctypes.byref(cc), _ptr(status), _stream(stream))
     _check(rc, "kv_append_chunk")
+
+
+def kv_attn_chunk_workspace_bytes(cfg: KVConfig, n_rows: int, max_ctx: int) -> int:
+    return int(lib().kv_attn_chunk_workspace_bytes(ctypes.byref(cfg.c()), int(n_rows), int(max_ctx)))
+
+
+def kv_attn_chunk(cfg: KVConfig, cache: KVCache, q_rot, cu_rows, out, sm_scale: float, max_ctx: int, workspace,
+                  status, stream=None) -> None:
+    """q_rot [n, Hq, d] (rows cu_rows[b] .. cu_rows[b+1]-1 the last tokens of sequence b) ->
+    out [n, Hq, d] float32: causal attention over the cache after the append."""
+    n = int(q_rot.shape[0])
+    c, cc = cfg.c(), cache.c()
+    rc = lib().kv_attn_chunk(ctypes.byref(c), ctypes.byref(cc), _ptr(q_rot), _ptr(cu_rows), n, _ptr(out),
+                             float(sm_scale), int(max_ctx), _ptr(workspace), int(workspace.numel()), _ptr(status),
+                             _stream(stream))
+    _check(rc, "kv_attn_chunk")
 
 
 def kv_quant_flush(cfg: KVConfig, cache: KVCache, max_tokens_per_seq: int, status, stream=None) -> None:

@@ -170,6 +170,29 @@ KVQ_API int kv_attn_decode_bf16(const kvq_config* cfg, const kvq_cache* cache, c
   return kvq_launch_attn(cfg, cache, q_rot, out, 1, sm_scale, max_ctx, workspace, d_status, (cudaStream_t)stream);
 }
 
+KVQ_API size_t kv_attn_chunk_workspace_bytes(const kvq_config* cfg, int32_t n_rows, int32_t max_ctx) {
+  if (check_config(cfg) != KVQ_OK || max_ctx < 0 || n_rows < 0 || n_rows > 65535) return 0;
+  return kvq_attn_chunk_ws_bytes(cfg, n_rows, max_ctx);
+}
+
+KVQ_API int kv_attn_chunk(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, const int32_t* cu_rows,
+                          int32_t n_rows, float* out, float sm_scale, int32_t max_ctx, void* workspace, size_t ws_bytes,
+                          int32_t* d_status, void* stream) {
+  int rc = check_config(cfg);
+  if (rc) return rc;
+  rc = check_cache(cfg, cache);
+  if (rc) return rc;
+  if (n_rows < 0 || max_ctx < 0 || !cu_rows || !aligned(cu_rows, 4)) return KVQ_ERR_INVALID_ARG;
+  if (n_rows > 65535) return KVQ_ERR_UNSUPPORTED;                  // one grid row per query row
+  if (n_rows == 0) return KVQ_OK;
+  if (!q_rot || !out || !aligned(q_rot, 16) || !aligned(out, 16)) return KVQ_ERR_INVALID_ARG;
+  if (!(sm_scale == sm_scale)) return KVQ_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 256)) return KVQ_ERR_INVALID_ARG;
+  if (ws_bytes < kvq_attn_chunk_ws_bytes(cfg, n_rows, max_ctx)) return KVQ_ERR_WORKSPACE;
+  return kvq_launch_attn_chunk(cfg, cache, q_rot, cu_rows, n_rows, out, sm_scale, max_ctx, workspace, d_status,
+                               (cudaStream_t)stream);
+}
+
 KVQ_API int kv_attn_decode_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
                                    float* out, float sm_scale, int32_t max_ctx, int32_t* d_status, void* stream) {
   int rc = check_config(cfg);

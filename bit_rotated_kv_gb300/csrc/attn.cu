@@ -72,7 +72,39 @@ struct AttnParams {
   int merge1;         // 1: the last CTA of a unit merges every split partial from shared memory
   int out_bf16;       // 1: the output is rounded once to bf16 (nearest-even)
   float scale_log2;   // sm_scale * log2(e)
+  // chunk queries (kv_attn_chunk): grid row b is query row b; its cache sequence is the bc with
+  // cu_rows[bc] <= b < cu_rows[bc + 1] (seqs sequences) and it sees tokens [0, p], p its
+  // position seq_len[bc] - (cu_rows[bc + 1] - b).  nullptr: one decode query per sequence.
+  const int32_t* cu_rows;
+  int seqs;
 };
+
+// Cache sequence of grid row b (-1: a chunk row outside cu_rows).  cu_rows is a caller input,
+// read before the dependency wait.
+__device__ __forceinline__ int attn_seq(const AttnParams& P, int b) {
+  if (!P.cu_rows) return b;
+  if (b < __ldg(P.cu_rows) || b >= __ldg(P.cu_rows + P.seqs)) return -1;
+  int lo = 0, hi = P.seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(P.cu_rows + mid) <= b) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Length and INT2 edge that grid row b sees (after the dependency wait): a decode query sees
+// its sequence's seq_len tokens; a chunk query the tokens up to its own position.
+__device__ __forceinline__ void unit_state(const AttnParams& P, int b, int bc, int& L, int& sq) {
+  if (bc < 0) {
+    L = 0;
+    sq = P.s_sink;
+    return;
+  }
+  L = P.seq_len[bc];
+  sq = P.s_quant[bc];
+  if (P.cu_rows) L = max(0, min(L, L - (__ldg(P.cu_rows + bc + 1) - b) + 1));
+}
 
 // ---- PTX helpers ----------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -280,7 +312,7 @@ __device__ __forceinline__ uint32_t dz_operand(uint32_t dz, bool odd) {
 }
 
 template <int NG, bool L2, bool KC>
-__device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int split, float* res,
+__device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int bc, int h, int split, float* res,
                            size_t wstride) {
   // accumulators per group; with one group the k-steps alternate between two accumulators so
   // that consecutive MMAs do not wait on each other
@@ -294,7 +326,7 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
   const int p1 = (int)((long long)P.mp * (split + 1) / P.n_int2);
   const int first = p0 + warp;
   const int nk_max = first < p1 ? (p1 - first + kWarps - 1) / kWarps : 0;
-  const int32_t* ptab = P.page_table + (size_t)b * P.max_pages;
+  const int32_t* ptab = P.page_table + (size_t)(bc < 0 ? 0 : bc) * P.max_pages;
   // page-table entries of this warp's pages, 32 at a time: lane i of chunk c holds page 32c + i
   auto load_pids = [&](int c) -> int {
     const int k = 32 * c + lane;
@@ -347,8 +379,8 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
     const int pid = __shfl_sync(0xffffffffu, pid_a, k);
     if (lane == 0 && k < n_first) refill(k, pid);
   }
-  const int Lraw = P.seq_len[b];
-  const int sqraw = P.s_quant[b];
+  int Lraw, sqraw;
+  unit_state(P, b, bc, Lraw, sqraw);
 
   // ---- this warp's pages inside the INT2 region
   const int L = Lraw;
@@ -821,13 +853,15 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int h, int
 }
 
 // ---- BF16 windows --------------------------------------------------------------------------
-__device__ void window_split(const AttnParams& P, int b, int h, int wsplit, float* res, size_t wstride) {
+__device__ void window_split(const AttnParams& P, int b, int bc, int h, int wsplit, float* res, size_t wstride) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = P.gqa;
   pdl_wait();
-  const int L = P.seq_len[b];
+  int L, sqw;
+  unit_state(P, b, bc, L, sqw);
   const int n_sink = min(P.s_sink, max(L, 0));
-  const int r0 = max(min(P.s_quant[b], L), P.s_sink);     // first recent token
+  const int r0 = max(min(sqw, L), P.s_sink);              // first recent token
+  const int bcc = bc < 0 ? 0 : bc;                        // the cache rows (none read when L = 0)
   const int n_sink_t = (n_sink + kPage - 1) / kPage;
   const int rt0 = r0 / kPage;
   const int n_rec_t = (L > r0) ? ((L - 1) / kPage - rt0 + 1) : 0;
@@ -870,7 +904,7 @@ __device__ void window_split(const AttnParams& P, int b, int h, int wsplit, floa
       tok0 = ti * kPage;
       lo = tok0;
       hi = min(tok0 + kPage, n_sink);
-      const size_t off = ((size_t)b * P.hkv + h) * P.s_sink * kHeadDim + (size_t)tok0 * kHeadDim;
+      const size_t off = ((size_t)bcc * P.hkv + h) * P.s_sink * kHeadDim + (size_t)tok0 * kHeadDim;
       kbase = P.sink_k + off;
       vbase = P.sink_v + off;
       rows_avail = hi - tok0;                 // rows beyond the sink buffer are never read
@@ -878,7 +912,7 @@ __device__ void window_split(const AttnParams& P, int b, int h, int wsplit, floa
       tok0 = (rt0 + ti - n_sink_t) * kPage;
       lo = max(tok0, r0);
       hi = min(tok0 + kPage, L);
-      const size_t off = (((size_t)b * P.hkv + h) * P.ring_cap + (tok0 % P.ring_cap)) * kHeadDim;
+      const size_t off = (((size_t)bcc * P.hkv + h) * P.ring_cap + (tok0 % P.ring_cap)) * kHeadDim;
       kbase = P.ring_k + off;
       vbase = P.ring_v + off;
       rows_avail = kPage;
@@ -1064,16 +1098,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const
   // later, partly empty ones and the short window splits (longest work first)
   const int split = blockIdx.z, h = blockIdx.x, b = blockIdx.y;
   const int g = P.gqa;
+  const int bc = attn_seq(P, b);
+  if (bc < 0 && threadIdx.x == 0 && split == 0 && h == 0) set_status(P.status, KVQ_ERR_BOUNDS);
   // per-warp results: an INT2 warp writes into its own (drained) page ring, a window warp
   // into a plain array; both start after the 1 KB of barriers and query data.
   float* res = reinterpret_cast<float*>(smem + 1024);
   size_t wstride;
   if (split < P.n_int2) {
     wstride = (size_t)kStages * P.page_bytes / sizeof(float);
-    int2_split<NG, L2, KC>(P, smem, b, h, split, res, wstride);
+    int2_split<NG, L2, KC>(P, smem, b, bc, h, split, res, wstride);
   } else {
     wstride = (size_t)g * kRow;
-    window_split(P, b, h, split - P.n_int2, res, wstride);
+    window_split(P, b, bc, h, split - P.n_int2, res, wstride);
   }
   __syncthreads();
   // ---- CTA partial: merge the warps, store to the workspace
@@ -1230,10 +1266,14 @@ extern "C" size_t kvq_attn_ws_bytes(const kvq_config* cfg, int32_t max_ctx) {
   return kvq_attn_counter_bytes(cfg, max_ctx) + units * (ns + n_grp) * g * kRow * sizeof(float);
 }
 
-extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
-                               void* out, int out_bf16, float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status,
-                               cudaStream_t stream) {
+// The decode launch; cfg->batch is the number of grid rows (sequences, or chunk query rows
+// with cu_rows over seqs sequences).
+static int launch_attn_impl(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, void* out,
+                            int out_bf16, float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status,
+                            cudaStream_t stream, const int32_t* cu_rows, int seqs) {
   AttnParams P{};
+  P.cu_rows = cu_rows;
+  P.seqs = seqs;
   P.pages = (const uint8_t*)cache->pages;
   P.page_table = cache->page_table;
   P.seq_len = cache->seq_len;
@@ -1303,6 +1343,30 @@ extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, co
   if (cfg->batch > 65535 || P.n_split > 65535) return KVQ_ERR_UNSUPPORTED;   // grid y / z limits
   dim3 grid(cfg->n_kv_heads, cfg->batch, P.n_split);
   return launch_pdl(kern, grid, dim3(kThreads), smem, stream, P) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+extern "C" int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
+                               void* out, int out_bf16, float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status,
+                               cudaStream_t stream) {
+  return launch_attn_impl(cfg, cache, q_rot, out, out_bf16, sm_scale, max_ctx, ws, d_status, stream, nullptr,
+                          cfg->batch);
+}
+
+// Chunk queries: one grid row per query row (the sizes follow from a config whose batch is
+// the number of rows).
+extern "C" size_t kvq_attn_chunk_ws_bytes(const kvq_config* cfg, int32_t n_rows, int32_t max_ctx) {
+  kvq_config c = *cfg;
+  c.batch = n_rows;
+  return kvq_attn_ws_bytes(&c, max_ctx);
+}
+
+extern "C" int kvq_launch_attn_chunk(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
+                                     const int32_t* cu_rows, int32_t n_rows, float* out, float sm_scale,
+                                     int32_t max_ctx, void* ws, int32_t* d_status, cudaStream_t stream) {
+  if (n_rows == 0) return KVQ_OK;
+  kvq_config c = *cfg;
+  c.batch = n_rows;
+  return launch_attn_impl(&c, cache, q_rot, out, 0, sm_scale, max_ctx, ws, d_status, stream, cu_rows, cfg->batch);
 }
 
 // ---- allocation-free variant ---------------------------------------------------------------

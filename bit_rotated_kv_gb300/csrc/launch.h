@@ -18,6 +18,10 @@ int kvq_launch_append(const kvq_config* cfg, const kvq_transform* tr, const uint
                       cudaStream_t stream);
 int kvq_launch_attn(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, void* out, int out_bf16,
                     float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status, cudaStream_t stream);
+int kvq_launch_attn_chunk(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, const int32_t* cu_rows,
+                          int32_t n_rows, float* out, float sm_scale, int32_t max_ctx, void* ws, int32_t* d_status,
+                          cudaStream_t stream);
+size_t kvq_attn_chunk_ws_bytes(const kvq_config* cfg, int32_t n_rows, int32_t max_ctx);
 int kvq_launch_attn_noalloc(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot, float* out,
                             float sm_scale, int32_t max_ctx, int32_t* d_status, cudaStream_t stream);
 int kvq_launch_div_selftest(unsigned long long* d_mismatches, cudaStream_t stream);

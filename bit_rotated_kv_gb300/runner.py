@@ -10,8 +10,8 @@ import math
 import numpy as np
 import torch
 
-from . import (KVCache, KVConfig, Transform, kv_append_chunk, kv_attn_decode, kv_quant_flush, kv_rotate_qk,
-               workspace)
+from . import (KVCache, KVConfig, Transform, kv_append_chunk, kv_attn_chunk, kv_attn_chunk_workspace_bytes,
+               kv_attn_decode, kv_quant_flush, kv_rotate_qk, workspace)
 
 
 def _rows_for(k_all: torch.Tensor, lengths_lo, lengths_hi):
@@ -71,6 +71,17 @@ class DecodeRunner:
     def decode(self, q_rot, out, stream=None) -> None:
         kv_attn_decode(self.cfg, self.cache, q_rot, out, self.sm_scale, self.max_ctx, self.ws, self.status,
                        self.stream if stream is None else stream)
+
+    def chunk_workspace(self, n_rows: int) -> torch.Tensor:
+        """A zeroed workspace for kv_attn_chunk over n_rows query rows."""
+        n = kv_attn_chunk_workspace_bytes(self.cfg, n_rows, self.max_ctx)
+        return torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)
+
+    def attn_chunk(self, q_rot, cu_rows, out, ws, stream=None) -> None:
+        """Causal attention of chunk query rows q_rot [n, Hq, d] over the cache (after their
+        tokens were appended) into out [n, Hq, d] float32."""
+        kv_attn_chunk(self.cfg, self.cache, q_rot, cu_rows, out, self.sm_scale, self.max_ctx, ws, self.status,
+                      self.stream if stream is None else stream)
 
     def prefill(self, k_all: torch.Tensor, v_all: torch.Tensor, lengths, chunk: int) -> None:
         """Append tokens [0, lengths[b]) of k_all / v_all [B, T, Hkv, d] (bf16, device) in chunks,

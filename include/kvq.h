@@ -19,6 +19,8 @@
  *   kv_attn_decode  GQA decode attention reading the mixed BF16 / INT2 cache
  *                   directly ([OSCAR] section 4 "Decoding Attention Kernel";
  *                   [OScaR] "系统设计与 CUDA 实现"; [WUSH] GQA background).
+ *   kv_attn_chunk   causal attention of a chunk's queries over the same cache
+ *                   (the prefill path; [WUSH] inference algorithm).
  *   kv_append_chunk the first two fused for a prefill chunk: transform on write
  *                   and quantize-on-write in one pass, rows bound for INT2 never
  *                   written as BF16 ([OScaR] "系统设计与 CUDA 实现", key-quant
@@ -277,6 +279,30 @@ KVQ_API int kv_quant_flush(const kvq_config* cfg, const kvq_cache* cache, int32_
 KVQ_API int kv_append_chunk(const kvq_config* cfg, const kvq_transform* tr,
                     const uint16_t* k, const uint16_t* v, const int32_t* cu_rows, int32_t n_rows,
                     const kvq_cache* cache, int32_t* d_status, void* stream);
+
+/* kv_attn_chunk: attention of the queries of an appended chunk (the prefill path) over the
+ * cache as it stands after the append.
+ *   q_rot    [n_rows][Hq][d] bf16 compensated queries (kv_rotate_qk output), row r of
+ *            sequence b for cu_rows[b] <= r < cu_rows[b+1] (the layout of kv_append_chunk)
+ *   cu_rows  [B + 1] int32 (device): rows of sequence b; row r sits at position
+ *            p = seq_len[b] - (cu_rows[b+1] - r), i.e. the rows are the last tokens of the
+ *            sequence, in order (rows outside [cu_rows[0], cu_rows[B]) get KVQ_ERR_BOUNDS)
+ *   out      [n_rows][Hq][d] float32
+ * Row r attends causally to tokens [0, p] as the cache holds them: BF16 sink rows, INT2
+ * tokens below min(s_quant, p + 1) dequantized, BF16 ring rows from s_quant to p -- the
+ * result of kv_attn_decode for a sequence whose length were p + 1.  max_ctx bounds seq_len as
+ * for kv_attn_decode; n_rows is at most 65535 (KVQ_ERR_UNSUPPORTED beyond); workspace of
+ * kv_attn_chunk_workspace_bytes(cfg, n_rows, max_ctx) bytes, zero-filled before its first use
+ * (every call leaves its ticket counters zero).
+ * Execution: the decode kernel with one grid row per query row, so each query streams its own
+ * prefix of the cache (L2 keeps a sequence's pages between the rows that share them).
+ * Source: [WUSH] inference algorithm (mixed-precision attention over the S_sink / S_keep windows
+ * and the INT2 middle); [OSCAR] section 4 "Decoding Attention Kernel" (BF16 and INT2 segments
+ * of one attention). */
+KVQ_API size_t kv_attn_chunk_workspace_bytes(const kvq_config* cfg, int32_t n_rows, int32_t max_ctx);
+KVQ_API int kv_attn_chunk(const kvq_config* cfg, const kvq_cache* cache, const uint16_t* q_rot,
+                  const int32_t* cu_rows, int32_t n_rows, float* out, float sm_scale, int32_t max_ctx,
+                  void* workspace, size_t ws_bytes, int32_t* d_status, void* stream);
 
 /* kv_attn_decode: one decode step of GQA attention for every sequence.
  *   q_rot   [B][Hq][d] bf16 compensated queries (kv_rotate_qk output)
