@@ -425,6 +425,18 @@ def measure_chunk(args, w, run, k_new, v_new, sidx, pos, reset, stream, peak):
     for _ in range(args.warmup):
         qrun()
     t_q = _timed_avg(qrun, args.steps, stream, lambda: flush_buf.zero_())
+    # chunk attention: the last n_att rotated chunk queries of every sequence over the cache as
+    # the append left it (each row streams its own causal prefix)
+    n_att = min(128, w.n_new)
+    rows = torch.cat([qo[b * w.n_new + w.n_new - n_att:(b + 1) * w.n_new] for b in range(w.batch)]).contiguous()
+    cu_att = torch.arange(0, (w.batch + 1) * n_att, n_att, dtype=torch.int32, device=r.device)
+    out_att = torch.empty((rows.shape[0], w.n_q_heads, w.head_dim), dtype=torch.float32, device=r.device)
+    ws_att = r.chunk_workspace(rows.shape[0])
+    arun = lambda: r.attn_chunk(rows, cu_att, out_att, ws_att)
+    for _ in range(args.warmup):
+        arun()
+    t_att = _timed_avg(arun, args.steps, stream, lambda: flush_buf.zero_())
+    att_bytes = chunk_attention_bytes(w, n_att)
     if int(r.status.item()) != 0:
         raise RuntimeError(f"{w.name}: device status {int(r.status.item())} after the chunk timings")
     flops_q = 2.0 * w.head_dim * w.head_dim * cb["query_rows"]
@@ -449,8 +461,33 @@ def measure_chunk(args, w, run, k_new, v_new, sidx, pos, reset, stream, peak):
                            "frac_of_peak": round(cb["query_rotation"] / (t_q * 1e-3) / 1e9 / peak, 4),
                            "tflops": round(flops_q / (t_q * 1e-3) / 1e12, 2)},
     }
-    del qd, qo, flush_buf
+    out["chunk_attention"] = {"calls": "kv_attn_chunk", "rows": int(rows.shape[0]),
+                              "rows_per_seq": n_att, "ms": round(t_att, 5),
+                              "queries_per_s": round(rows.shape[0] / (t_att * 1e-3), 1),
+                              "prefix_bytes": att_bytes,
+                              "prefix_gbs": round(att_bytes / (t_att * 1e-3) / 1e9, 2),
+                              "bytes_basis": "each row's causal prefix of the cache (INT2 pages, BF16 rows), "
+                                             "counted once per row: the rows share pages through L2"}
+    del qd, qo, flush_buf, rows, out_att, ws_att
     return out
+
+
+def chunk_attention_bytes(w, n_att: int) -> int:
+    """Bytes the last n_att chunk queries of every sequence read (each its own causal prefix,
+    all kv heads): INT2 tokens below the post-append s_quant, BF16 sink and ring rows, q' and out."""
+    d, hkv, ng = w.head_dim, w.n_kv_heads, w.head_dim // w.group_size
+    int2_tok = 2 * (d // 4) + 4 * ng + (4 * d / w.page_size + 4 / w.page_size if w.key_axis == "channel" else 4 * ng)
+    int2_tok += 2 if w.key_l2norm else 0
+    ctx = int(w.ctx_lo)
+    L = ctx + w.n_new
+    sq = synth_sq(w, ctx)
+    total = 0.0
+    for p in range(L - n_att, L):
+        n_int2 = max(0, min(sq, p + 1) - w.s_sink)
+        n_win = min(w.s_sink, p + 1) + max(0, p + 1 - max(sq, w.s_sink))
+        total += hkv * (n_int2 * int2_tok + n_win * 4 * d + -(-n_int2 // w.page_size) * 4)
+        total += w.n_q_heads * d * (2 + 4)
+    return int(total * w.batch)
 
 
 def run_ours(args, rank: int, world: int, local_rank: int):
