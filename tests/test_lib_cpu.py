@@ -119,3 +119,42 @@ def test_status_strings(kvq):
     for code in range(0, -8, -1):
         assert kvq.kvq_status_string(code) != "unknown status"
     assert kvq.lib().kvq_version() == 100
+
+
+def test_append_chunk_validation(kvq):
+    """kv_append_chunk's host checks, before any launch (fake device addresses are never used)."""
+    c = _cfg(kvq).c()
+    fake = kvq.CCache(*([4096] * 9))
+    had = kvq.CTransform(1, 0, None, None, None)
+    dense = kvq.CTransform(0, 0, 4096, 4096, None)
+    # Hadamard keys are not fused (their exact butterflies stay on the two-call path)
+    assert kvq.lib().kv_append_chunk(ctypes.byref(c), ctypes.byref(had), 4096, 4096, 4096, 1,
+                                     ctypes.byref(fake), None, None) == -2
+    # per-channel keys are not fused either
+    cp = _cfg(kvq, key_axis=1, s_flush=16).c()
+    assert kvq.lib().kv_append_chunk(ctypes.byref(cp), ctypes.byref(dense), 4096, 4096, 4096, 1,
+                                     ctypes.byref(fake), None, None) == -2
+    # missing cu_rows, misaligned rows, negative count
+    assert kvq.lib().kv_append_chunk(ctypes.byref(c), ctypes.byref(dense), 4096, 4096, None, 1,
+                                     ctypes.byref(fake), None, None) == -1
+    assert kvq.lib().kv_append_chunk(ctypes.byref(c), ctypes.byref(dense), 4104, 4096, 4096, 1,
+                                     ctypes.byref(fake), None, None) == -1
+    assert kvq.lib().kv_append_chunk(ctypes.byref(c), ctypes.byref(dense), 4096, 4096, 4096, -1,
+                                     ctypes.byref(fake), None, None) == -1
+
+
+def test_attn_chunk_validation(kvq):
+    """kv_attn_chunk's host checks: row limit, workspace size, alignment, empty calls."""
+    c = _cfg(kvq).c()
+    fake = kvq.CCache(*([4096] * 9))
+    lib = kvq.lib()
+    need = lib.kv_attn_chunk_workspace_bytes(ctypes.byref(c), 64, 4096)
+    assert need > lib.kv_attn_workspace_bytes(ctypes.byref(c), 4096)   # 64 rows vs 2 sequences
+    assert lib.kv_attn_chunk_workspace_bytes(ctypes.byref(c), 70000, 4096) == 0
+    call = lambda q, cu, n, out, ws, nbytes: lib.kv_attn_chunk(ctypes.byref(c), ctypes.byref(fake), q, cu, n, out,
+                                                               ctypes.c_float(0.1), 4096, ws, nbytes, None, None)
+    assert call(4096, 4096, 0, 4096, None, 0) == 0                   # nothing to do
+    assert call(4096, 4096, 70000, 4096, 4096, 1 << 40) == -2        # one grid row per query row
+    assert call(4096, None, 64, 4096, 4096, 1 << 40) == -1           # no cu_rows
+    assert call(4096, 4096, 64, 4096, 4096, 16) == -7                # workspace too small
+    assert call(4104, 4096, 64, 4096, 4096, 1 << 40) == -1           # misaligned queries
