@@ -22,9 +22,11 @@
 // products with a + b <= 3 go to four fp32 accumulators by level L = a + b:
 //   y = U_i V_r sum_L 2^(-8 L) D_L + (dropped digits and truncation, bounded below),
 // and the CUDA cores combine the four levels, bound the remainder, and decide the correctly
-// rounded bf16 whenever no rounding midpoint lies within that bound; the rest (none of 4.2 M
-// outputs on the pages' key rows and matrices; non-finite and subnormal results always) are
-// recomputed exactly in double-float.
+// rounded bf16 whenever no rounding midpoint lies within that bound; the rest (about 0.2% of
+// the outputs on the chunk workload's keys: near a midpoint, tiny after cancellation, or on
+// rows with an element 16 or more binades below the row's largest; non-finite and subnormal
+// results always) are recomputed by the exact tiers of exact.cuh -- queued for the whole tile
+// and shared out over the worker warps after its last chunk, so no chunk waits for them.
 //
 // Layout (one CTA of 17 warps per SM, it holds all 512 TMEM columns):
 //   TMEM columns   0..255  the four T digit matrices, A operand (lane = output i, K packed
@@ -32,7 +34,8 @@
 //   TMEM columns 256..511  the four level accumulators D_L for a chunk of 64 rows
 //                          (lane = output i, column = row);
 //   shared memory          the three x digit matrices of a chunk (B operand, K-major,
-//                          128-byte swizzle), double-buffered; per-row metadata.
+//                          128-byte swizzle), double-buffered; per-row metadata; the
+//                          tile's queue of undecided outputs.
 // Warp 16 issues the 72 MMAs of a chunk (M = 128, N = 64, K = 16 each) as soon as the
 // chunk's digits are written and the previous chunk's sums were read; warps 0-15 read the
 // accumulators into registers at once (so the next chunk's MMAs overlap this chunk's rounding
@@ -117,19 +120,17 @@ __device__ __forceinline__ void x_slice(const RotParams& P, const RotTensor& T, 
   }
 }
 
-// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly; returns 0.
-// The queued undecided outputs of a warp ((row << 7) | output), recomputed exactly (exact.cuh);
-// returns 0.
-__device__ __noinline__ int exact_list(const uint16_t* list, int count, const UmRow* mrow, const float* tmat,
-                                       int lane) {
-  __syncwarp();
-  for (int f = 0; f < count; ++f) {
-    const int r = list[f] >> 7, o = list[f] & 127;
-    exact_output_warp(tmat + (size_t)o * kHeadDim, mrow[r].src, static_cast<uint16_t*>(mrow[r].dst), o, lane);
-  }
-  __syncwarp();
-  return 0;
-}
+// Undecided outputs of a tile, queued in the shared memory the staging of appends would use
+// and recomputed exactly (exact.cuh) after the tile's last chunk by all worker warps at once:
+// recomputing them within each chunk made every chunk wait for the warp that drew the most.
+struct XqEntry {
+  uint16_t* dst;         // destination row
+  uint32_t src_row;      // source row (row * heads + head) of the tensor
+  uint32_t o;            // output index
+};
+static_assert(sizeof(XqEntry) == 16, "XqEntry layout");
+constexpr int kUmSmemTile = 152 * 1024;                     // dynamic shared memory of this kernel
+constexpr int kXqCap = (kUmSmemTile - 1024 - kStgOff) / (int)sizeof(XqEntry);
 
 
 // One CTA per tile: P.rpc chunks of 64 (row, head) pairs that share one matrix.  Warps
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
   __shared__ __align__(8) uint64_t bar_x[2], bar_acc, bar_mma[2];
   __shared__ int tile_bad;
   __shared__ volatile int abort_sh;
+  __shared__ int xq_count;
   extern __shared__ uint8_t um_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(um_smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -150,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
     Ps = Pk;
     tile_bad = 0;
     abort_sh = 0;
+    xq_count = 0;
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(um_saddr(&bar_x[0])), "r"(kWorkers) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(um_saddr(&bar_x[1])), "r"(kWorkers) : "memory");
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(um_saddr(&bar_acc)), "r"(kWorkers) : "memory");
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
   const int c0 = (tile % tiles_per_mat) * P.rpc, nch = min(cpm, c0 + P.rpc) - c0;
   const float* tmat = T.mat + (size_t)mh * kHeadDim * kHeadDim;
   UmRow* meta = reinterpret_cast<UmRow*>(sm + kMetaOff);
-  uint16_t* list = reinterpret_cast<uint16_t*>(sm + kListOff) + (warp % kWorkers) * kList;
+  XqEntry* xq = reinterpret_cast<XqEntry*>(sm + kStgOff);
   int* ex_e = reinterpret_cast<int*>(sm + kExchOff);                           // [kParts][128]
   float* ex_s = reinterpret_cast<float*>(sm + kExchOff + kParts * 128 * 4);    // [kParts][128]
   auto xbuf = [&](int n) { return sm + (n & 1) * kXBuf; };
@@ -265,7 +268,6 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
       publish(1);
       if (nch > 2) x_prefetch(P, T, mh, c0 + 2, pairs, warp, lane, true, pre);
     }
-    int count = 0;
     for (int n = 0; n < nch; ++n) {
       if (!warp_wait(&bar_mma[n & 1], (uint32_t)((n >> 1) & 1), &abort_sh, lane)) break;
       tc_fence_after();
@@ -313,18 +315,40 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
         for (int c = 0; c < kEpiRows; ++c) {
           const bool und = (und_bits >> c) & 1u;
           const unsigned mk = __ballot_sync(0xffffffffu, und);
-          if (und) list[count + __popc(mk & ((1u << lane) - 1u))] = (uint16_t)(((kEpiRows * part + c) << 7) | i);
-          count += __popc(mk);
-          if (count > kList - 32) count = exact_list(list, count, mrow, tmat, lane);
+          if (!mk) continue;
+          int base = 0;
+          if (lane == 0) base = atomicAdd(&xq_count, __popc(mk));
+          base = __shfl_sync(0xffffffffu, base, 0);
+          const int r = kEpiRows * part + c;
+          const int pos = base + __popc(mk & ((1u << lane) - 1u));
+          if (und && pos < kXqCap)
+            xq[pos] = XqEntry{static_cast<uint16_t*>(mrow[r].dst),
+                              (uint32_t)((mrow[r].src - T.src) / kHeadDim), (uint32_t)i};
+          // beyond the queue's capacity: recomputed at once (the whole warp, one output at a time)
+          unsigned over = __ballot_sync(0xffffffffu, und && pos >= kXqCap);
+          while (over) {
+            const int l = __ffs(over) - 1;
+            over &= over - 1;
+            const int o = __shfl_sync(0xffffffffu, i, l);
+            exact_output_warp(tmat + (size_t)o * kHeadDim, mrow[r].src, static_cast<uint16_t*>(mrow[r].dst), o,
+                              lane);
+          }
         }
       }
-      count = exact_list(list, count, mrow, tmat, lane);
       // ---- digits of chunk n + 2 into chunk n's buffer (its MMAs have completed) ----
       if (n + 2 < nch) {
         x_slice(P, T, pre, xbuf(n), meta + ((n + 2) & 3) * kUmRows, warp, lane);
         publish(n + 2);
         if (n + 3 < nch) x_prefetch(P, T, mh, c0 + n + 3, pairs, warp, lane, true, pre);
       }
+    }
+    // ---- the tile's queued undecided outputs, spread over the worker warps (every worker warp
+    // meets this barrier once, also after a timeout) ----
+    asm volatile("bar.sync 1, %0;" ::"r"(kWorkers * 32) : "memory");
+    const int nq = min(xq_count, kXqCap);
+    for (int e = warp; e < nq; e += kWorkers) {
+      const XqEntry x = xq[e];
+      exact_output_warp(tmat + (size_t)x.o * kHeadDim, T.src + (size_t)x.src_row * kHeadDim, x.dst, (int)x.o, lane);
     }
   }
   tc_fence_before();
@@ -492,13 +516,13 @@ int launch_rotate_tc(RotParams P, cudaStream_t stream) {
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!(attr_done & (1ull << dev))) {
-      if (cudaFuncSetAttribute(rotate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmSmemPlain) !=
+      if (cudaFuncSetAttribute(rotate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUmSmemTile) !=
           cudaSuccess)
         return KVQ_ERR_CUDA;
       attr_done |= 1ull << dev;
     }
   }
-  return launch_pdl(rotate_tc_kernel, dim3((unsigned)P.dense_total), dim3(kThreads), (size_t)kUmSmemPlain, stream,
+  return launch_pdl(rotate_tc_kernel, dim3((unsigned)P.dense_total), dim3(kThreads), (size_t)kUmSmemTile, stream,
                     P) ==
                  cudaSuccess
              ? KVQ_OK
