@@ -241,6 +241,25 @@ __device__ __forceinline__ int exact_dot_tier2(float4 t4, float4 x4) {
   return ffb_decide(hi, lo, bnd);
 }
 
+// Tier 2 by one thread over a whole row: sum_j t_j x_j for j < 128 with t float32 (16-byte
+// aligned) and x bf16 (8-byte aligned), in order, with the same tracked bound (rigorous in any
+// order) and an exact renormalization every 16 terms (ffb_decide needs |lo| <= ulp(hi) / 2);
+// the bf16 bits, or -1 when only tier 3 can decide.  Lets a warp take 32 outputs at once.
+__device__ __forceinline__ int exact_dot_tier2_row(const float* trow, const uint16_t* xrow) {
+  float hi = 0.f, lo = 0.f, bnd = 0.f;
+#pragma unroll 4
+  for (int j = 0; j < 32; ++j) {
+    const float4 t4 = __ldg(reinterpret_cast<const float4*>(trow) + j);
+    const uint2 xr = __ldg(reinterpret_cast<const uint2*>(xrow) + j);
+    ffb_mac(hi, lo, bnd, t4.x, __uint_as_float(xr.x << 16));
+    ffb_mac(hi, lo, bnd, t4.y, __uint_as_float(xr.x & 0xffff0000u));
+    ffb_mac(hi, lo, bnd, t4.z, __uint_as_float(xr.y << 16));
+    ffb_mac(hi, lo, bnd, t4.w, __uint_as_float(xr.y & 0xffff0000u));
+    if ((j & 3) == 3) two_sum(hi, lo, hi, lo);           // exact: keeps lo below half an ulp of hi
+  }
+  return ffb_decide(hi, lo, bnd);
+}
+
 // bf16 bits of the exact sum_j t_j x_j over one warp: lane l holds terms 4l .. 4l + 3 (t float32,
 // x bf16 values held exactly as floats).  Every lane returns the result.  Tier 2 inline, tier 3
 // out of line.

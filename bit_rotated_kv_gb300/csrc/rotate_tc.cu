@@ -345,10 +345,25 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
     // ---- the tile's queued undecided outputs, spread over the worker warps (every worker warp
     // meets this barrier once, also after a timeout) ----
     asm volatile("bar.sync 1, %0;" ::"r"(kWorkers * 32) : "memory");
+    // one output per lane (tier 2 by one thread), the few it leaves undecided by the whole warp
     const int nq = min(xq_count, kXqCap);
-    for (int e = warp; e < nq; e += kWorkers) {
-      const XqEntry x = xq[e];
-      exact_output_warp(tmat + (size_t)x.o * kHeadDim, T.src + (size_t)x.src_row * kHeadDim, x.dst, (int)x.o, lane);
+    for (int e0 = 32 * warp; e0 < nq; e0 += 32 * kWorkers) {
+      const int e = e0 + lane;
+      XqEntry x{nullptr, 0u, 0u};
+      int r = 0;
+      if (e < nq) {
+        x = xq[e];
+        r = exact_dot_tier2_row(tmat + (size_t)x.o * kHeadDim, T.src + (size_t)x.src_row * kHeadDim);
+        if (r >= 0) x.dst[x.o] = (uint16_t)r;
+      }
+      unsigned und = __ballot_sync(0xffffffffu, e < nq && r < 0);
+      while (und) {
+        const int l = __ffs(und) - 1;
+        und &= und - 1;
+        uint16_t* dst = (uint16_t*)__shfl_sync(0xffffffffu, (unsigned long long)x.dst, l);
+        const uint32_t srow = __shfl_sync(0xffffffffu, x.src_row, l), o = __shfl_sync(0xffffffffu, x.o, l);
+        exact_output_warp(tmat + (size_t)o * kHeadDim, T.src + (size_t)srow * kHeadDim, dst, (int)o, lane);
+      }
     }
   }
   tc_fence_before();
