@@ -296,11 +296,12 @@ __device__ __forceinline__ uint32_t octet_or_scatter(const uint32_t (&w)[8], int
 }
 
 // l2-scale (keys with key_l2norm), quantize and store the octet's row as token tp of the
-// (page, kv head) chunk (nullptr or !valid: computed, nothing stored).  y holds channels
+// (page, kv head) chunk (nullptr or !valid: computed, nothing stored; key_axis: the page
+// layout's key-scale kind, which places the value scales).  y holds channels
 // 16 j .. 16 j + 15 (j = lane % 8) and is overwritten.  All 32 lanes call it.
 __device__ __forceinline__ void quantize_store_octet(const QuantConsts& Q, bool is_key, bool key_norm,
                                                      float (&y)[16], uint8_t* chunk, int tp, int ng, bool valid,
-                                                     int lane, int32_t* status) {
+                                                     int lane, int32_t* status, int key_axis = 0) {
   const int j = lane & 7;
   bool bad = false;
   if (key_norm) {
@@ -318,7 +319,7 @@ __device__ __forceinline__ void quantize_store_octet(const QuantConsts& Q, bool 
     divn_by_scale<16>(y, sdiv, yn);
 #pragma unroll
     for (int m = 0; m < 16; ++m) y[m] = sf == 0.0f ? 0.0f : yn[m];
-    if (valid && j == 0) reinterpret_cast<__half*>(chunk + norm_off(ng))[tp] = s16;
+    if (valid && j == 0) reinterpret_cast<__half*>(chunk + norm_off(ng, key_axis))[tp] = s16;
   }
   uint32_t c[16];
   __half2 dz;
@@ -329,8 +330,8 @@ __device__ __forceinline__ void quantize_store_octet(const QuantConsts& Q, bool 
     if (is_key) {
       *reinterpret_cast<__half2*>(chunk + k_scale_off() + (tp * ng + g) * 4) = dz;
     } else {
-      *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g)) = __low2half(dz);
-      *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g)) = __high2half(dz);
+      *reinterpret_cast<__half*>(chunk + v_delta_off(ng, tp, g, key_axis)) = __low2half(dz);
+      *reinterpret_cast<__half*>(chunk + v_zero_off(ng, tp, g, key_axis)) = __high2half(dz);
     }
   }
   uint32_t w[8];
