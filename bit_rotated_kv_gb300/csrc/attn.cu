@@ -686,13 +686,17 @@ __device__ void int2_split(const AttnParams& P, uint8_t* smem, int b, int bc, in
     // HMUL2 per group with the Delta_v pairs of the same tokens
     const uint32_t pb0 = movmatrix_trans(pack_half2(p[0], p[1]));
     const uint32_t pb1 = movmatrix_trans(pack_half2(p[2], p[3]));
-    if constexpr (MASKED) {                            // clear the dead tokens' scale data
+    if constexpr (MASKED) {
+      // clear the dead tokens' scale data: their bytes are whatever the page held before (the
+      // pool need not be initialised), and 0 * Inf or NaN would poison the products
       const uint32_t m0 = (2 * quad < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 1 < valid_tok ? 0xffff0000u : 0u);
       const uint32_t m1 = (2 * quad + 8 < valid_tok ? 0x0000ffffu : 0u) | (2 * quad + 9 < valid_tok ? 0xffff0000u : 0u);
 #pragma unroll
       for (int gi = 0; gi < NG; ++gi) { dv0[gi] &= m0; dv1[gi] &= m1; }
       zp0 &= m0;
       zp1 &= m1;
+      gd0 &= m0;
+      gd1 &= m1;
     }
     uint32_t bw[NG][2];
 #pragma unroll

@@ -71,7 +71,8 @@ def bits(t: torch.Tensor) -> np.ndarray:
 class GpuRun:
     """The workload's cache built through the library, then one measured step."""
 
-    def __init__(self, w: synth.Workload, device="cuda", attn_splits=0, ring_extra=1024, do_step=True):
+    def __init__(self, w: synth.Workload, device="cuda", attn_splits=0, ring_extra=1024, do_step=True,
+                 pool_fill=None, edit_kv=None):
         import bit_rotated_kv_gb300 as kvq
         from bit_rotated_kv_gb300.runner import DecodeRunner
         self.w = w
@@ -82,7 +83,11 @@ class GpuRun:
         self.tr, self.host_tr = device_transform(w, self.device)
         self.runner = DecodeRunner(self.cfg, self.tr, int(self.after.max()), self.device)
         self.runner.set_page_table(self.table)
+        if pool_fill is not None:       # a pool that was never cleared: every byte pool_fill
+            self.runner.cache.pages.fill_(pool_fill)
         self.k_all, self.v_all = gen_kv(w, self.lengths, self.device)
+        if edit_kv is not None:         # planted rows (inputs the generator does not draw)
+            edit_kv(self.k_all, self.v_all)
         self.q = gen_q(w, self.device)
         chunk = self.cfg.ring_cap - w.s_keep - w.s_flush
         self.runner.prefill(self.k_all, self.v_all, self.lengths, chunk)

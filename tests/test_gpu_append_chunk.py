@@ -20,7 +20,8 @@ class AppendRun:
     """A cache prefilled through the two-call path, then one step appending counts[b] rows to
     sequence b -- fused (kv_append_chunk) or not -- with its queries rotated and decoded."""
 
-    def __init__(self, w: synth.Workload, counts, fused: bool, ring_cap: int | None = None, device="cuda"):
+    def __init__(self, w: synth.Workload, counts, fused: bool, ring_cap: int | None = None, device="cuda",
+                 edit_kv=None):
         import bit_rotated_kv_gb300 as kvq
         from bit_rotated_kv_gb300.runner import DecodeRunner, _rows_for
         self.w = w
@@ -35,6 +36,8 @@ class AppendRun:
         self.runner = DecodeRunner(self.cfg, self.tr, int(self.after.max()), dev)
         self.runner.set_page_table(self.table)
         k_all, v_all = harness.gen_kv(w, self.lengths, dev)
+        if edit_kv is not None:
+            edit_kv(k_all, v_all)
         q = harness.gen_q(w, dev)
         self.runner.prefill(k_all, v_all, self.lengths, self.cfg.ring_cap - w.s_keep - w.s_flush)
         ib, it = _rows_for(k_all, self.lengths, self.after)

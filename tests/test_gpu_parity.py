@@ -113,6 +113,26 @@ def test_edge(name):
     _check_units(run, [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)])
 
 
+# Partial INT2 pages (S_flush = 1) in a page pool whose bytes start as 0xFF (fp16 NaN in every
+# scale slot): the flush must write each token's codes and scales whole, and the decode must
+# ignore the dead tokens' bytes of the last page, whatever they hold.
+GARBAGE = {
+    "g128": BASE.replace(s_flush=1, s_keep=20, s_sink=4, ctx_lo=203, ctx_hi=203, n_new=1),
+    "g32_gqa8": BASE.replace(s_flush=1, s_keep=12, s_sink=3, ctx_lo=250, ctx_hi=301, n_new=1, batch=2,
+                             n_q_heads=16, n_kv_heads=2, group_size=32),
+    "g64_append": BASE.replace(s_flush=1, s_keep=9, s_sink=0, ctx_lo=120, ctx_hi=170, n_new=7, batch=3,
+                               group_size=64),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GARBAGE))
+def test_uninitialised_page_pool(name):
+    w = GARBAGE[name]
+    run = harness.GpuRun(w, pool_fill=0xFF)
+    _check_units(run, [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)])
+    assert np.isfinite(run.snapshot()["out"]).all()
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])     # 64: partials beyond the one-level merge
 def test_split_count_invariance(splits):
     w = BASE.replace(ctx_lo=900, ctx_hi=900)
