@@ -1089,14 +1089,9 @@ __device__ __noinline__ void merge_global(const float* src, int n, int g, void* 
 // One kernel per (groups per row, key norms, per-channel keys) variant, so that each launch's
 // code is only its own page loop (a short loop per warp is sensitive to instruction-fetch misses).
 template <int NG, bool L2, bool KC>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const AttnParams Pk) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const __grid_constant__ AttnParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_trigger();
-  // shared-memory copy of the parameters (device functions take references to it)
-  __shared__ AttnParams Ps;
-  if (threadIdx.x == 0) Ps = Pk;
-  __syncthreads();
-  const AttnParams& P = Ps;
   // (each branch below waits for the producer kernels itself, after its independent loads)
   // split index slowest: every unit's first INT2 split (always full) is dispatched before the
   // later, partly empty ones and the short window splits (longest work first)

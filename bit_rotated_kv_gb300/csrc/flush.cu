@@ -203,13 +203,10 @@ __device__ __forceinline__ void flush_publish(const FlushParams& P, int b, int s
   if (P.cu_rows) P.seq_len[b] = L_new;
 }
 
-__global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
-  // shared-memory copy of the parameters (see rotate_kernel)
+// The parameter block is a grid constant: device functions read it by reference, with
+// run-time indices, straight from the launch's parameter space (no per-CTA copy).
+__global__ void __launch_bounds__(256, 3) flush_kernel(const __grid_constant__ FlushParams P) {
   pdl_trigger();
-  __shared__ FlushParams Ps;
-  if (threadIdx.x == 0) Ps = Pk;
-  __syncthreads();
-  const FlushParams& P = Ps;
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   {
@@ -233,6 +230,10 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
   const int L = P.seq_len[b], sq = P.s_quant[b];
   int n, n_adv, L_new;
   flush_span(P, b, L, sq, lane == 0 && warp == 0, n, n_adv, L_new);
+  // Nothing to quantize or publish this step (every CTA of the sequence derives that from the
+  // same L and s_quant, so the whole CTA leaves here): a decode step's grid is sized for the
+  // largest flush, and most steps flush nothing.
+  if (n_adv == 0 && L_new == L) return;
   // Every warp has read s_quant once the CTA passes this barrier.  A single CTA publishes the
   // new value at once (later kernels read it only after this grid completes); otherwise each
   // CTA takes a ticket now -- a release atomic whose result is only needed at the end, so its
@@ -392,12 +393,8 @@ __global__ void __launch_bounds__(256, 3) flush_kernel(const FlushParams Pk) {
 // Runs before the value flush of the same call, which publishes s_quant: both see the same
 // span.  Source: OScaR reading note, "背景：KIVI 与逐通道量化范式" (Delta_{j,g}, z_{j,g} over a
 // block of tokens) and the algorithm's key processing (l2-scaled keys quantized per channel).
-__global__ void __launch_bounds__(128) flush_keys_channel_kernel(const FlushParams Pk) {
+__global__ void __launch_bounds__(128) flush_keys_channel_kernel(const __grid_constant__ FlushParams P) {
   pdl_trigger();
-  __shared__ FlushParams Ps;
-  if (threadIdx.x == 0) Ps = Pk;
-  __syncthreads();
-  const FlushParams& P = Ps;
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   pdl_wait();
@@ -693,12 +690,8 @@ __device__ __forceinline__ void quant_row8(const QuantConsts& Q, const float (&y
   dz = __halves2half2(d16, z16);
 }
 
-__global__ void __launch_bounds__(256, 3) flush_kernel2(const FlushParams Pk) {
+__global__ void __launch_bounds__(256, 3) flush_kernel2(const __grid_constant__ FlushParams P) {
   pdl_trigger();
-  __shared__ FlushParams Ps;
-  if (threadIdx.x == 0) Ps = Pk;
-  __syncthreads();
-  const FlushParams& P = Ps;
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int hr = lane >> 4, hl = lane & 15;
@@ -718,6 +711,7 @@ __global__ void __launch_bounds__(256, 3) flush_kernel2(const FlushParams Pk) {
   const int L = P.seq_len[b], sq = P.s_quant[b];
   int n, n_adv, L_new;
   flush_span(P, b, L, sq, lane == 0 && warp == 0, n, n_adv, L_new);
+  if (n_adv == 0 && L_new == L) return;                 // nothing to do (see flush_kernel)
   __syncthreads();
   int ticket = -1;
   if (threadIdx.x == 0) {
@@ -963,15 +957,19 @@ static FlushParams flush_params(const kvq_config* cfg, const kvq_cache* cache, i
   return P;
 }
 
-// Work items are (token, kv head, K|V) rows, one warp each, over `grid_tokens` tokens per
-// sequence.  Decode-sized flushes: CTAs of 4 warps with one item per warp, spread over many
-// SMs so the flush costs about one row's latency.  Prefill-sized flushes: CTAs of 8 warps,
-// enough items per warp to fill one wave of the GPU, each warp prefetching its next row and
-// taking two rows at a time.  The last CTA of a sequence publishes s_quant.
+// Work items are (token, kv head, K|V) rows over `grid_tokens` tokens per sequence.
+// Decode-sized flushes: CTAs of 4 warps, one item per warp while that fits one wave of 16 warps
+// per SM, spread over many SMs so the flush costs about one row's latency; a grid sized for a
+// large S_flush (which flushes on few steps and finds nothing to do on the others) gives each
+// warp several items instead, so that the empty launches stay one short wave.  Prefill-sized
+// flushes: CTAs of 8 warps, enough items per warp to fill one wave of the GPU, each warp
+// prefetching its next row and taking two rows at a time.  The last CTA of a sequence
+// publishes s_quant.
 static int launch_flush_grid(FlushParams& P, const kvq_config* cfg, int grid_tokens, cudaStream_t stream) {
   const long long items = 2LL * grid_tokens * cfg->n_kv_heads;
   const long long total = items * cfg->batch;
-  int threads = 128, ipw = 1;
+  int threads = 128;
+  int ipw = (int)std::max(1LL, (total + kSms * 16LL - 1) / (kSms * 16LL));
   if (total > 4LL * kSms * 16) {
     threads = 256;
     const long long slots = (long long)kSms * 3 * (threads / 32);   // 3 resident CTAs per SM (<= 85 registers)

@@ -307,15 +307,12 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
 // kMulti: dense tiles span several row chunks (prefill-sized calls); decode-sized calls use
 // the single-chunk instantiation, whose smaller register footprint leaves room on the SMs for
 // the next kernels of the step to start early.
+// The parameter block is a grid constant: device functions take references to it and index
+// its arrays at run time, reading the launch's parameter space directly (no per-CTA copy and no
+// barrier before the first load).
 template <bool kMulti>
-__global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
-  // Work on a shared-memory copy of the parameters: device functions take references and
-  // index arrays of the struct at run time, which must never address the parameter space.
+__global__ void __launch_bounds__(256) rotate_kernel(const __grid_constant__ RotParams P) {
   pdl_trigger();
-  __shared__ RotParams Ps;
-  if (threadIdx.x == 0) Ps = Pk;
-  __syncthreads();
-  const RotParams& P = Ps;
   int blk = blockIdx.x;
   // each path waits for the producer kernels itself, after loading the caller's inputs
   if (blk < P.dense_total) {
@@ -341,12 +338,8 @@ __global__ void __launch_bounds__(256) rotate_kernel(const RotParams Pk) {
 // copies-only instantiation (kWht = false: no Walsh-Hadamard rows in the call) leaves out the
 // Hadamard path's bounds and exact recomputation as well.
 template <bool kWht>
-__global__ void __launch_bounds__(256, kWht ? 4 : 6) rotate_items_kernel(const RotParams Pk) {
+__global__ void __launch_bounds__(256, kWht ? 4 : 6) rotate_items_kernel(const __grid_constant__ RotParams P) {
   pdl_trigger();
-  __shared__ RotParams Ps;
-  if (threadIdx.x == 0) Ps = Pk;
-  __syncthreads();
-  const RotParams& P = Ps;
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (w >= P.warp_total) {
     pdl_wait();

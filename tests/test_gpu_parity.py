@@ -95,6 +95,10 @@ EDGES = {
     "identity": BASE.replace(transform="identity", value_transform="identity"),
     "invertible": BASE.replace(transform="invertible", value_transform="identity"),
     "append_100": BASE.replace(n_new=100, ctx_lo=300, ctx_hi=300),
+    # the step's decode-size flush quantizes 32 tokens of 8 sequences x 8 kv heads: 4096 rows,
+    # two per warp of the 4-warp flush CTAs (303 - 16 - 64 = 6 * 32 + 31: one more token flushes)
+    "flush_two_rows_per_warp": BASE.replace(batch=8, n_q_heads=32, n_kv_heads=8, s_keep=64, s_flush=32,
+                                            ctx_lo=303, ctx_hi=303, n_new=1),
     "degenerate_rows": BASE.replace(key_dist="degenerate", group_size=32),
     "degenerate_rows_l2": BASE.replace(key_dist="degenerate", group_size=32, key_l2norm=True, kappa_k=1.0),
     "oscar_window_64_256": BASE.replace(s_sink=64, s_keep=256, ctx_lo=700, ctx_hi=700),
