@@ -14,8 +14,9 @@
 // within that bound of a midpoint, an exact fixed-point sum).  The matrices stay L2-resident
 // across decode steps.
 // The Hadamard transform is a warp-wide butterfly (two in-thread stages, five shuffle
-// stages) in double-float with an error bound, then one scaling by 1/sqrt(d); outputs the
-// bound leaves undecided are recomputed exactly (exact.cuh).
+// stages): in exact int64 arithmetic when the row's elements span fewer than 32 binades (the
+// usual case), else in double-float with an error bound; then one scaling by 1/sqrt(d) with a
+// bound, and outputs the bound leaves undecided are recomputed exactly (exact.cuh).
 #include "rotate.cuh"
 #include "exact.cuh"
 
@@ -190,13 +191,14 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   pdl_wait();                           // (the caller's inputs above: see dense_tile)
   uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
   if (dst == nullptr) return;
-  // S = H x in double-float (hi, lo) with a bound bd on |S - (hi + lo)| (every butterfly is a
-  // sum or difference of two such values, ffb_add).  When the row's nonzero elements span fewer
-  // than 40 binades every partial sum has at most 48 significant bits and the double-float
-  // butterflies are exact (bd = 0): that path keeps no bound.  (A partial sum of +-x_j is a
-  // multiple of the smallest element's last place, 2^(emin - 7), below 2^(emax + 8): at most
-  // span + 15 <= 46 bits, which hi + lo holds, and each rounding inside a two-sum
-  // addition is then exact.)
+  // S = H x.  Two ways, both ending in (hi, lo) with |S - (hi + lo)| <= bd (times the scale sc):
+  // * every nonzero element a normal bf16 of exponent E >= 9 and the row spanning fewer than 32
+  //   binades: x_j = I_j 2^(emin - 134) with the integer I_j = +-M_j << (E_j - emin) (M the 8-bit
+  //   significand), |I_j| < 2^39, so every partial sum of the butterflies is an integer below
+  //   2^46 and exact in int64; then hi = RN(S), lo = S - hi exactly (at most 22 bits remain), bd
+  //   = 0, and the scale sc = 2^(emin - 134) is applied after the product with 1/sqrt(128);
+  // * otherwise double-float butterflies, each a sum or difference of two such values with its
+  //   bound (ffb_add), at the row's own scale (sc = 1).
   float hi[4], lo[4], bd[4];
   hi[0] = __uint_as_float(raw.x << 16);
   hi[1] = __uint_as_float(raw.x & 0xffff0000u);
@@ -215,17 +217,25 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   }
   emax = __reduce_max_sync(0xffffffffu, emax);
   emin = __reduce_min_sync(0xffffffffu, emin);
-  if (emax < emin + 32u) {
-    // exact butterflies (every partial sum fits hi + lo; the bound part of ffb_add is unused)
+  const bool int_path = emax < emin + 32u && emin >= 9u;
+  float sc = 1.0f;
+  if (int_path) {
+    long long I[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t b16 = __float_as_uint(hi[m]) >> 16;
+      const uint32_t E = (b16 >> 7) & 0xffu;
+      const long long mag = (b16 & 0x7fffu) ? (long long)((b16 & 0x7fu) | 0x80u) << (E - emin) : 0LL;
+      I[m] = (b16 & 0x8000u) ? -mag : mag;
+    }
 #pragma unroll
     for (int st = 1; st <= 2; st <<= 1) {
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         if (m & st) continue;
-        const float ah = hi[m], al = lo[m], bh = hi[m + st], bl = lo[m + st];
-        float unused;
-        ffb_add(ah, al, 0.f, bh, bl, 0.f, hi[m], lo[m], unused);
-        ffb_add(ah, al, 0.f, -bh, -bl, 0.f, hi[m + st], lo[m + st], unused);
+        const long long u = I[m], v = I[m + st];
+        I[m] = u + v;
+        I[m + st] = u - v;
       }
     }
 #pragma unroll
@@ -233,13 +243,16 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
       const bool upper = (lane & ls) != 0;
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const float ph = __shfl_xor_sync(0xffffffffu, hi[m], ls);
-        const float pl = __shfl_xor_sync(0xffffffffu, lo[m], ls);
-        float unused;
-        if (upper) ffb_add(ph, pl, 0.f, -hi[m], -lo[m], 0.f, hi[m], lo[m], unused);
-        else       ffb_add(hi[m], lo[m], 0.f, ph, pl, 0.f, hi[m], lo[m], unused);
+        const long long pv = __shfl_xor_sync(0xffffffffu, I[m], ls);
+        I[m] = upper ? pv - I[m] : I[m] + pv;                 // a - b (b is mine) / a + b (a is mine)
       }
     }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      hi[m] = __ll2float_rn(I[m]);
+      lo[m] = __ll2float_rn(I[m] - __float2ll_rn(hi[m]));       // hi is an integer: exact
+    }
+    sc = __uint_as_float((emin - 7u) << 23);                  // 2^(emin - 134), a normal float
   } else {
   // in-thread stages: stride 1 then stride 2
 #pragma unroll
@@ -283,8 +296,14 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
     const float e4 = __fadd_rn(e0, e3);
     float yh, yl;
     two_sum(p, e4, yh, yl);
-    const float by = bd[m] * 0.08838835f + (fabsf(hi[m]) + fabsf(lo[m])) * 0x1p-51f + fabsf(lo[m] * cl) +
-                     kU * (fabsf(e1) + fabsf(e2) + fabsf(e3) + fabsf(e4));
+    float by = bd[m] * 0.08838835f + (fabsf(hi[m]) + fabsf(lo[m])) * 0x1p-51f + fabsf(lo[m] * cl) +
+               kU * (fabsf(e1) + fabsf(e2) + fabsf(e3) + fabsf(e4));
+    // the row's scale (a power of two: exact unless the result is a float subnormal, whose
+    // rounding the decision's absolute margin covers; beyond the float range it is infinite,
+    // as is the bf16 result)
+    yh *= sc;
+    yl *= sc;
+    by *= sc;
     int r;
     if (hi[m] == 0.f && lo[m] == 0.f && bd[m] == 0.f) r = 0;             // S exactly zero: +0
     else r = ffb_decide(yh, yl, by);

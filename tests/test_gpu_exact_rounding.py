@@ -141,29 +141,32 @@ def test_dense_near_midpoint_tensor_core_size():
     _compare(_run_queries(x, tkit), _oracle(x, tkit))
 
 
-def _hadamard_rows(n):
-    """Rows whose output 0, S / sqrt(128) with S = sum of the row, lies within ~2^-60 of a
-    midpoint m: S = K 2^-56 with K the integer nearest m sqrt(128) 2^56, split into 8-bit
-    chunks (each an exact bf16)."""
+def _hadamard_rows(n, chunks=8):
+    """Rows whose output 0, S / sqrt(128) with S = sum of the row, lies within ~2^-(8 chunks + 4)
+    of a midpoint m: S = K 2^-(8 chunks) with K the integer nearest m sqrt(128) 2^(8 chunks),
+    split into 8-bit chunks (each an exact bf16).  8 chunks span 56 binades (the double-float
+    path with its bound); 4 span fewer than 32 (the integer path)."""
     getcontext().prec = 60
     sqrt128 = Decimal(128).sqrt()
+    nb = 8 * chunks
     x = np.zeros((n, HKV, 128), np.float64)
     for r in range(n):
         for h in range(HKV):
             k = (r * HKV + h) % 128
             m = Decimal(1) + Decimal(2 * k + 1) / Decimal(256)
-            K = int((m * sqrt128 * (Decimal(2) ** 56)).to_integral_value())
+            K = int((m * sqrt128 * (Decimal(2) ** nb)).to_integral_value())
             s = [0, -50, 30][(r + h) % 3]
             sign = -1.0 if (r + h) % 2 else 1.0
-            for c in range(8):
+            for c in range(chunks):
                 chunk = (K >> (8 * c)) & 0xFF
-                x[r, h, 3 + 7 * c] = sign * chunk * 2.0 ** (8 * c - 56 + s)
+                x[r, h, 3 + 7 * c] = sign * chunk * 2.0 ** (8 * c - nb + s)
     return synth.f32_to_bf16_bits(x.astype(np.float32))
 
 
 @pytest.mark.gpu
-def test_hadamard_near_midpoint():
-    x = _hadamard_rows(12)
+@pytest.mark.parametrize("chunks", [8, 4])
+def test_hadamard_near_midpoint(chunks):
+    x = _hadamard_rows(12, chunks)
     # the chunks are exact bf16 values (8-bit integers times powers of two)
     assert np.array_equal(synth.f32_to_bf16_bits(synth.bf16_bits_to_f32(x)), x)
     _compare(_run_queries(x, None, hadamard=True), _oracle(x, None, hadamard=True))
