@@ -79,8 +79,8 @@ struct AttnParams {
   int seqs;
 };
 
-// Cache sequence of grid row b (-1: a chunk row outside cu_rows).  cu_rows is a caller input,
-// read before the dependency wait.
+// Cache sequence of grid row b (-1: a chunk row outside cu_rows).  cu_rows is a per-call input:
+// chunk launches read it only after the dependency wait.
 __device__ __forceinline__ int attn_seq(const AttnParams& P, int b) {
   if (!P.cu_rows) return b;
   if (b < __ldg(P.cu_rows) || b >= __ldg(P.cu_rows + P.seqs)) return -1;
@@ -1097,6 +1097,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) attn_decode_kernel(const
   // later, partly empty ones and the short window splits (longest work first)
   const int split = blockIdx.z, h = blockIdx.x, b = blockIdx.y;
   const int g = P.gqa;
+  if (P.cu_rows) pdl_wait();          // (the rows' sequences: see attn_seq)
   const int bc = attn_seq(P, b);
   if (bc < 0 && threadIdx.x == 0 && split == 0 && h == 0) set_status(P.status, KVQ_ERR_BOUNDS);
   // per-warp results: an INT2 warp writes into its own (drained) page ring, a window warp

@@ -27,7 +27,7 @@ namespace kvq {
 namespace {
 
 // The rows of chunk `chunk` of this warp, loaded ahead of slicing, with their sequence (from
-// cu_rows, a caller input: safe before the dependency wait).
+// cu_rows; called after the dependency wait: the caller's last kernel may be writing them).
 __device__ __forceinline__ void x_prefetch_append(const RotParams& P, const RotTensor& T, int mh, int chunk,
                                                   int pairs, int warp, int lane, XPre& pre) {
   const int p0 = chunk * kUmRows, np = min(kUmRows, pairs - p0);
@@ -216,13 +216,12 @@ __global__ void __launch_bounds__(kThreads, 1) append_tc_kernel(const RotParams 
   float* ex_s = reinterpret_cast<float*>(sm + kExchOff + kParts * 128 * 4);    // [kParts][128]
   auto xbuf = [&](int n) { return sm + (n & 1) * kXBuf; };
 
-  // ---- the matrix (a caller input: before the dependency wait) ----
+  // ---- the matrix (configuration: before the dependency wait) ----
   XPre pre;
   int e_i = 1, tnz = 0;
   float st16 = 0.f;
   const float* trow = tmat + (size_t)i * kHeadDim + kTSpan * part;
   if (worker) {
-    x_prefetch_append(P, T, mh, c0, pairs, warp, lane, pre);
     int e = 1, nz = 0, bad = 0;
 #pragma unroll 4
     for (int j4 = 0; j4 < kTSpan / 4; ++j4) {
@@ -289,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) append_tc_kernel(const RotParams 
       __syncwarp();
       if (lane == 0) um_arrive(&bar_x[n & 1]);
     };
+    x_prefetch_append(P, T, mh, c0, pairs, warp, lane, pre);
     x_slice_append(P, T, pre, xbuf(0), meta, warp, lane);
     publish(0);
     if (nch > 1) {

@@ -72,16 +72,17 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
       xr = reinterpret_cast<const uint4*>(T.src + ((size_t)row * T.heads + head) * kHeadDim)[xpart];
     }
   };
-  load_chunk(c0);
-  // the matrix, once per tile: thread 2i + half keeps T[mh][i][64 half .. 64 half + 63]
+  // the matrix, once per tile: thread 2i + half keeps T[mh][i][64 half .. 64 half + 63].  A
+  // transform is configuration, read before the dependency wait (it overlaps the kernel before
+  // this one on the stream); the call's rows, sequences and positions come after it -- the
+  // caller's last kernel may still be writing them -- and so does the cache state
   const float* mrow = T.mat + ((size_t)mh * kHeadDim + i) * kHeadDim;
   const float4* m4 = reinterpret_cast<const float4*>(mrow + 64 * half);
   float4 m[16];
 #pragma unroll
   for (int j4 = 0; j4 < 16; ++j4) m[j4] = m4[j4];
-  // everything above reads only the caller's inputs, which the kernels of this library never
-  // write: it overlaps the producer kernel; the cache state (s_quant, seq_len) comes after
   pdl_wait();
+  load_chunk(c0);
   for (int c = c0; c < c1; ++c) {
     const int np = min(P.rt, pairs - c * P.rt);
     if (tid < np) dst_sh[tid] = rot_dst(P, T, d_row, d_head, d_b, d_p, true);
@@ -152,6 +153,7 @@ __device__ void warp_copies(const RotParams& P, int tt, int witem, int lane) {
     kh -= T.heads;
     ++krow;
   }
+  pdl_wait();                           // the call's rows and positions: after the wait
   int kb = 0, kp = 0;
   if (lane < n && !T.is_query) {
     kb = P.seq_idx[krow];
@@ -166,7 +168,6 @@ __device__ void warp_copies(const RotParams& P, int tt, int witem, int lane) {
       raw[k] = reinterpret_cast<const uint2*>(T.src + ((size_t)rk * T.heads + hk) * kHeadDim)[lane];
     }
   }
-  pdl_wait();                           // (the caller's inputs above: see dense_tile)
   uint16_t* dst = lane < n ? rot_dst(P, T, krow, kh, kb, kp, true) : nullptr;
 #pragma unroll
   for (int k = 0; k < kMaxRPW; ++k) {
@@ -181,6 +182,7 @@ __device__ void warp_copies(const RotParams& P, int tt, int witem, int lane) {
 __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   const RotTensor& T = P.t[tt];
   int row = item / T.heads, h = item % T.heads;
+  pdl_wait();                           // the call's rows and positions: after the wait
   int b = 0, p = 0;
   if (!T.is_query) {
     b = P.seq_idx[row];
@@ -188,7 +190,6 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   }
   const uint16_t* src = T.src + ((size_t)row * T.heads + h) * kHeadDim;
   uint2 raw = *reinterpret_cast<const uint2*>(src + 4 * lane);
-  pdl_wait();                           // (the caller's inputs above: see dense_tile)
   uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
   if (dst == nullptr) return;
   // S = H x.  Two ways, both ending in (hi, lo) with |S - (hi + lo)| <= bd (times the scale sc):
@@ -333,7 +334,7 @@ template <bool kMulti>
 __global__ void __launch_bounds__(256) rotate_kernel(const __grid_constant__ RotParams P) {
   pdl_trigger();
   int blk = blockIdx.x;
-  // each path waits for the producer kernels itself, after loading the caller's inputs
+  // each path waits for the kernel before it itself (a dense tile after loading its matrix)
   if (blk < P.dense_total) {
     int tt, item;
     find_item(P.n_dense, blk, tt, item);

@@ -187,13 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
   float* ex_s = reinterpret_cast<float*>(sm + kExchOff + kParts * 128 * 4);    // [kParts][128]
   auto xbuf = [&](int n) { return sm + (n & 1) * kXBuf; };
 
-  // ---- the matrix (a caller input: before the dependency wait) ----
+  // ---- the matrix (configuration: before the dependency wait; the call's rows, sequences and
+  // positions only after it, as the caller's last kernel may still be writing them) ----
   XPre pre;
   int e_i = 1, tnz = 0;
   float st16 = 0.f;
   const float* trow = tmat + (size_t)i * kHeadDim + kTSpan * part;
   if (worker) {
-    x_prefetch(P, T, mh, c0, pairs, warp, lane, false, pre);
     int e = 1, nz = 0, bad = 0;
 #pragma unroll 4
     for (int j4 = 0; j4 < kTSpan / 4; ++j4) {
@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) rotate_tc_kernel(const RotParams 
       __syncwarp();
       if (lane == 0) um_arrive(&bar_x[n & 1]);
     };
+    x_prefetch(P, T, mh, c0, pairs, warp, lane, true, pre);
     x_slice(P, T, pre, xbuf(0), meta, warp, lane);
     publish(0);
     if (nch > 1) {

@@ -44,15 +44,13 @@
  *     unit of work is skipped and the first such code is stored into
  *     *d_status (a device int32 the caller zeroes and reads when it likes).
  *   - Overlap between consecutive calls: every kernel lets the next kernel of the
- *     stream begin early (programmatic dependent launch) and waits for its
- *     predecessor's results before it touches the cache state.  Before that wait a
- *     kernel may already read inputs that no call of this library writes:
- *     kv_rotate_qk reads q, k, v, seq_idx, pos and the transform matrices,
- *     kv_append_chunk k, v, cu_rows and the matrices, and kv_attn_decode the
- *     page table.  These must therefore be complete before the
- *     call is made -- the usual case (written by the host, or by a kernel that
- *     finished before the call): only a kernel that itself triggers programmatic
- *     dependent launch and writes them afterwards would violate it.
+ *     stream begin early (programmatic dependent launch) and waits for the kernel
+ *     before it -- the caller's or this library's -- to complete before it reads a
+ *     per-call input (q, k, v, seq_idx, pos, cu_rows) or touches the cache state.
+ *     Configuration is read before that wait: the transform matrices (kv_rotate_qk,
+ *     kv_append_chunk) and the page table (kv_attn_decode, kv_attn_chunk).  These
+ *     must not be written by the kernel launched immediately before the call on
+ *     the same stream; a copy, or any earlier kernel, may write them.
  *
  * Supported shapes: head_dim 128; page_size 16; group_size 32, 64 or 128;
  * GQA ratio Hq/Hkv in {1, 2, 4, 8}; 2-bit codes.
