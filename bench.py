@@ -208,7 +208,7 @@ def measure_config(args, w: synth.Workload, rank: int, world: int, local_rank: i
 
     dev = torch.device("cuda", local_rank)
     # the realistic ring capacity (S_keep + S_flush + n_new): window splits are sized by it
-    run = harness.GpuRun(w, device=dev, do_step=False, ring_extra=0, attn_splits=args.splits)
+    run = harness.DeviceRun(w, device=dev, do_step=False, ring_extra=0, attn_splits=args.splits)
     r = run.runner
     stream = torch.cuda.current_stream()
     seq0, sq0 = r.cache.seq_len.clone(), r.cache.s_quant.clone()
@@ -493,15 +493,15 @@ def chunk_attention_bytes(w, n_att: int) -> int:
 def run_ours(args, rank: int, world: int, local_rank: int):
     import torch
     torch.cuda.set_device(torch.device("cuda", local_rank))
-    configs = [int(c) for c in str(args.configs).split(",") if c.strip()] if args.configs else [args.config]
-    head = measure_config(args, workload(args, configs[0]), rank, world, local_rank, True)
+    chosen = [int(c) for c in str(args.configs).split(",") if c.strip()] if args.configs else [args.config]
+    head = measure_config(args, workload(args, chosen[0]), rank, world, local_rank, True)
     res = {"metric": METRIC, "value": head.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "int2 codes x f16 tensor-core MMA, f32 accumulate",
            "data": "synthetic (seeded; shapes of the pages' Qwen3 workloads, random transforms)"}
     res.update(head)
     subs = {}
-    for c in configs[1:]:
+    for c in chosen[1:]:
         sub = measure_config(args, workload(args, c), rank, world, local_rank, False)
         subs[sub["config"]["workload"]] = sub
     if subs:

@@ -68,7 +68,7 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-class GpuRun:
+class DeviceRun:
     """The workload's cache built through the library, then one measured step."""
 
     def __init__(self, w: synth.Workload, device="cuda", attn_splits=0, ring_extra=1024, do_step=True,

@@ -15,7 +15,7 @@ def oracle_unit(w: synth.Workload, b: int, h: int, lengths, host_tr):
     return pipeline.run_unit(w, ui, tk, tkit, tv)
 
 
-def compare_unit(run: GpuRun, snap: dict, b: int, h: int) -> dict:
+def compare_unit(run: DeviceRun, snap: dict, b: int, h: int) -> dict:
     """Element-wise comparison of one (sequence, kv head) with the oracle."""
     w = run.w
     ref = oracle_unit(w, b, h, run.lengths, run.host_tr)

@@ -20,7 +20,7 @@ def _run(w, counts):
     """Prefill, append counts[b] rows per sequence (two calls), rotate the chunk queries and run
     kv_attn_chunk.  Returns (run, q' bits [rows, Hq, d], out [rows, Hq, d], raw chunk q bits)."""
     from bit_rotated_kv_gb300.runner import _rows_for
-    run = harness.GpuRun(w, do_step=False)
+    run = harness.DeviceRun(w, do_step=False)
     r = run.runner
     counts = np.asarray(counts)
     ib, it = _rows_for(run.k_all, run.lengths, run.lengths + counts)

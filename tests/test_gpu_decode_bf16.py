@@ -29,7 +29,7 @@ def _round_bf16(x: np.ndarray) -> np.ndarray:
                          ids=["tiny", "g64_ragged_gqa8", "l2_hadamard_g32"])
 def test_bf16_output_is_rounded_float32_output(w):
     import bit_rotated_kv_gb300 as kvq
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     r = run.runner
     snap = run.snapshot()
     assert snap["status"] == 0
@@ -53,7 +53,7 @@ def test_bf16_output_is_rounded_float32_output(w):
 def test_bf16_output_rejects_misaligned_out():
     import bit_rotated_kv_gb300 as kvq
     w = synth.TINY_GQA4
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     r = run.runner
     buf = torch.zeros(r.out.numel() + 8, dtype=torch.bfloat16, device=r.device)
     bad = buf[1:1 + r.out.numel()].view(r.out.shape)         # 2-byte aligned only

@@ -71,7 +71,7 @@ def test_nonfinite_scales_reported(name):
     for big, expect in ((OVER, KVQ_ERR_NONFINITE), (FINITE, 0)):
         flagged = _oracle_block_flag(big, kappa) if block else _oracle_token_flag(big, kappa, w.group_size)
         assert flagged == (expect != 0), (big, flagged)
-        run = harness.GpuRun(w, do_step=False, edit_kv=_plant(tokens, big, which, alternate=block))
+        run = harness.DeviceRun(w, do_step=False, edit_kv=_plant(tokens, big, which, alternate=block))
         assert run.status_prefill == expect, (name, big, run.status_prefill)
 
 

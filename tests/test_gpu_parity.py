@@ -45,33 +45,33 @@ def _check_units(run, units):
     return worst
 
 
-def test_config1_full():
+def test_tiny_gqa4_full():
     w = synth.TINY_GQA4
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     _check_units(run, [(0, 0)])
 
 
-def test_config2_full():
+def test_qwen3_8b_ctx32k_full():
     w = synth.QWEN3_8B_32K
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     _check_units(run, [(0, h) for h in range(w.n_kv_heads)])
 
 
-def test_config3_sampled():
+def test_qwen3_4b_b64_sampled():
     w = synth.QWEN3_4B_B64
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     _check_units(run, harness.units_sample(w, 10, seed=3))
 
 
-def test_config4_sampled():
+def test_qwen3_32b_ctx128k_sampled():
     w = synth.QWEN3_32B_128K
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     _check_units(run, harness.units_sample(w, 5, seed=4))
 
 
-def test_config5_sampled():
+def test_wush_chunk2048_sampled():
     w = synth.WUSH_CHUNK_B16
-    run = harness.GpuRun(w, ring_extra=2048)
+    run = harness.DeviceRun(w, ring_extra=2048)
     _check_units(run, harness.units_sample(w, 5, seed=5))
 
 
@@ -113,7 +113,7 @@ EDGES = {
 @pytest.mark.parametrize("name", sorted(EDGES))
 def test_edge(name):
     w = EDGES[name]
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     _check_units(run, [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)])
 
 
@@ -132,7 +132,7 @@ GARBAGE = {
 @pytest.mark.parametrize("name", sorted(GARBAGE))
 def test_uninitialised_page_pool(name):
     w = GARBAGE[name]
-    run = harness.GpuRun(w, pool_fill=0xFF)
+    run = harness.DeviceRun(w, pool_fill=0xFF)
     _check_units(run, [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)])
     assert np.isfinite(run.snapshot()["out"]).all()
 
@@ -140,8 +140,8 @@ def test_uninitialised_page_pool(name):
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])     # 64: partials beyond the one-level merge
 def test_split_count_invariance(splits):
     w = BASE.replace(ctx_lo=900, ctx_hi=900)
-    ref = harness.GpuRun(w, attn_splits=1).snapshot()["out"]
-    run = harness.GpuRun(w, attn_splits=splits)
+    ref = harness.DeviceRun(w, attn_splits=1).snapshot()["out"]
+    run = harness.DeviceRun(w, attn_splits=splits)
     out = run.snapshot()["out"]
     rel = np.abs(out - ref).max() / np.abs(ref).max()
     # different splits see different running maxima, so P * Delta_v is rounded to fp16 at
@@ -178,7 +178,7 @@ def test_chunk_query_rotation():
 
 def test_bad_page_id_sets_status_without_fault():
     w = BASE.replace(ctx_lo=400, ctx_hi=400)
-    run = harness.GpuRun(w, do_step=False)
+    run = harness.DeviceRun(w, do_step=False)
     # corrupt one page-table entry of the INT2 region, then decode
     run.runner.cache.page_table[0, 3] = run.cfg.num_pages + 7
     run.runner.status.zero_()
@@ -192,7 +192,7 @@ def test_bad_page_id_sets_status_without_fault():
 
 def test_position_outside_ring_is_rejected():
     w = BASE.replace(ctx_lo=400, ctx_hi=400)
-    run = harness.GpuRun(w, do_step=False)
+    run = harness.DeviceRun(w, do_step=False)
     dev = run.device
     run.runner.status.zero_()
     k = run.k_all[0, :1].contiguous()
@@ -225,7 +225,7 @@ def test_pipelined_decode_steps_without_sync(w):
     """n_new single-token decode steps (rotate, flush, decode) launched back to back with no
     host synchronization, so each kernel overlaps its predecessor's tail; the final cache and
     the last step's attention must equal the oracle's state after the n_new tokens."""
-    run = harness.GpuRun(w, do_step=False)
+    run = harness.DeviceRun(w, do_step=False)
     r = run.runner
     steps = [r.step_inputs(run.k_all, run.v_all, run.lengths + t, 1) for t in range(w.n_new)]
     torch.cuda.synchronize()

@@ -33,15 +33,15 @@ CASES = {
 @pytest.mark.parametrize("name", sorted(CASES))
 def test_per_channel_keys(name):
     w = CASES[name]
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     _check_units(run, [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)])
 
 
 @pytest.mark.parametrize("splits", [1, 7])
 def test_per_channel_split_invariance(splits):
     w = BASE.replace(ctx_lo=900, ctx_hi=900)
-    ref = harness.GpuRun(w, attn_splits=1).snapshot()["out"]
-    run = harness.GpuRun(w, attn_splits=splits)
+    ref = harness.DeviceRun(w, attn_splits=1).snapshot()["out"]
+    run = harness.DeviceRun(w, attn_splits=splits)
     out = run.snapshot()["out"]
     assert np.abs(out - ref).max() / np.abs(ref).max() < 5e-4
     _check_units(run, [(0, 0)])

@@ -37,5 +37,5 @@ def random_workload(seed: int) -> synth.Workload:
 @pytest.mark.parametrize("seed", range(24))
 def test_random_configuration(seed):
     w = random_workload(seed)
-    run = harness.GpuRun(w)
+    run = harness.DeviceRun(w)
     _check_units(run, [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)])

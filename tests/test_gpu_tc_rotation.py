@@ -129,6 +129,6 @@ def test_hadamard_keys_with_dense_values_at_chunk_size():
     kernel: both launches of one call, through the whole step against the oracle."""
     from tests.test_gpu_parity import _check_units
     w = synth.QWEN3_32B_128K.replace(batch=1, ctx_lo=4500, ctx_hi=4500, value_transform="orthogonal")
-    run = harness.GpuRun(w, ring_extra=4096)            # prefill rotates 4096-row chunks
+    run = harness.DeviceRun(w, ring_extra=4096)            # prefill rotates 4096-row chunks
     assert 4096 * w.n_kv_heads >= TC_MIN_PAIRS
     _check_units(run, [(0, h) for h in range(w.n_kv_heads)])

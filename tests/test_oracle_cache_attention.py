@@ -31,17 +31,17 @@ def test_flush_schedule_closed_form(s_sink, s_keep, s_flush):
             assert sq <= L - s_keep
 
 
-def test_survey_cache_states():
-    # config 1: INT2 [16, 384) = 23 pages, BF16 16 + 128
+def test_cache_states_of_the_workloads():
+    # tiny-gqa4-ctx512: INT2 [16, 384) = 23 pages, BF16 16 + 128
     w = synth.TINY_GQA4
     assert pipeline.s_quant_schedule(w, 504) == (376, 384)
-    # config 2: s_quant = 32768 - 264 before, one span of 8 flushed by the step
+    # qwen3-8b-ctx32k-b1: s_quant = 32768 - 264 before, one span of 8 flushed by the step
     w = synth.QWEN3_8B_32K
     assert pipeline.s_quant_schedule(w, 32760) == (32504, 32512)
-    # config 5: INT2 [64, 16128) before, +2048 after
+    # wush-qwen3-8b-b16-chunk2048-on-16k: INT2 [64, 16128) before, +2048 after
     w = synth.WUSH_CHUNK_B16
     assert pipeline.s_quant_schedule(w, 16384) == (16128, 18176)
-    # config 4: everything INT2, one new BF16 token
+    # qwen3-32b-ctx128k-b4-oscar: everything INT2, one new BF16 token
     w = synth.QWEN3_32B_128K
     assert pipeline.s_quant_schedule(w, 131072) == (131072, 131072)
 
@@ -104,8 +104,8 @@ def test_all_bf16_when_context_fits_windows():
     assert np.allclose(r["out"], _sdpa(q, k, v, 1 / math.sqrt(128)), rtol=1e-12, atol=1e-12)
 
 
-def test_config1_end_to_end_shapes_and_accuracy():
-    """Config 1 through the oracle.  The accuracy of INT2 attention against
+def test_tiny_workload_end_to_end_shapes_and_accuracy():
+    """The tiny GQA-4 workload (512 tokens) through the oracle.  The accuracy of INT2 attention against
     unquantized attention is reported, not pinned (the pages' accuracy claims
     need trained models)."""
     w = synth.TINY_GQA4

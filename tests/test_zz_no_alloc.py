@@ -29,7 +29,7 @@ def _rel(out: torch.Tensor, ref: torch.Tensor) -> float:
 ], ids=["config1", "gqa8_b2_g64"])
 def test_noalloc_matches_workspace_entry_point_on_two_calls(w):
     import bit_rotated_kv_gb300 as kvq
-    run = harness.GpuRun(w)                 # cache built, one step decoded with a caller workspace
+    run = harness.DeviceRun(w)                 # cache built, one step decoded with a caller workspace
     r = run.runner
     torch.cuda.synchronize()
     ref = r.out.clone()
