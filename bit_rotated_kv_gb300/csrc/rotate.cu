@@ -36,6 +36,7 @@ namespace kvq {
 // Loads are issued in the order that overlaps them: the destination's sequence index and
 // position, the matrix, the rows, and only then the dependent s_quant check.
 constexpr int kMaxRT = 16;
+constexpr int kXPad = 4;
 constexpr int kMaxRPW = 8;
 template <bool kMulti>
 __device__ void dense_tile(const RotParams& P, int tt, int tile) {
@@ -46,7 +47,9 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
   const int mh = tile / tiles_per_mat;
   const int c0 = (tile % tiles_per_mat) * P.rpc;         // first chunk of this tile
   const int c1 = kMulti ? min(chunks_per_mat, c0 + P.rpc) : c0 + 1;
-  __shared__ __align__(16) float xs[kMaxRT][kHeadDim];
+  // rows as floats; the second half of a row starts 4 floats later (kXPad) so that the two
+  // half-row broadcasts of one load fall in different banks
+  __shared__ __align__(16) float xs[kMaxRT][kHeadDim + kXPad];
   __shared__ uint16_t* dst_sh[kMaxRT];
   __shared__ uint16_t fallback[kMaxRT * kHeadDim];      // (row << 7) | output, undecided outputs
   __shared__ int n_fallback;
@@ -87,7 +90,7 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
     const int np = min(P.rt, pairs - c * P.rt);
     if (tid < np) dst_sh[tid] = rot_dst(P, T, d_row, d_head, d_b, d_p, true);
     if (xrow < np) {
-      float4* xd = reinterpret_cast<float4*>(&xs[xrow][8 * xpart]);
+      float4* xd = reinterpret_cast<float4*>(&xs[xrow][8 * xpart + (xpart >= 8 ? kXPad : 0)]);
       xd[0] = make_float4(__uint_as_float(xr.x << 16), __uint_as_float(xr.x & 0xffff0000u),
                           __uint_as_float(xr.y << 16), __uint_as_float(xr.y & 0xffff0000u));
       xd[1] = make_float4(__uint_as_float(xr.z << 16), __uint_as_float(xr.z & 0xffff0000u),
@@ -99,7 +102,7 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
     for (int r = 0; r < np; ++r) {
       uint16_t* dst = dst_sh[r];
       if (dst == nullptr) continue;
-      const float* x = xs[r] + 64 * half;
+      const float* x = xs[r] + (64 + kXPad) * half;
       // four independent FMA chains of 16 terms (float4 j4 feeds chain j4 % 4), each with its
       // running sum of |partial|; then two adds inside the thread and one with the partner
       float vc[4] = {0.f, 0.f, 0.f, 0.f}, ac[4] = {0.f, 0.f, 0.f, 0.f};
@@ -130,7 +133,7 @@ __device__ void dense_tile(const RotParams& P, int tt, int tile) {
     for (int f = warp; f < n_fallback; f += (int)(blockDim.x >> 5)) {
       const int r = fallback[f] >> 7, o = fallback[f] & 127;
       const float4 t4 = reinterpret_cast<const float4*>(T.mat + ((size_t)mh * kHeadDim + o) * kHeadDim)[lane];
-      const float4 x4 = reinterpret_cast<const float4*>(xs[r])[lane];
+      const float4 x4 = reinterpret_cast<const float4*>(xs[r])[lane + (lane >= 16 ? kXPad / 4 : 0)];
       const uint32_t res = exact_dot_bf16_warp(t4, x4, lane);
       if (lane == 0) dst_sh[r][o] = (uint16_t)res;
     }
