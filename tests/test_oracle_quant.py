@@ -221,3 +221,30 @@ def test_planted_dropped_rounding_is_caught(monkeypatch):
     monkeypatch.setattr(quant, "codes_from_params", bad_codes)
     with pytest.raises(AssertionError):
         test_error_bound_unclipped(128)
+
+
+def _quest_mse(alpha, group, seed=21, rows=4000):
+    """Mean squared error of the oracle's QuEST grid on Gaussian rows, in units of each group's
+    mean square."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((rows, 128)).astype(np.float32)
+    bits = synth.f32_to_bf16_bits(x)
+    q = quant.quantize_rows(bits, group, quantizer="quest", alpha=alpha)
+    xb = synth.bf16_bits_to_f32(bits).astype(np.float64)
+    err = (xb - quant.dequantize(q)).reshape(rows, 128 // group, group)
+    ms = (xb.reshape(rows, 128 // group, group) ** 2).mean(-1, keepdims=True)
+    return float((err ** 2 / ms).mean())
+
+
+def test_quest_delta_against_the_gaussian_integral():
+    """The grid's scale is pinned by what it is for: on Gaussian groups the oracle's error (in
+    units of the group's mean square) equals the integral of the 4-level clipped grid at alpha
+    over N(0, 1) -- up to the group's own RMS estimate (1.3% at G = 128).  A grid scaled by the
+    norm over sqrt(d) instead of sqrt(G), or by alpha / 2, lands far from it."""
+    alpha = 1.4935705
+    ref = _gauss_mse(alpha)
+    assert abs(_quest_mse(alpha, 128) / ref - 1) < 0.03
+    assert 0.9 < _quest_mse(alpha, 32) / ref < 1.0           # finite-G: RMS from 32 values
+    # the same error with the grid misplaced: both far outside those bands
+    assert _quest_mse(alpha / 2, 128) / ref > 1.5
+    assert _quest_mse(alpha * 2, 128) / ref > 1.5
