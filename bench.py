@@ -502,8 +502,17 @@ def run_ours(args, rank: int, world: int, local_rank: int):
     res.update(head)
     subs = {}
     for c in chosen[1:]:
-        sub = measure_config(args, workload(args, c), rank, world, local_rank, False)
-        subs[sub["config"]["workload"]] = sub
+        wc = workload(args, c)
+        if world > 1:                   # every rank takes the same barriers: no partial records
+            sub = measure_config(args, wc, rank, world, local_rank, False)
+            subs[sub["config"]["workload"]] = sub
+            continue
+        try:
+            sub = measure_config(args, wc, rank, world, local_rank, False)
+            subs[sub["config"]["workload"]] = sub
+        except Exception as e:          # the headline record stands; the failure is reported
+            msg = str(e).strip().splitlines()
+            subs[wc.name] = {"config": {"workload": wc.name}, "error": f"{type(e).__name__}: {msg[0] if msg else ''}"}
     if subs:
         res["sub_configs"] = subs
     return res
