@@ -196,8 +196,8 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   uint16_t* dst = rot_dst(P, T, row, h, b, p, lane == 0);
   if (dst == nullptr) return;
   // S = H x.  Two ways, both ending in (hi, lo) with |S - (hi + lo)| <= bd (times the scale sc):
-  // * every nonzero element a normal bf16 of exponent E >= 9 and the row spanning fewer than 32
-  //   binades: x_j = I_j 2^(emin - 134) with the integer I_j = +-M_j << (E_j - emin) (M the 8-bit
+  // * every nonzero element a finite normal bf16 of exponent E >= 9 and the row spanning fewer
+  //   than 32 binades: x_j = I_j 2^(emin - 134) with the integer I_j = +-M_j << (E_j - emin) (M the 8-bit
   //   significand), |I_j| < 2^39, so every partial sum of the butterflies is an integer below
   //   2^46 and exact in int64; then hi = RN(S), lo = S - hi exactly (at most 22 bits remain), bd
   //   = 0, and the scale sc = 2^(emin - 134) is applied after the product with 1/sqrt(128);
@@ -221,7 +221,7 @@ __device__ void warp_item(const RotParams& P, int tt, int item, int lane) {
   }
   emax = __reduce_max_sync(0xffffffffu, emax);
   emin = __reduce_min_sync(0xffffffffu, emin);
-  const bool int_path = emax < emin + 32u && emin >= 9u;
+  const bool int_path = emax < emin + 32u && emin >= 9u && emax < 255u;   // (255: Inf / NaN)
   float sc = 1.0f;
   if (int_path) {
     long long I[4];
